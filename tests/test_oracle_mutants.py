@@ -1,0 +1,83 @@
+"""The oracle's pins must catch plausible mistakes (not gpu).
+
+Each case plants one mistake in a temporary copy of oracle.c (on the CPU, in a
+scratch directory), rebuilds it there and runs the oracle pin tests against
+the copy; the run must fail.  Mistakes: a wrong twist root, a missing output
+bit reversal, a '+' for the negacyclic '-', a lost automorphism sign, a
+Garner radix error, a non-minimal root, a missing 1/n, swapped key
+components, a wrong tensor cross term, a wrong prime step and a dropped
+Miller-Rabin round.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "twist_uses_inverse_root": (
+        "a[j] = mulmod(a[j] % q, pw, q); pw = mulmod(pw, psi, q);",
+        "a[j] = mulmod(a[j] % q, pw, q); pw = mulmod(pw, invmod(psi, q), q);"),
+    "no_output_bit_reversal": (
+        "    /* A[k] is the value at psi^(2k+1); the definition stores it at brv(k) */\n"
+        "    bit_reverse_permute(a, log_n);\n", ""),
+    "negacyclic_wrap_added": (
+        "else c[i + j - n] = submod(c[i + j - n], p, q);",
+        "else c[i + j - n] = addmod(c[i + j - n], p, q);"),
+    "automorph_sign_lost": (
+        "else out[s - n] = (q - a[t] % q) % q;",
+        "else out[s - n] = a[t] % q;"),
+    "garner_radix_wrong": (
+        "radix = mulmod(radix, d[k] % qi, qi);",
+        "radix = mulmod(radix, d[k] % qi, qi); if (k == 1) radix = mulmod(radix, 2, qi);"),
+    "psi_not_smallest": (
+        "if (cur < best) best = cur;",
+        "if (cur > best) best = cur;"),
+    "missing_n_inverse": (
+        "uint64_t n_inv = invmod(n % q, q), pw = n_inv;",
+        "uint64_t pw = 1;"),
+    "key_components_swapped": (
+        "uint64_t kv = keys[(((uint64_t)j * 2 + c) * LK + l) * n + i];",
+        "uint64_t kv = keys[(((uint64_t)j * 2 + (1 - c)) * LK + l) * n + i];"),
+    "tensor_cross_term_wrong": (
+        "d1[o] = addmod(mulmod(a0[o], b1[o], ql), mulmod(a1[o], b0[o], ql), ql);",
+        "d1[o] = addmod(mulmod(a0[o], b0[o], ql), mulmod(a1[o], b1[o], ql), ql);"),
+    "prime_scan_skips": (
+        "        c -= m;\n    }\n    return found;",
+        "        c -= 2 * m;\n    }\n    return found;"),
+    "miller_rabin_one_round": (
+        "    for (int i = 0; i < 12; i++) {\n        uint64_t x = powmod(small[i], d, n);",
+        "    for (int i = 0; i < 1; i++) {\n        uint64_t x = powmod(small[i], d, n);"),
+}
+
+PIN_FILES = ["test_oracle_primes_psi.py", "test_oracle_ntt.py", "test_oracle_automorph.py",
+             "test_oracle_keyswitch.py"]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(os.path.join(ROOT, "oracle", "oracle.c")) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    work = tmp_path / "w"
+    shutil.copytree(os.path.join(ROOT, "oracle"), work / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "*.tmp*", "__pycache__"))
+    shutil.copytree(os.path.join(ROOT, "ntt_arithmetic_gb300"), work / "ntt_arithmetic_gb300",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__", "_build", "csrc"))
+    (work / "tests").mkdir()
+    for f in PIN_FILES + ["conftest.py"]:
+        shutil.copy(os.path.join(ROOT, "tests", f), work / "tests" / f)
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), work / "tests" / "golden")
+    (work / "oracle" / "oracle.c").write_text(source.replace(old, new))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "not gpu", "-p", "no:cacheprovider",
+                        "tests"], cwd=work, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout or "error" in r.stdout.lower()
