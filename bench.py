@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched RNS-NTT hot path on GB300.
+
+One step = every kernel of the hot path once, chained on the n = 2^16, L = 24
+workload (16 polynomials = 4 pairs of 2-component ciphertexts, 201 MB of u64
+residues; key switch over 24 + 8 primes with dnum = 3):
+
+  1. fhe_ntt_fwd      X[2][4][2][24][n]           coefficient -> NTT   (384 transforms)
+                      (X[0]: the 4 ciphertexts a, X[1]: the 4 ciphertexts b)
+  2. fhe_automorph    Y = sigma_k(X)  NTT domain  k = 5^(2^(step mod 16)) mod 2n
+  3. fhe_mul_ntt      Z = X * Y
+  4. fhe_tensor       D[4][3][24][n] = tensor(Z[0], Z[1])
+  5. fhe_ntt_inv      D                           NTT -> coefficient   (288 transforms)
+  6. fhe_keyswitch_ip KS[4][2][32][n] = keyswitch(D[:, 2])  (ModUp + 384 transforms + IP)
+
+metric: NTT (poly x prime)/s = 1056 transforms per step / step time (whole
+job, inputs resident in HBM).  Per-kernel CUDA-event times give the NTT's
+achieved GB/s and the key-switch ops/s.  `--impl reference` times the CPU
+oracle on a bounded sample of the same step instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LOG_N, N, L, K, DNUM, PAIRS = 16, 1 << 16, 24, 8, 3, 4
+NPOLY = PAIRS * 2 * 2                      # 16 polynomials
+FWD_T, INV_T, KS_T = NPOLY * L, PAIRS * 3 * L, PAIRS * DNUM * (L + K)
+UNITS = FWD_T + INV_T + KS_T               # 1056 poly x prime NTTs per step
+METRIC = "NTT (poly×prime)/s and achieved GB/s at n=2^16,L=24; key-switch ops/s"
+UNIT = "NTT (poly x prime)/s"
+WORKLOAD = "n=2^16, L=24 primes (largest q<2^50, q=1 mod 2^17), 16 polys = 4 ciphertext pairs; " \
+           "fwd NTT -> automorph -> mul -> tensor -> inv NTT -> key switch (24+8 primes, dnum=3) x4"
+# Integer-pipe roofline of one lazy Shoup butterfly (3 mul.wide + 2 mul.hi +
+# 4 mul.lo on the FMA pipe; measured pipe rates on GB300: 25.2, 32 and 64 per
+# clock per SM), at the maximum SM clock.
+BFLY_PER_CLK_SM = 1.0 / (3 / 25.2 + 2 / 32.0 + 4 / 64.0)
+SMS, SM_MAX_MHZ = 152, 2070.0
+ALU_PEAK_BFLY = SMS * BFLY_PER_CLK_SM * SM_MAX_MHZ * 1e6
+BFLY_PER_FWD = NPOLY * L * (N // 2) * LOG_N
+NTT_BYTES_PER_FWD = 16 * NPOLY * L * N     # read + write every residue once
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        load = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ our arm ------
+
+def build_state(device):
+    import torch
+    from ntt_arithmetic_gb300 import api, inputs
+    q = api.find_primes(LOG_N, L)
+    p = api.find_primes(LOG_N, K, below=q[-1])
+    qp = q + p
+    st = {"q": q, "qp": qp}
+    st["tq"] = api.NttTables(LOG_N, q, device)
+    st["tqp"] = api.NttTables(LOG_N, qp, device)
+    st["modup"] = api.ModupTables(L, K, DNUM, qp, device)
+    x_host = inputs.uniform_residues((2, PAIRS, 2, L, N), q, seed=3, buffer=0)
+    keys_host = inputs.uniform_residues((DNUM, 2, L + K, N), qp, seed=3, buffer=1)
+    st["x_pinned"] = torch.from_numpy(x_host).pin_memory()
+    st["X"] = st["x_pinned"].to(device)
+    st["keys"] = torch.from_numpy(keys_host).to(device)
+    st["Y"] = torch.empty_like(st["X"])
+    st["D"] = torch.empty((PAIRS, 3, L, N), dtype=torch.uint64, device=device)
+    st["KS"] = torch.empty((PAIRS, 2, L + K, N), dtype=torch.uint64, device=device)
+    st["ws"] = torch.empty(api.keyswitch_workspace_bytes(LOG_N, L, K, DNUM, PAIRS) // 8, dtype=torch.uint64,
+                           device=device)
+    st["ks_pinned"] = torch.empty(st["KS"].shape, dtype=torch.uint64).pin_memory()
+    return st
+
+
+def run_step(st, step: int, ev=None):
+    """One pass of the hot path; `ev` (list of 7 events) brackets each call."""
+    from ntt_arithmetic_gb300 import api
+    k = pow(5, 1 << (step % 16), 2 * N)
+    rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
+    X, Y, D = st["X"], st["Y"], st["D"]
+    rec(0)
+    api.ntt_fwd(X, st["tq"])
+    rec(1)
+    api.automorph(Y, X, k, st["tq"], domain="ntt")
+    rec(2)
+    api.mul_ntt(Y, X, Y, st["tq"])
+    rec(3)
+    api.tensor(D, Y[0], Y[1], st["tq"])
+    rec(4)
+    api.ntt_inv(D, st["tq"])
+    rec(5)
+    # relinearisation input: component d2 of each of the 4 products (batch stride 3 L n)
+    api.keyswitch_ip(st["KS"], D, st["keys"], L, K, DNUM, st["tqp"], st["modup"], st["ws"],
+                     in_offset=2 * L * N, in_stride=3 * L * N, batch=PAIRS)
+    rec(6)
+
+
+def ours(args):
+    import torch
+    import torch.distributed as dist
+    from ntt_arithmetic_gb300 import api
+    from ntt_arithmetic_gb300 import build as B
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(B.OUT):
+        B.build()
+    if ws > 1:
+        dist.barrier()
+    st = build_state(device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for i in range(args.warmup):
+        run_step(st, i)
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = api.launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            run_step(st, args.warmup + i, evs[i])
+        stop.record(stream)
+        barrier()
+    launches = api.launch_count() - launches0
+    ms = start.elapsed_time(stop) / args.steps
+    per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)]
+    kern = [statistics.mean(p[j] for p in per) for j in range(6)]
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's input, the whole step, D2H of its key-switch output
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        st["X"].copy_(st["x_pinned"], non_blocking=True)
+        run_step(st, i)
+        st["ks_pinned"].copy_(st["KS"], non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+    if ws > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    clocks = clk.summary()
+    hbm, hbm_kind = peaks()
+    fwd_s = kern[0] * 1e-3
+    achieved_bfly = BFLY_PER_FWD / fwd_s
+    line = {
+        "metric": METRIC,
+        "value": UNITS * ws / (ms_max * 1e-3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u64",
+        "data": "synthetic: seeded uniform residues in [0, q) (SplitMix64 counter generator)",
+        "config": {"workload": WORKLOAD, "n": N, "L": L, "K": K, "dnum": DNUM, "polys": NPOLY,
+                   "units_per_step": UNITS, "l2": "inputs larger than L2 (201 MB residues + 101 MB keys per step)",
+                   "parallelism": f"replicas x{ws}"},
+        "kernels_ms": {"ntt_fwd": kern[0], "automorph_ntt": kern[1], "mul_ntt": kern[2], "tensor": kern[3],
+                       "ntt_inv": kern[4], "keyswitch_ip_x4": kern[5]},
+        "ntt_fwd_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9,
+        "ntt_fwd_poly_prime_per_s": NPOLY * L / fwd_s,
+        "ntt_fwd_hbm_frac": NTT_BYTES_PER_FWD / fwd_s / 1e9 / hbm,
+        "keyswitch_ops_per_s": PAIRS / (kern[5] * 1e-3) * ws,
+        "roofline": {"bound": "alu", "achieved": achieved_bfly / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
+                     "unit": "Gbutterfly/s", "frac": achieved_bfly / ALU_PEAK_BFLY, "traffic": None,
+                     "kernel": "k_ntt_fwd<16,3,8,5> (cluster NTT, n=2^16, 384 rows)",
+                     "hbm_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9, "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind},
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "e2e": {"value": UNITS * ws / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": st["x_pinned"].numel() * 8, "d2h_bytes_per_step": st["ks_pinned"].numel() * 8},
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_sample_steps)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------- oracle (CPU) arm --
+
+def oracle_sample_state():
+    """One of the 4 ciphertext pairs of the step (a quarter of its work)."""
+    import oracle
+    from ntt_arithmetic_gb300 import inputs
+    qp = [int(v) for v in oracle.primes(2 * N, L + K)]
+    q = qp[:L]
+    x = inputs.uniform_residues((2, PAIRS, 2, L, N), q, seed=3, buffer=0)[:, :1]
+    keys = inputs.uniform_residues((DNUM, 2, L + K, N), qp, seed=3, buffer=1)
+    return {"q": q, "qp": qp, "psi_q": oracle.psis(q, N), "psi_qp": oracle.psis(qp, N), "x": x, "keys": keys}
+
+
+def oracle_step(s, step: int, threads: int):
+    import oracle
+    k = pow(5, 1 << (step % 16), 2 * N)
+    X = oracle.ntt_batch(s["x"], s["q"], s["psi_q"], threads=threads)
+    Y = oracle.automorph_batch(X, s["q"], s["psi_q"], k, ntt_domain=True, threads=threads)
+    Z = oracle.mul_batch(X, Y, s["q"])
+    D = oracle.tensor_batch(Z[0], Z[1], s["q"])
+    D = oracle.ntt_batch(D, s["q"], s["psi_q"], inverse=True, threads=threads)
+    oracle.keyswitch_batch(D[:, 2], s["keys"], s["qp"], s["psi_qp"], L, K, DNUM, threads=threads)
+
+
+SAMPLE_UNITS = UNITS // PAIRS   # transforms in one pair's share of the step
+
+
+def cpu_baseline(steps: int):
+    import oracle
+    threads = oracle.default_threads()
+    s = oracle_sample_state()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle_step(s, i, threads)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": SAMPLE_UNITS / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"1 of the 4 ciphertext pairs of the step ({SAMPLE_UNITS} transforms + its automorph, "
+                      f"mul, tensor and 1 key switch), {steps} step(s), {dt:.2f} s/step, {threads} threads"}
+
+
+def reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from oracle import build as OB
+    OB.build() if OB.stale() else None
+    threads = oracle.default_threads()
+    s = oracle_sample_state()
+    for i in range(args.warmup):
+        oracle_step(s, i, threads)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(s, args.warmup + i, threads)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    value = SAMPLE_UNITS / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+        "data": "synthetic: seeded uniform residues in [0, q) (SplitMix64 counter generator)",
+        "config": {"workload": WORKLOAD, "n": N, "L": L, "K": K, "dnum": DNUM, "polys": NPOLY,
+                   "units_per_step": SAMPLE_UNITS, "sample": "1 of 4 ciphertext pairs per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"1 of the 4 ciphertext pairs of the step per timed step, {threads} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-steps", type=int, default=2)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

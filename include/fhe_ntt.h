@@ -1,0 +1,212 @@
+/*
+ * fhe_ntt.h -- C ABI of libfhe_ntt.so: batched RNS negacyclic NTT and the
+ * NTT-domain kernels of RNS-CKKS on one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  A residue tensor is row-major uint64_t[batch][L][n]: row (b, l)
+ *   holds the n residues of polynomial b modulo the l-th prime (FHElium,
+ *   "Eager, Compile, and native execution", section "Shared implementation
+ *   and native path": an RNS tensor is [*batch, limb, coefficient] and
+ *   parameter column j describes limb j).  n = 2^log_n, 1 <= log_n <= 17.
+ * Values.  Inputs must be fully reduced (0 <= x < q_l); outputs always are
+ *   ("For standard RNS addition, CPU and CUDA produce residues in [0, q_i)",
+ *   same page, section "One operation through both use models").  Inputs
+ *   outside [0, q) are not checked and give unspecified outputs.
+ * Moduli.  Every prime satisfies 2^48 < q < 2^50 and q = 1 (mod 2n); the
+ *   table builders reject anything else with FHE_EINVAL.
+ * Memory.  Every residue, table and workspace pointer is a device pointer
+ *   owned by the caller (PyTorch in the Python binding): the library never
+ *   allocates, frees or copies device memory.  All device pointers of one
+ *   call must live on one CUDA device; the call makes that device current
+ *   (as FHElium's CUDA adapters do) and fails with FHE_EDEVICE otherwise.
+ *   Host pointers where a device pointer is required fail with FHE_EDEVICE
+ *   before any launch, so no kernel ever receives a host address.  Residue,
+ *   table and workspace pointers must be 16-byte aligned (FHE_EINVAL).
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   Kernels are enqueued on it and the call returns without synchronising
+ *   ("Kernels launch on the current stream ... and do not introduce an
+ *   implicit host synchronization", same page, section "CUDA execution").
+ *   A fault inside a kernel surfaces at the caller's next synchronisation.
+ * Validation.  Arguments (sizes, pointer kinds, table shape, aliasing) are
+ *   checked on the host before launch ("C++ validation checks shape, dtype,
+ *   device agreement, parameter-row counts, broadcasting rules, and
+ *   prohibited overlap before ... launching a CUDA kernel", same page,
+ *   section "Schema registration and device dispatch").  Nothing aborts or
+ *   throws; every entry point returns a status code.
+ * Limb subsets.  A call with L smaller than the tables' L uses limbs [0, L).
+ */
+#ifndef FHE_NTT_H
+#define FHE_NTT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define FHE_OK 0
+#define FHE_EINVAL (-1)    /* bad size, modulus, k, null pointer or table shape */
+#define FHE_EALIAS (-2)    /* prohibited overlap between an output and another buffer */
+#define FHE_ECUDA (-3)     /* a CUDA runtime call or a kernel launch failed */
+#define FHE_ESPACE (-4)    /* workspace or host buffer too small */
+#define FHE_EDEVICE (-5)   /* host pointer where a device pointer is required, or mixed devices */
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fhe_version(void);
+
+/* Static message for a status code (never NULL). */
+const char *fhe_status_str(int status);
+
+/* Number of kernels this library has enqueued in this process (all devices,
+ * all streams) -- a diagnostic for counting launches around a timed region. */
+uint64_t fhe_launch_count(void);
+
+/* Diagnostic: checks the library's modular arithmetic routines (the lazy
+ * Shoup product, Barrett reductions, 128-bit accumulation) compiled for the
+ * host against exact 128-bit arithmetic on `iters` pseudo-random operands
+ * per prime (seeded by `seed`).  Needs no GPU.  FHE_OK when all agree. */
+int fhe_selftest_host(uint64_t seed, int iters);
+
+/* ---- primes and roots -------------------------------------------------- */
+
+/* The `count` largest primes q < below (below = 0 means 2^bits) with
+ * q = 1 (mod 2^(log_n+1)), in descending order, written to host out[count].
+ * Primality: deterministic Miller-Rabin for 64-bit inputs.  This reading of
+ * "the largest q < 2^50 with q = 1 mod 2n" is the one used for every
+ * workload; the special primes of a key switch are the next ones after the
+ * chain's primes (pass below = the last chain prime).
+ * Returns FHE_EINVAL if the range holds fewer than `count` primes. */
+int fhe_find_primes(int log_n, int bits, int count, uint64_t below, uint64_t *out);
+
+/* psi = the smallest primitive 2n-th root of unity modulo prime q
+ * (q = 1 mod 2n), written to *psi (host).  The transform below evaluates at
+ * the odd powers of this psi.  The pages fix no root; the smallest one is
+ * canonical and independent of any generator choice. */
+int fhe_root_of_unity(uint64_t q, int log_n, uint64_t *psi);
+
+/* ---- NTT tables -------------------------------------------------------- */
+
+/* Device view of a table blob: pointers into one caller-owned device buffer.
+ * FHElium passes "schedule and twiddle Tensors" to every NTT call (same page,
+ * section "Shared implementation and native path"); this struct is that
+ * argument.  Filled by fhe_ntt_tables_bind; treat the fields as opaque. */
+typedef struct fhe_ntt_tables {
+    int32_t log_n;            /* tables are for n = 2^log_n */
+    int32_t L;                /* number of primes covered */
+    const uint64_t *q;        /* [L] moduli */
+    const uint64_t *consts;   /* [L][16] per-prime constants */
+    const uint64_t *fwd;      /* [L][n][2] forward twiddles and Shoup companions */
+    const uint64_t *inv;      /* [L][n][2] inverse twiddles and Shoup companions */
+    const void *blob;         /* base of the device blob */
+    size_t bytes;             /* blob size */
+} fhe_ntt_tables;
+
+/* Size in bytes of the table blob for (log_n, L). */
+int fhe_ntt_tables_bytes(int log_n, int L, size_t *bytes);
+
+/* Build the blob for primes q[L] (host array) into host memory host_blob of
+ * `bytes` bytes (FHE_ESPACE if smaller than fhe_ntt_tables_bytes).  Copy
+ * the blob unchanged to device memory (any 16-byte aligned address), then
+ * call fhe_ntt_tables_bind. */
+int fhe_ntt_tables_build_host(int log_n, int L, const uint64_t *q, void *host_blob, size_t bytes);
+
+/* Fill *out with device pointers into dev_blob (no copy, no launch). */
+int fhe_ntt_tables_bind(const void *dev_blob, size_t bytes, int log_n, int L, fhe_ntt_tables *out);
+
+/* ---- transforms -------------------------------------------------------- */
+
+/* In-place forward negacyclic NTT of every row of res[batch][L][n]:
+ *   res[b][l][i] <- sum_j res[b][l][j] * psi_l^((2 brv(i) + 1) j)  mod q_l,
+ * i.e. the values of the row's polynomial at the n roots of X^n + 1, stored
+ * in bit-reversed order (brv over log_n bits).  The NTT is the transform
+ * under every CKKS multiplication, relinearisation and rotation in the
+ * kestrel-llm chain (lpnh.cn news 2512365, section 3, vllm_ntt.c) and
+ * FHElium's "power-of-two-radix NTT" family ("Eager, Compile, and native
+ * execution", table "Native operator families"). */
+int fhe_ntt_fwd(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream);
+
+/* In-place exact inverse of fhe_ntt_fwd, including the 1/n factor:
+ * bit-reversed evaluations in, natural-order coefficients out. */
+int fhe_ntt_inv(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream);
+
+/* ---- NTT-domain kernels ------------------------------------------------ */
+
+/* out = a * b mod q_l elementwise over [batch][L][n] (the pointwise product
+ * that turns into the negacyclic product after fhe_ntt_inv; kestrel-llm
+ * section 3 "polynomial multiplication").  out may equal a or b exactly;
+ * any other overlap is FHE_EALIAS. */
+int fhe_mul_ntt(uint64_t *out, const uint64_t *a, const uint64_t *b, int log_n, int L, int batch,
+                const fhe_ntt_tables *t, void *stream);
+
+/* Ciphertext tensor product in the NTT domain (the CKKS multiply before
+ * relinearisation; kestrel-llm section 3, vllm_ckks.c):
+ *   a, b: [batch][2][L][n] (components 0 and 1),  d: [batch][3][L][n]
+ *   d0 = a0 b0,  d1 = a0 b1 + a1 b0,  d2 = a1 b1   (mod q_l).
+ * d must not overlap a or b (FHE_EALIAS). */
+int fhe_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, int log_n, int L, int batch,
+               const fhe_ntt_tables *t, void *stream);
+
+#define FHE_DOMAIN_COEFF 0
+#define FHE_DOMAIN_NTT 1
+
+/* Galois automorphism sigma_k: a(X) -> a(X^k), k odd, 1 <= k < 2n (the
+ * rotations inside coeff_to_slot / slot_to_coeff, kestrel-llm section 4.2;
+ * FHElium "Galois automorphisms").  out, in: [batch][L][n].
+ *   FHE_DOMAIN_COEFF: coefficient t moves to s = t k mod 2n, negated
+ *     (q - a mod q) when s >= n, since X^n = -1.
+ *   FHE_DOMAIN_NTT: out[i] = in[j] with 2 brv(j) + 1 = k (2 brv(i) + 1)
+ *     mod 2n (a permutation of the evaluation points; no arithmetic).
+ * out must not overlap in (FHE_EALIAS). */
+int fhe_automorph(uint64_t *out, const uint64_t *in, int log_n, int L, int batch, uint64_t k,
+                  int domain, const fhe_ntt_tables *t, void *stream);
+
+/* ---- hybrid key switch ------------------------------------------------- */
+
+/* Basis: qp = (q_0 .. q_{L-1}, p_0 .. p_{K-1}), L + K <= 64.  Digits: with
+ * alpha = ceil(L / dnum), digit j covers limbs [j alpha, min((j+1) alpha, L)),
+ * 1 <= alpha <= 16, and every digit is non-empty. */
+
+/* Size of the ModUp constant blob (Garner and mixed-radix constants). */
+int fhe_modup_tables_bytes(int L, int K, int dnum, size_t *bytes);
+
+/* Build the ModUp blob for basis qp[L+K] (host) into host memory; copy it
+ * unchanged to a 16-byte aligned device buffer and pass that pointer as
+ * `modup` below. */
+int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_t *qp, void *host_blob,
+                                size_t bytes);
+
+/* Workspace bytes fhe_keyswitch_ip needs: batch * dnum * (L+K) * n * 8. */
+int fhe_keyswitch_workspace_bytes(int log_n, int L, int K, int dnum, int batch, size_t *bytes);
+
+/* Hybrid key-switch inner product, before ModDown (FHElium "key-switch
+ * multiply-accumulate" and "mixed-radix decomposition and basis extension",
+ * "Eager, Compile, and native execution", section "CUDA execution";
+ * kestrel-llm's Garner extension, section 4.2):
+ *   in:   batch items of [L][n], item b at in + b * in_stride (elements;
+ *         in_stride = 0 means L * n, i.e. a contiguous [batch][L][n]; it
+ *         lets a call read component d2 of a [batch][3][L][n] tensor
+ *         product directly), coefficient domain, basis q_0..q_{L-1}
+ *   keys: [dnum][2][L+K][n]      NTT domain, basis qp
+ *   out:  [batch][2][L+K][n]     NTT domain, basis qp
+ * For every digit j: X_j = the exact CRT integer of the digit's residues
+ * (0 <= X_j < prod of the digit's primes; mixed-radix / Garner), extended to
+ * every prime of qp (limbs inside the digit are copied), transformed with
+ * fhe_ntt_fwd over qp, then
+ *   out[b][c][l] = sum_j NTT(X_j)[l] * keys[j][c][l]  mod qp_l.
+ * t_qp: NTT tables for the L+K primes of qp in that order.
+ * workspace: device buffer of at least fhe_keyswitch_workspace_bytes; its
+ * contents on entry are ignored and on return are unspecified.  out, in,
+ * keys and workspace must be pairwise disjoint (FHE_EALIAS); in_stride, if
+ * nonzero, must be >= L * n and even. */
+int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
+                     int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
+                     const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FHE_NTT_H */

@@ -1,0 +1,222 @@
+"""Python API over the C ABI (include/fhe_ntt.h), with PyTorch tensors as the
+device memory and PyTorch's current CUDA stream as the launch stream.
+
+Residue tensors are contiguous CUDA tensors of dtype torch.uint64 (or
+torch.int64 holding the same bits) with shape [..., L, n].  Every function
+here only marshals arguments; all arithmetic runs in libfhe_ntt.so kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+import numpy as np
+import torch
+
+from . import _native as N
+
+_RESIDUE_DTYPES = (torch.uint64, torch.int64)
+
+
+def _stream(device: torch.device, stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _residues(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or t.dtype not in _RESIDUE_DTYPES:
+        raise TypeError(f"{name} must be a torch.uint64/int64 tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _log2(n: int) -> int:
+    if n < 2 or n & (n - 1):
+        raise ValueError(f"n = {n} is not a power of two >= 2")
+    return n.bit_length() - 1
+
+
+# ---------------------------------------------------------------- primes ---
+
+def find_primes(log_n: int, count: int, bits: int = 50, below: int = 0) -> list[int]:
+    """The `count` largest primes q < min(2^bits, below) with q = 1 mod 2n, descending."""
+    out = (ctypes.c_uint64 * count)()
+    N.call("fhe_find_primes", log_n, bits, count, below, out)
+    return [int(v) for v in out]
+
+
+def root_of_unity(q: int, log_n: int) -> int:
+    """Smallest primitive 2n-th root of unity modulo q."""
+    v = ctypes.c_uint64()
+    N.call("fhe_root_of_unity", q, log_n, ctypes.byref(v))
+    return int(v.value)
+
+
+def launch_count() -> int:
+    """Kernels enqueued by the library so far in this process."""
+    return int(N.lib().fhe_launch_count())
+
+
+# ---------------------------------------------------------------- tables ---
+
+class NttTables:
+    """Twiddle/constant tables for primes q[0..L) at degree n = 2^log_n,
+    built on the host by the library and held in one device tensor."""
+
+    def __init__(self, log_n: int, primes: Sequence[int], device="cuda"):
+        self.log_n = int(log_n)
+        self.primes = [int(q) for q in primes]
+        self.L = len(self.primes)
+        self.device = torch.device(device)
+        nbytes = ctypes.c_size_t()
+        N.call("fhe_ntt_tables_bytes", self.log_n, self.L, ctypes.byref(nbytes))
+        host = np.zeros(nbytes.value, dtype=np.uint8)
+        qs = (ctypes.c_uint64 * self.L)(*self.primes)
+        N.call("fhe_ntt_tables_build_host", self.log_n, self.L, qs, host.ctypes.data_as(ctypes.c_void_p),
+               nbytes.value)
+        self.host_blob = host
+        self.blob = torch.from_numpy(host).to(self.device)
+        self.struct = N.NttTables()
+        N.call("fhe_ntt_tables_bind", _ptr(self.blob), nbytes.value, self.log_n, self.L,
+               ctypes.byref(self.struct))
+
+    @property
+    def n(self) -> int:
+        return 1 << self.log_n
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+class ModupTables:
+    """Garner / mixed-radix constants of the key-switch basis extension for
+    basis qp = (q_0..q_{L-1}, p_0..p_{K-1}) split into dnum digits."""
+
+    def __init__(self, L: int, K: int, dnum: int, qp: Sequence[int], device="cuda"):
+        self.L, self.K, self.dnum = int(L), int(K), int(dnum)
+        if len(qp) != self.L + self.K:
+            raise ValueError("qp must list L + K primes")
+        nbytes = ctypes.c_size_t()
+        N.call("fhe_modup_tables_bytes", self.L, self.K, self.dnum, ctypes.byref(nbytes))
+        host = np.zeros(nbytes.value, dtype=np.uint8)
+        arr = (ctypes.c_uint64 * len(qp))(*[int(v) for v in qp])
+        N.call("fhe_modup_tables_build_host", self.L, self.K, self.dnum, arr,
+               host.ctypes.data_as(ctypes.c_void_p), nbytes.value)
+        self.blob = torch.from_numpy(host).to(torch.device(device))
+
+
+def _shape(x: torch.Tensor, tables: NttTables):
+    if x.dim() < 2:
+        raise ValueError("residue tensor needs shape [..., L, n]")
+    L, n = x.shape[-2], x.shape[-1]
+    log_n = _log2(n)
+    if log_n != tables.log_n:
+        raise ValueError(f"n = {n} does not match the tables (n = {tables.n})")
+    batch = x.numel() // (L * n)
+    return log_n, L, batch
+
+
+# ------------------------------------------------------------ transforms ---
+
+def ntt_fwd(x: torch.Tensor, tables: NttTables, stream=None) -> torch.Tensor:
+    """In-place forward negacyclic NTT of every [.., l, :] row; returns x."""
+    _residues(x, "x")
+    log_n, L, batch = _shape(x, tables)
+    N.call("fhe_ntt_fwd", _ptr(x), log_n, L, batch, tables.ref(), _stream(x.device, stream))
+    return x
+
+
+def ntt_inv(x: torch.Tensor, tables: NttTables, stream=None) -> torch.Tensor:
+    """In-place inverse NTT (with 1/n); returns x."""
+    _residues(x, "x")
+    log_n, L, batch = _shape(x, tables)
+    N.call("fhe_ntt_inv", _ptr(x), log_n, L, batch, tables.ref(), _stream(x.device, stream))
+    return x
+
+
+def mul_ntt(out: torch.Tensor, a: torch.Tensor, b: torch.Tensor, tables: NttTables, stream=None) -> torch.Tensor:
+    """out = a * b (mod q_l) elementwise; out may be a or b."""
+    for t, nm in ((out, "out"), (a, "a"), (b, "b")):
+        _residues(t, nm)
+    if a.shape != b.shape or out.shape != a.shape:
+        raise ValueError("a, b and out must have one shape")
+    log_n, L, batch = _shape(a, tables)
+    N.call("fhe_mul_ntt", _ptr(out), _ptr(a), _ptr(b), log_n, L, batch, tables.ref(), _stream(a.device, stream))
+    return out
+
+
+def tensor(d: torch.Tensor, a: torch.Tensor, b: torch.Tensor, tables: NttTables, stream=None) -> torch.Tensor:
+    """Ciphertext tensor product: a, b [batch, 2, L, n] -> d [batch, 3, L, n]."""
+    for t, nm in ((d, "d"), (a, "a"), (b, "b")):
+        _residues(t, nm)
+    if a.shape != b.shape or a.dim() < 3 or a.shape[-3] != 2:
+        raise ValueError("a and b must have shape [..., 2, L, n]")
+    if tuple(d.shape) != tuple(a.shape[:-3]) + (3,) + tuple(a.shape[-2:]):
+        raise ValueError("d must have shape [..., 3, L, n]")
+    log_n, L, batch2 = _shape(a, tables)
+    N.call("fhe_tensor", _ptr(d), _ptr(a), _ptr(b), log_n, L, batch2 // 2, tables.ref(), _stream(a.device, stream))
+    return d
+
+
+def automorph(out: torch.Tensor, x: torch.Tensor, k: int, tables: NttTables, domain: str = "ntt",
+              stream=None) -> torch.Tensor:
+    """out = sigma_k(x) (a(X) -> a(X^k)); domain 'ntt' or 'coeff'."""
+    _residues(out, "out")
+    _residues(x, "x")
+    if out.shape != x.shape:
+        raise ValueError("out and x must have one shape")
+    dom = {"ntt": N.FHE_DOMAIN_NTT, "coeff": N.FHE_DOMAIN_COEFF}[domain]
+    log_n, L, batch = _shape(x, tables)
+    N.call("fhe_automorph", _ptr(out), _ptr(x), log_n, L, batch, int(k), dom, tables.ref(),
+           _stream(x.device, stream))
+    return out
+
+
+def keyswitch_workspace_bytes(log_n: int, L: int, K: int, dnum: int, batch: int) -> int:
+    v = ctypes.c_size_t()
+    N.call("fhe_keyswitch_workspace_bytes", log_n, L, K, dnum, batch, ctypes.byref(v))
+    return int(v.value)
+
+
+def keyswitch_ip(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, L: int, K: int, dnum: int,
+                 tables_qp: NttTables, modup: ModupTables, workspace: torch.Tensor | None = None,
+                 stream=None, in_offset: int = 0, in_stride: int = 0, batch: int | None = None) -> torch.Tensor:
+    """Hybrid key-switch inner product (before ModDown).
+
+    x: coefficient-domain input, [batch, L, n] contiguous, or -- with
+    in_offset/in_stride (elements) and batch -- `batch` items of [L, n] at
+    x.flatten()[in_offset + b * in_stride:] (e.g. component d2 of a
+    [batch, 3, L, n] tensor product);  keys: [dnum, 2, L+K, n] NTT domain;
+    out: [batch, 2, L+K, n] NTT domain."""
+    for t, nm in ((out, "out"), (x, "x"), (keys, "keys")):
+        _residues(t, nm)
+    n = keys.shape[-1]
+    log_n = _log2(n)
+    if tuple(keys.shape) != (dnum, 2, L + K, n):
+        raise ValueError("keys must be [dnum, 2, L+K, n]")
+    item = L * n
+    if batch is None:
+        if x.shape[-2:] != (L, n) or in_offset or in_stride:
+            raise ValueError("x must be [..., L, n] (or pass batch with in_offset/in_stride)")
+        batch = x.numel() // item
+    stride = in_stride or item
+    if in_offset < 0 or stride < item or in_offset + (batch - 1) * stride + item > x.numel():
+        raise ValueError("in_offset/in_stride/batch reach outside x")
+    if tuple(out.shape[-3:]) != (2, L + K, n) or out.numel() != batch * 2 * (L + K) * n:
+        raise ValueError("out must be [batch, 2, L+K, n]")
+    need = keyswitch_workspace_bytes(log_n, L, K, dnum, batch)
+    if workspace is None:
+        workspace = torch.empty(need // 8, dtype=torch.uint64, device=x.device)
+    src = ctypes.c_void_p(x.data_ptr() + 8 * in_offset)
+    N.call("fhe_keyswitch_ip", _ptr(out), src, in_stride, _ptr(keys), log_n, L, K, dnum, batch, tables_qp.ref(),
+           _ptr(modup.blob), _ptr(workspace), workspace.numel() * workspace.element_size(),
+           _stream(x.device, stream))
+    return out

@@ -1,0 +1,85 @@
+"""Build step for libfhe_ntt.so (sm_103a), in-tree.
+
+Compiles every translation unit under csrc/ with nvcc in parallel and links
+one shared library next to this file.  No CMake; one -gencode target.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+ROOT = os.path.dirname(HERE)
+OUT = os.path.join(HERE, "libfhe_ntt.so")
+BUILD_DIR = os.path.join(HERE, "_build")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+SOURCES = ["ntt.cu", "pointwise.cu", "automorph.cu", "modup.cu", "abi.cu", "tables.cpp"]
+HEADERS = ["fhe_arith.cuh", "fhe_internal.h", "launch_util.h"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libfhe_ntt.so")
+
+
+def cuda_lib_dir(nv: str) -> str:
+    return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nv))), "lib64")
+
+
+def _inputs():
+    yield os.path.join(ROOT, "include", "fhe_ntt.h")
+    yield os.path.abspath(__file__)
+    for f in SOURCES + HEADERS:
+        yield os.path.join(CSRC, f)
+
+
+def stale() -> bool:
+    if not os.path.exists(OUT):
+        return True
+    t = os.path.getmtime(OUT)
+    return any(os.path.getmtime(f) > t for f in _inputs())
+
+
+def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = False) -> str:
+    if not force and not stale():
+        return OUT
+    nv = nvcc()
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    common = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        cmd = [nv, "-c", os.path.join(CSRC, src), "-o", obj] + common
+        if src.endswith(".cu"):
+            cmd += ARCH + ["-lineinfo"]
+            if ptxas_verbose:
+                cmd += ["-Xptxas", "-v"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if verbose or r.returncode != 0 or ptxas_verbose:
+            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}")
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = OUT + f".tmp{os.getpid()}"
+    libdir = cuda_lib_dir(nv)
+    link = [nv, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "shared", "-Xlinker", f"-rpath,{libdir}"]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if verbose or r.returncode != 0:
+        sys.stderr.write(" ".join(link) + "\n" + r.stdout + r.stderr)
+    if r.returncode != 0:
+        raise RuntimeError("link of libfhe_ntt.so failed")
+    os.replace(tmp, OUT)
+    return OUT
+
+
+if __name__ == "__main__":
+    print(build(verbose=True, ptxas_verbose="-v" in sys.argv, force=True))

@@ -1,0 +1,209 @@
+// abi.cu -- the extern "C" entry points of libfhe_ntt.so: host-side
+// validation, device selection and launches on the caller's stream.
+//
+// Validation follows the rules FHElium states for its adapters ("Eager,
+// Compile, and native execution", sections "Schema registration and device
+// dispatch", "CUDA execution" and "Execution properties"): shape, device
+// agreement, parameter-row counts and prohibited overlap are checked before
+// launch; mixed-device operands fail; the operand's device is made current;
+// kernels go on the given stream with no host synchronisation.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "fhe_internal.h"
+
+namespace fhe {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launches(int k) {
+    if (k > 0) g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed);
+}
+
+namespace {
+
+struct Span {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlap(Span a, Span b) {
+    const uintptr_t a0 = (uintptr_t)a.p, a1 = a0 + a.bytes, b0 = (uintptr_t)b.p, b1 = b0 + b.bytes;
+    return a.bytes && b.bytes && a0 < b1 && b0 < a1;
+}
+
+bool same(Span a, Span b) { return a.p == b.p && a.bytes == b.bytes; }
+
+// Resolve the device of every pointer; all must be device (or managed)
+// memory of one device, which becomes current.  Host or unknown pointers
+// are rejected so that no kernel is ever handed a host address.
+int select_device(std::initializer_list<const void *> ptrs) {
+    int dev = -1;
+    for (const void *p : ptrs) {
+        if (!p) return FHE_EINVAL;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            cudaGetLastError();
+            return FHE_EDEVICE;
+        }
+        if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return FHE_EDEVICE;
+        if (dev < 0) dev = a.device;
+        else if (a.device != dev) return FHE_EDEVICE;
+    }
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return FHE_ECUDA;
+    if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return FHE_ECUDA;
+    return FHE_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+int check_tables(const fhe_ntt_tables *t, int log_n, int L) {
+    if (!t || !t->q || !t->consts || !t->fwd || !t->inv || !t->blob) return FHE_EINVAL;
+    if (t->log_n != log_n || L > t->L) return FHE_EINVAL;
+    if (t->bytes < ntt_layout(t->log_n, t->L).bytes) return FHE_EINVAL;
+    return FHE_OK;
+}
+
+int check_shape(int log_n, int L, long batch) {
+    if (log_n < 1 || log_n > kMaxLogN || L < 1 || batch < 1) return FHE_EINVAL;
+    const long rows = batch * (long)L;
+    if (rows > (1L << 30) / (log_n >= 14 ? (1L << (log_n - 13)) : 1)) return FHE_EINVAL;  // grid size
+    return FHE_OK;
+}
+
+int finish(int launched) {
+    if (launched < 0) {
+        cudaGetLastError();
+        return FHE_ECUDA;
+    }
+    count_launches(launched);
+    return FHE_OK;
+}
+
+}  // namespace
+}  // namespace fhe
+
+using namespace fhe;
+
+extern "C" int fhe_version(void) { return 100; }
+
+extern "C" const char *fhe_status_str(int s) {
+    switch (s) {
+        case FHE_OK: return "ok";
+        case FHE_EINVAL: return "invalid argument (size, modulus, k, null pointer, alignment or table shape)";
+        case FHE_EALIAS: return "prohibited overlap between an output and another buffer";
+        case FHE_ECUDA: return "CUDA runtime or kernel launch failure";
+        case FHE_ESPACE: return "workspace or host buffer too small";
+        case FHE_EDEVICE: return "host pointer where a device pointer is required, or operands on different devices";
+        default: return "unknown status";
+    }
+}
+
+extern "C" uint64_t fhe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+static int ntt_call(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream, bool inverse) {
+    int s = check_shape(log_n, L, batch);
+    if (s) return s;
+    if ((s = check_tables(t, log_n, L))) return s;
+    if (!res || !aligned16(res)) return FHE_EINVAL;
+    if ((s = select_device({res, t->blob}))) return s;
+    const Span r{res, ((size_t)batch * L << log_n) * 8}, tb{t->blob, t->bytes};
+    if (overlap(r, tb)) return FHE_EALIAS;
+    return finish(launch_ntt(res, log_n, L, (long)batch * L, t, inverse, stream));
+}
+
+extern "C" int fhe_ntt_fwd(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream) {
+    return ntt_call(res, log_n, L, batch, t, stream, false);
+}
+
+extern "C" int fhe_ntt_inv(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream) {
+    return ntt_call(res, log_n, L, batch, t, stream, true);
+}
+
+extern "C" int fhe_mul_ntt(uint64_t *out, const uint64_t *a, const uint64_t *b, int log_n, int L, int batch,
+                           const fhe_ntt_tables *t, void *stream) {
+    int s = check_shape(log_n, L, batch);
+    if (s) return s;
+    if ((s = check_tables(t, log_n, L))) return s;
+    if (!out || !a || !b || !aligned16(out) || !aligned16(a) || !aligned16(b)) return FHE_EINVAL;
+    if ((s = select_device({out, a, b, t->blob}))) return s;
+    const size_t bytes = ((size_t)batch * L << log_n) * 8;
+    const Span o{out, bytes}, sa{a, bytes}, sb{b, bytes}, tb{t->blob, t->bytes};
+    if ((overlap(o, sa) && !same(o, sa)) || (overlap(o, sb) && !same(o, sb)) || overlap(o, tb)) return FHE_EALIAS;
+    return finish(launch_mul(out, a, b, log_n, L, (long)batch * L, t, stream));
+}
+
+extern "C" int fhe_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, int log_n, int L, int batch,
+                          const fhe_ntt_tables *t, void *stream) {
+    int s = check_shape(log_n, L, batch);
+    if (s) return s;
+    if ((s = check_tables(t, log_n, L))) return s;
+    if (!d || !a || !b || !aligned16(d) || !aligned16(a) || !aligned16(b)) return FHE_EINVAL;
+    if ((s = select_device({d, a, b, t->blob}))) return s;
+    const size_t plane = ((size_t)L << log_n) * 8;
+    const Span sd{d, 3 * plane * batch}, sa{a, 2 * plane * batch}, sb{b, 2 * plane * batch}, tb{t->blob, t->bytes};
+    if (overlap(sd, sa) || overlap(sd, sb) || overlap(sd, tb)) return FHE_EALIAS;
+    return finish(launch_tensor(d, a, b, log_n, L, batch, t, stream));
+}
+
+extern "C" int fhe_automorph(uint64_t *out, const uint64_t *in, int log_n, int L, int batch, uint64_t k, int domain,
+                             const fhe_ntt_tables *t, void *stream) {
+    int s = check_shape(log_n, L, batch);
+    if (s) return s;
+    if ((s = check_tables(t, log_n, L))) return s;
+    if (domain != FHE_DOMAIN_COEFF && domain != FHE_DOMAIN_NTT) return FHE_EINVAL;
+    if ((k & 1) == 0 || k >= (2ull << log_n)) return FHE_EINVAL;
+    if (!out || !in || !aligned16(out) || !aligned16(in)) return FHE_EINVAL;
+    if ((s = select_device({out, in, t->blob}))) return s;
+    const size_t bytes = ((size_t)batch * L << log_n) * 8;
+    const Span o{out, bytes}, i{in, bytes}, tb{t->blob, t->bytes};
+    if (overlap(o, i) || overlap(o, tb)) return FHE_EALIAS;
+    return finish(launch_automorph(out, in, log_n, L, (long)batch * L, k, domain, t, stream));
+}
+
+extern "C" int fhe_keyswitch_workspace_bytes(int log_n, int L, int K, int dnum, int batch, size_t *bytes) {
+    if (!bytes || log_n < 1 || log_n > kMaxLogN || batch < 1 || !modup_shape_ok(L, K, dnum) || dnum > 32)
+        return FHE_EINVAL;
+    *bytes = ((size_t)batch * dnum * (L + K) << log_n) * 8;
+    return FHE_OK;
+}
+
+extern "C" int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys, int log_n,
+                                int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp, const void *modup,
+                                uint64_t *workspace, size_t ws_bytes, void *stream) {
+    size_t need = 0;
+    int s = fhe_keyswitch_workspace_bytes(log_n, L, K, dnum, batch, &need);
+    if (s) return s;
+    const int LK = L + K;
+    if ((s = check_shape(log_n, LK, (long)batch * dnum))) return s;
+    if ((s = check_tables(t_qp, log_n, LK))) return s;
+    if (!out || !in || !keys || !modup || !workspace) return FHE_EINVAL;
+    if (!aligned16(out) || !aligned16(in) || !aligned16(keys) || !aligned16(workspace) || !aligned16(modup))
+        return FHE_EINVAL;
+    if (ws_bytes < need) return FHE_ESPACE;
+    const size_t item = (size_t)L << log_n;
+    if (in_stride == 0) in_stride = item;
+    if (in_stride < item || (in_stride & 1)) return FHE_EINVAL;
+    if ((s = select_device({out, in, keys, modup, workspace, t_qp->blob}))) return s;
+    const size_t plane = ((size_t)LK << log_n) * 8;
+    const Span so{out, 2 * plane * batch}, si{in, ((size_t)(batch - 1) * in_stride + item) * 8}, sk{keys, 2 * plane * dnum},
+        sw{workspace, need}, tb{t_qp->blob, t_qp->bytes}, sm{modup, modup_layout(L, K, dnum).bytes};
+    const Span all[6] = {so, si, sk, sw, tb, sm};
+    for (int x = 0; x < 6; x++)
+        for (int y = x + 1; y < 6; y++) {
+            if ((x == 1 || x == 2 || x == 4 || x == 5) && (y == 1 || y == 2 || y == 4 || y == 5)) continue;  // read-only pairs
+            if (overlap(all[x], all[y])) return FHE_EALIAS;
+        }
+    int launched = 0, r;
+    if ((r = launch_modup(workspace, in, (long)in_stride, log_n, L, K, dnum, batch, t_qp, modup, stream)) < 0)
+        return finish(-1);
+    launched += r;
+    if ((r = launch_ntt(workspace, log_n, LK, (long)batch * dnum * LK, t_qp, false, stream)) < 0) return finish(-1);
+    launched += r;
+    if ((r = launch_ks_ip(out, workspace, keys, log_n, LK, dnum, batch, t_qp, stream)) < 0) return finish(-1);
+    launched += r;
+    return finish(launched);
+}

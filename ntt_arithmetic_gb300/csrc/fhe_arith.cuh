@@ -1,0 +1,136 @@
+// fhe_arith.cuh -- 64-bit modular arithmetic for primes 2^48 < q < 2^50,
+// written for the integer pipes of sm_103a and usable on the host as well
+// (the same code path is exercised by the library's host self-test).
+//
+// Cost model (measured on GB300 with a register-resident microbenchmark):
+// 32-bit mul.lo issues at 64/clk/SM, mul.hi and mul.wide at ~32 and ~25/clk/SM
+// (twice the cost), adds and logic run on a separate pipe.  The butterflies
+// below therefore minimise hi/wide partial products and keep every reduction
+// that is not strictly needed out of the inner loop (Harvey's lazy bounds).
+#pragma once
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define FHE_HD __host__ __device__ __forceinline__
+#else
+#define FHE_HD inline
+#endif
+
+namespace fhe {
+
+FHE_HD uint32_t lo32(uint64_t x) { return (uint32_t)x; }
+FHE_HD uint32_t hi32(uint64_t x) { return (uint32_t)(x >> 32); }
+
+FHE_HD uint32_t umulhi32(uint32_t a, uint32_t b) {
+#if defined(__CUDA_ARCH__)
+    return __umulhi(a, b);
+#else
+    return (uint32_t)(((uint64_t)a * b) >> 32);
+#endif
+}
+
+FHE_HD uint64_t umulhi64(uint64_t a, uint64_t b) {
+#if defined(__CUDA_ARCH__)
+    return __umul64hi(a, b);
+#else
+    return (uint64_t)(((unsigned __int128)a * b) >> 64);
+#endif
+}
+
+// x - c if x >= c, else x
+FHE_HD uint64_t csub(uint64_t x, uint64_t c) { return x >= c ? x - c : x; }
+
+// Per-prime constants, one row of 16 words per prime in the table blob.
+enum ConstSlot {
+    K_Q = 0,          // q
+    K_MU12 = 1,       // floor(2^100 / q) << 12       (Barrett, full products)
+    K_C58 = 2,        // floor(2^58 / q)              (small-quotient reduction)
+    K_NINV = 3,       // n^-1 mod q
+    K_NINV_S = 4,     //   its Shoup companion floor(w 2^64 / q)
+    K_W1NINV = 5,     // psi^-brv(1) * n^-1 mod q     (last inverse stage)
+    K_W1NINV_S = 6,   //   its Shoup companion
+    K_PSI = 7,        // psi (smallest primitive 2n-th root)
+    K_COUNT = 16
+};
+
+// Lazy Shoup product.  V. Shoup's precomputed-quotient multiplication by a
+// fixed w (as in NTL's MulModPrecon), with D. Harvey's lazy output range
+// ("Faster arithmetic for number-theoretic transforms", J. Symb. Comp. 2014):
+// for w < q, wp = floor(w 2^64 / q) and any y < 2^62, returns r = w y - Q q
+// with 0 <= r < 4q.  The quotient Q uses three 32x32 partial products of
+// wp * y -- the low x low term is dropped -- so Q is at most 3 below
+// floor(w y / q) and never above it.
+FHE_HD uint64_t shoup_lazy(uint64_t y, uint64_t w, uint64_t wp, uint64_t q) {
+    const uint32_t yl = lo32(y), yh = hi32(y), wl = lo32(wp), wh = hi32(wp);
+    const uint64_t Q = (uint64_t)wh * yh + umulhi32(wh, yl) + umulhi32(wl, yh);
+    return w * y - Q * q;
+}
+
+// Reduction of x < 2^58 into [0, q) with one 32x32 high product (a Barrett
+// step on the top 32 bits): Q = floor((x >> 26) * c58 / 2^32), c58 =
+// floor(2^58 / q), lies in (x/q - 3, x/q], so x - Q q < 3q.
+FHE_HD uint64_t reduce_small(uint64_t x, uint64_t q, uint32_t c58) {
+    const uint32_t Q = umulhi32((uint32_t)(x >> 26), c58);
+    uint64_t r = x - (uint64_t)Q * q;
+    r = csub(r, 2 * q);
+    return csub(r, q);
+}
+
+// Barrett reduction (P. Barrett, CRYPTO '86) of a 128-bit value T = hi:lo
+// with T < 2^105: x = floor(T / 2^48), Q = floor(x mu / 2^52) with
+// mu = floor(2^100 / q), so T - Q q < (3 + T / 2^100) q < 2^58 and the
+// small-quotient step finishes the reduction.
+FHE_HD uint64_t barrett_reduce128(uint64_t hi, uint64_t lo, uint64_t q, uint64_t mu12, uint32_t c58) {
+    const uint64_t x = (hi << 16) | (lo >> 48);
+    const uint64_t Q = umulhi64(x, mu12);
+    return reduce_small(lo - Q * q, q, c58);
+}
+
+// a * b mod q exactly, for a, b < q (Barrett with mu = floor(2^100/q)):
+// T = a b < 2^100, so T - Q q < 3q.
+FHE_HD uint64_t mulmod(uint64_t a, uint64_t b, uint64_t q, uint64_t mu12) {
+    const uint64_t lo = a * b, hi = umulhi64(a, b);
+    const uint64_t x = (hi << 16) | (lo >> 48);
+    const uint64_t Q = umulhi64(x, mu12);
+    uint64_t r = lo - Q * q;
+    r = csub(r, 2 * q);
+    return csub(r, q);
+}
+
+// 128-bit multiply-accumulate: (hi:lo) += a * b
+FHE_HD void mac128(uint64_t &hi, uint64_t &lo, uint64_t a, uint64_t b) {
+    const uint64_t pl = a * b, ph = umulhi64(a, b);
+    lo += pl;
+    hi += ph + (lo < pl ? 1 : 0);
+}
+
+// Forward (Cooley-Tukey) butterfly with the psi-merged twiddle w (Roy et
+// al./Poppelmann et al. merged negacyclic NTT) and Harvey's lazy additive
+// bound: if X, Y < B then X', Y' < B + 4q.  No comparison at all.
+FHE_HD void ct_bfly(uint64_t &X, uint64_t &Y, uint64_t w, uint64_t wp, uint64_t q) {
+    const uint64_t t = shoup_lazy(Y, w, wp, q);
+    const uint64_t x = X;
+    X = x + t;
+    Y = x - t + 4 * q;
+}
+
+// Inverse (Gentleman-Sande) butterfly, values kept in [0, 4q):
+// X' = X + Y folded back below 4q, Y' = (X - Y) w.
+FHE_HD void gs_bfly(uint64_t &X, uint64_t &Y, uint64_t w, uint64_t wp, uint64_t q) {
+    const uint64_t x = X, y = Y, q4 = 4 * q;
+    X = csub(x + y, q4);
+    Y = shoup_lazy(x - y + q4, w, wp, q);
+}
+
+// Last inverse stage with n^-1 folded into both outputs.
+FHE_HD void gs_bfly_last(uint64_t &X, uint64_t &Y, uint64_t ni, uint64_t nip, uint64_t wni,
+                         uint64_t wnip, uint64_t q) {
+    const uint64_t x = X, y = Y;
+    X = shoup_lazy(x + y, ni, nip, q);
+    Y = shoup_lazy(x - y + 4 * q, wni, wnip, q);
+}
+
+// [0, 4q) -> [0, q)
+FHE_HD uint64_t reduce4(uint64_t x, uint64_t q) { return csub(csub(x, 2 * q), q); }
+
+}  // namespace fhe

@@ -1,0 +1,105 @@
+// modup.cu -- exact basis extension (ModUp) of every key-switch digit.
+//
+// For digit j with primes d_0..d_{a-1} and one coefficient with residues
+// x_0..x_{a-1}, Garner's algorithm gives the mixed-radix digits of the CRT
+// integer X in [0, d_0 ... d_{a-1}):
+//   v_0 = x_0,  v_i = ((((x_i - v_0) d_0^-1 - v_1) d_1^-1 ...) - v_{i-1}) d_{i-1}^-1 mod d_i,
+// and X mod p = v_0 + v_1 d_0 + v_2 d_0 d_1 + ... (mod p) for every prime p of
+// the extended basis.  This is the "mixed-radix decomposition and basis
+// extension" of FHElium's CUDA layer ("Eager, Compile, and native
+// execution", section "CUDA execution") and the "Garner extension" of the
+// kestrel-llm chain (overview, section 4.2).  All constants are fixed per
+// basis, so every product is a lazy Shoup product; the extension sums stay
+// below 2^56 and are reduced once.
+#include <cuda_runtime.h>
+
+#include "fhe_arith.cuh"
+#include "fhe_internal.h"
+#include "launch_util.h"
+
+namespace fhe {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int MAXA>
+__global__ void __launch_bounds__(kThreads)
+k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int dnum, int alpha,
+        const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ garner, const ulonglong2 *__restrict__ mr,
+        const uint64_t *__restrict__ consts) {
+    const long n = 1L << log_n;
+    const int j = blockIdx.y, bi = blockIdx.z;
+    const int lo = dg[j].lo, cnt = dg[j].count;
+    const ulonglong2 *gj = garner + (long)j * alpha * alpha;
+    const ulonglong2 *mj = mr + (long)j * LK * alpha;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        uint64_t x[MAXA], v[MAXA];
+        const uint64_t *src = in + (long)bi * in_stride + (long)lo * n + i;
+#pragma unroll
+        for (int a = 0; a < MAXA; a++) x[a] = a < cnt ? __ldcs(src + a * n) : 0;
+        v[0] = x[0];
+#pragma unroll
+        for (int a = 1; a < MAXA; a++) {
+            v[a] = 0;
+            if (a < cnt) {
+                const uint64_t d = __ldg(consts + (long)(lo + a) * K_COUNT + K_Q);
+                uint64_t u = x[a];
+#pragma unroll
+                for (int b = 0; b < a; b++) {
+                    const ulonglong2 c = __ldg(gj + a * alpha + b);
+                    u = shoup_lazy(u + 4 * d - v[b], c.x, c.y, d);   // v_b < 2^50 < 4 d
+                }
+                v[a] = reduce4(u, d);
+            }
+        }
+        uint64_t *dst = ext + ((long)bi * dnum + j) * LK * n + i;
+#pragma unroll
+        for (int a = 0; a < MAXA; a++)
+            if (a < cnt) __stcs(dst + (long)(lo + a) * n, x[a]);   // limbs of the digit are copies
+        for (int l = 0; l < LK; l++) {
+            if (l >= lo && l < lo + cnt) continue;
+            const uint64_t *kc = consts + (long)l * K_COUNT;
+            const uint64_t p = __ldg(kc + K_Q);
+            uint64_t acc = v[0];
+#pragma unroll
+            for (int a = 1; a < MAXA; a++) {
+                if (a < cnt) {
+                    const ulonglong2 m = __ldg(mj + l * alpha + a);
+                    acc += shoup_lazy(v[a], m.x, m.y, p);
+                }
+            }
+            __stcs(dst + (long)l * n, reduce_small(acc, p, (uint32_t)__ldg(kc + K_C58)));
+        }
+    }
+}
+
+template <int MAXA>
+void launch_modup_t(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
+                    const fhe_ntt_tables *t, const void *modup, cudaStream_t st) {
+    const ModupLayout lay = modup_layout(L, K, dnum);
+    const char *base = (const char *)modup;
+    const long n = 1L << log_n;
+    const long bx = (n + kThreads - 1) / kThreads;
+    const long cap = ((long)sm_count() * 8 + (long)dnum * batch - 1) / ((long)dnum * batch);
+    dim3 grid((unsigned)(bx < cap ? bx : (cap > 0 ? cap : 1)), (unsigned)dnum, (unsigned)batch);
+    k_modup<MAXA><<<grid, kThreads, 0, st>>>(ext, in, in_stride, log_n, L + K, dnum, lay.alpha,
+                                             (const ModupDigit *)(base + lay.off_digits),
+                                             (const ulonglong2 *)(base + lay.off_garner),
+                                             (const ulonglong2 *)(base + lay.off_mr), t->consts);
+}
+
+}  // namespace
+
+int launch_modup(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
+                 const fhe_ntt_tables *t, const void *modup, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const int alpha = modup_layout(L, K, dnum).alpha;
+    if (alpha <= 1) launch_modup_t<1>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
+    else if (alpha <= 2) launch_modup_t<2>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
+    else if (alpha <= 4) launch_modup_t<4>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
+    else if (alpha <= 8) launch_modup_t<8>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
+    else launch_modup_t<16>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace fhe

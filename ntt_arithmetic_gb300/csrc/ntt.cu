@@ -1,0 +1,479 @@
+// ntt.cu -- batched negacyclic NTT / INTT over RNS primes on sm_103a.
+//
+// One (polynomial, prime) row of n = 2^LOGN residues is transformed by a
+// thread-block cluster of C = 2^LOGC CTAs (C = 1 for n <= 2^13).  Each CTA
+// owns M = n / C residues in shared memory, so a row crosses HBM exactly once
+// in each direction: the "compact grouped" / "fixed-radix shared-memory"
+// execution FHElium describes for its CUDA NTT families ("Eager, Compile, and
+// native execution", table "Native operator families"), here built on
+// Blackwell clusters and distributed shared memory.
+//
+// Forward (natural -> bit-reversed, psi-merged Cooley-Tukey):
+//   stage s (s = 0 .. LOGN-1) pairs positions p and p + n/2^(s+1) inside blocks
+//   of n/2^s and multiplies by psi^brv(2^s + block) (table fwd[2^s + block]).
+//   * cross stages s < LOGC: the C elements {j1 M + j2 : j1 < C} of a column
+//     j2 live in C different CTAs; each thread loads whole columns from HBM,
+//     applies the LOGC stages in registers and scatters element j1 into CTA
+//     j1's shared memory (DSMEM), then one cluster barrier;
+//   * local stages s >= LOGC run in passes of up to LOGE stages: a thread
+//     holds 2^LOGE residues (radix-2^LOGE in registers), with one shared-
+//     memory round trip and one __syncthreads between passes.
+// Inverse (bit-reversed -> natural, Gentleman-Sande with psi^-brv, n^-1 in
+//   the last stage): the mirror image -- local passes first, cross stages last.
+//
+// Arithmetic: lazy Shoup butterflies (fhe_arith.cuh).  Forward values grow by
+// < 4q per stage with no comparisons (< 69 q < 2^57 after 17 stages) and are
+// reduced once before the store; inverse values stay below 4q.
+//
+// Shared-memory index swizzle: index p is stored at p ^ (((p >> LOGE) & 7) << 1),
+// which makes every pass's accesses bank-conflict-free (two wavefronts per
+// 64-bit warp access) and keeps 16-byte pairs (2k, 2k+1) adjacent.
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include "fhe_arith.cuh"
+#include "fhe_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace fhe {
+namespace {
+
+template <int LOGN_, int LOGC_, int LOGT_, int LOGE_>
+struct Shape {
+    static constexpr int LOGN = LOGN_, LOGC = LOGC_, LOGT = LOGT_, LOGE = LOGE_;
+    static constexpr int N = 1 << LOGN, C = 1 << LOGC, LOGM = LOGN - LOGC, M = 1 << LOGM;
+    static constexpr int T = 1 << LOGT, E = 1 << LOGE;
+    static constexpr int P = (LOGM + LOGE - 1) / LOGE;     // local passes
+    static constexpr int EREM = LOGM - (P - 1) * LOGE;     // stages in the odd-sized pass
+    static_assert(LOGM == LOGT + LOGE, "M = T * E");
+    static_assert(LOGC == 0 || (E / C) % 2 == 0, "cross phase moves 16-byte column pairs");
+};
+
+struct Ctx {
+    const ulonglong2 *tw;   // this prime's twiddle pairs (w, floor(w 2^64 / q))
+    const uint64_t *kc;     // this prime's constants
+    uint64_t q;
+    int t;                  // thread index
+    int r;                  // rank in the cluster
+};
+
+template <int LOGE>
+__device__ __forceinline__ int swz(int p) { return p ^ (((p >> LOGE) & 7) << 1); }
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Position inside the CTA's block of the j-th residue of group g in a pass
+// covering local bit positions [B, B + EP).
+template <int B, int EP>
+__device__ __forceinline__ int pass_pos(int g, int j) {
+    return (g & ((1 << B) - 1)) | (j << B) | ((g >> B) << (B + EP));
+}
+
+template <class SH, int B, int EP>
+__device__ __forceinline__ void smem_load(uint64_t (&x)[SH::E], const uint64_t *sm, int t) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = t + SH::T * k;
+        if constexpr (B == 0 && EP >= 1) {
+#pragma unroll
+            for (int j = 0; j < EPN; j += 2) {
+                const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(sm + swz<SH::LOGE>(pass_pos<B, EP>(g, j)));
+                x[k * EPN + j] = v.x;
+                x[k * EPN + j + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < EPN; j++) x[k * EPN + j] = sm[swz<SH::LOGE>(pass_pos<B, EP>(g, j))];
+        }
+    }
+}
+
+template <class SH, int B, int EP>
+__device__ __forceinline__ void smem_store(const uint64_t (&x)[SH::E], uint64_t *sm, int t) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = t + SH::T * k;
+        if constexpr (B == 0 && EP >= 1) {
+#pragma unroll
+            for (int j = 0; j < EPN; j += 2) {
+                *reinterpret_cast<ulonglong2 *>(sm + swz<SH::LOGE>(pass_pos<B, EP>(g, j))) =
+                    make_ulonglong2(x[k * EPN + j], x[k * EPN + j + 1]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < EPN; j++) sm[swz<SH::LOGE>(pass_pos<B, EP>(g, j))] = x[k * EPN + j];
+        }
+    }
+}
+
+// HBM <-> registers for a pass; `blk` points at this CTA's block of M residues.
+template <class SH, int B, int EP>
+__device__ __forceinline__ void global_load(uint64_t (&x)[SH::E], const uint64_t *blk, int t) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = t + SH::T * k;
+        if constexpr (B == 0 && EP >= 1) {
+#pragma unroll
+            for (int j = 0; j < EPN; j += 2) {
+                const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(blk + pass_pos<B, EP>(g, j)));
+                x[k * EPN + j] = v.x;
+                x[k * EPN + j + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < EPN; j++) x[k * EPN + j] = __ldcs(blk + pass_pos<B, EP>(g, j));
+        }
+    }
+}
+
+template <class SH, int B, int EP>
+__device__ __forceinline__ void global_store(const uint64_t (&x)[SH::E], uint64_t *blk, int t) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = t + SH::T * k;
+        if constexpr (B == 0 && EP >= 1) {
+#pragma unroll
+            for (int j = 0; j < EPN; j += 2)
+                __stcs(reinterpret_cast<ulonglong2 *>(blk + pass_pos<B, EP>(g, j)),
+                       make_ulonglong2(x[k * EPN + j], x[k * EPN + j + 1]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < EPN; j++) __stcs(blk + pass_pos<B, EP>(g, j), x[k * EPN + j]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- forward --
+
+// Local stage I of a pass over bits [B, B+EP): global stage s = LOGN-B-EP+I,
+// register distance 2^(EP-1-I), 2^I distinct twiddles per group.
+template <class SH, int B, int EP, int I>
+__device__ __forceinline__ void fwd_stage(uint64_t (&x)[SH::E], const Ctx &c) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+    constexpr int S = SH::LOGN - B - EP + I;
+    constexpr int HALF = 1 << (EP - 1 - I);
+    constexpr int NW = 1 << I;
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = c.t + SH::T * k;
+        const int base = (1 << S) + (c.r << (SH::LOGM - B - EP + I)) + ((g >> B) << I);
+#pragma unroll
+        for (int jj = 0; jj < NW; jj++) {
+            const ulonglong2 w = __ldg(c.tw + base + jj);
+#pragma unroll
+            for (int u = 0; u < HALF; u++) {
+                const int j = jj * 2 * HALF + u;
+                ct_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
+            }
+        }
+    }
+}
+
+template <class SH, int B, int EP, int I = 0>
+__device__ __forceinline__ void fwd_compute(uint64_t (&x)[SH::E], const Ctx &c) {
+    if constexpr (I < EP) {
+        fwd_stage<SH, B, EP, I>(x, c);
+        fwd_compute<SH, B, EP, I + 1>(x, c);
+    }
+}
+
+// Cross-CTA stages (s < LOGC) on columns: x[col * C + j1].
+template <class SH, int S>
+__device__ __forceinline__ void cross_fwd(uint64_t (&x)[SH::E], const Ctx &c) {
+    if constexpr (S < SH::LOGC) {
+        constexpr int C = SH::C, COLS = SH::E / C, H = C >> (S + 1);
+#pragma unroll
+        for (int j1 = 0; j1 < C; j1++) {
+            if (j1 & H) continue;
+            const ulonglong2 w = __ldg(c.tw + (1 << S) + (j1 >> (SH::LOGC - S)));
+#pragma unroll
+            for (int col = 0; col < COLS; col++) ct_bfly(x[col * C + j1], x[col * C + j1 + H], w.x, w.y, c.q);
+        }
+        cross_fwd<SH, S + 1>(x, c);
+    }
+}
+
+// Column j2 of thread-local column index col: pairs of adjacent columns.
+template <class SH>
+__device__ __forceinline__ int col_j2(int cp, int t, int r) {
+    return r * (SH::M / SH::C) + 2 * (cp * SH::T + t);
+}
+
+template <class SH, int PI>
+__device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, const Ctx &c) {
+    constexpr int LOGE = SH::LOGE;
+    constexpr int B = (SH::P - 1 - PI) * LOGE;
+    constexpr int EP = PI == 0 ? SH::EREM : LOGE;
+    fwd_compute<SH, B, EP>(x, c);
+    if constexpr (PI + 1 < SH::P) {
+        smem_store<SH, B, EP>(x, sm, c.t);
+        __syncthreads();
+        constexpr int B2 = (SH::P - 2 - PI) * LOGE;
+        smem_load<SH, B2, LOGE>(x, sm, c.t);
+        fwd_passes<SH, PI + 1>(x, sm, blk, c);
+    } else {
+        const uint32_t c58 = (uint32_t)c.kc[K_C58];
+#pragma unroll
+        for (int i = 0; i < SH::E; i++) x[i] = reduce_small(x[i], c.q, c58);
+        global_store<SH, B, EP>(x, blk, c.t);
+    }
+}
+
+template <int LOGN, int LOGC, int LOGT, int LOGE>
+__global__ void __launch_bounds__(1 << LOGT)
+k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    extern __shared__ __align__(16) uint64_t sm[];
+    Ctx c;
+    c.t = threadIdx.x;
+    c.r = SH::C > 1 ? (int)(blockIdx.x & (SH::C - 1)) : 0;
+    const long row = (long)(blockIdx.x >> LOGC);
+    const int l = (int)(row % L);
+    uint64_t *data = res + row * SH::N;
+    c.tw = tw + (long)l * SH::N;
+    c.kc = consts + (long)l * K_COUNT;
+    c.q = c.kc[K_Q];
+    uint64_t x[SH::E];
+    if constexpr (SH::C > 1) {
+        constexpr int C = SH::C, PAIRS = SH::E / C / 2;
+        cluster_arrive_relaxed();
+#pragma unroll
+        for (int cp = 0; cp < PAIRS; cp++) {
+            const int j2 = col_j2<SH>(cp, c.t, c.r);
+#pragma unroll
+            for (int j1 = 0; j1 < C; j1++) {
+                const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(data + (long)j1 * SH::M + j2));
+                x[(2 * cp) * C + j1] = v.x;
+                x[(2 * cp + 1) * C + j1] = v.y;
+            }
+        }
+        cross_fwd<SH, 0>(x, c);
+        cluster_wait();   // every CTA of the cluster has started: DSMEM is live
+        cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+        for (int j1 = 0; j1 < C; j1++) {
+            uint64_t *dst = cl.map_shared_rank(sm, (unsigned)j1);
+#pragma unroll
+            for (int cp = 0; cp < PAIRS; cp++) {
+                const int j2 = col_j2<SH>(cp, c.t, c.r);
+                *reinterpret_cast<ulonglong2 *>(dst + swz<LOGE>(j2)) =
+                    make_ulonglong2(x[(2 * cp) * C + j1], x[(2 * cp + 1) * C + j1]);
+            }
+        }
+        cluster_arrive();
+        cluster_wait();
+        smem_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, sm, c.t);
+    } else {
+        global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, data, c.t);
+    }
+    fwd_passes<SH, 0>(x, sm, data + (long)c.r * SH::M, c);
+}
+
+// ---------------------------------------------------------------- inverse --
+
+// Local GS stage I of a pass over bits [B, B+EP): stride bit KB = B + I,
+// twiddle psi^-brv(n/2^(KB+1) + (p >> (KB+1))), 2^(EP-1-I) per group.
+template <class SH, int B, int EP, int I, bool LASTG>
+__device__ __forceinline__ void inv_stage(uint64_t (&x)[SH::E], const Ctx &c) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+    constexpr int KB = B + I;
+    constexpr int HALF = 1 << I;
+    constexpr int NW = 1 << (EP - 1 - I);
+    constexpr bool LAST = LASTG && (I == EP - 1);
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = c.t + SH::T * k;
+        if constexpr (LAST) {
+            const uint64_t ni = c.kc[K_NINV], nip = c.kc[K_NINV_S], wn = c.kc[K_W1NINV], wnp = c.kc[K_W1NINV_S];
+#pragma unroll
+            for (int u = 0; u < HALF; u++) gs_bfly_last(x[k * EPN + u], x[k * EPN + u + HALF], ni, nip, wn, wnp, c.q);
+        } else {
+            const int base = (SH::N >> (KB + 1)) + (c.r << (SH::LOGM - KB - 1)) + ((g >> B) << (EP - I - 1));
+#pragma unroll
+            for (int jj = 0; jj < NW; jj++) {
+                const ulonglong2 w = __ldg(c.tw + base + jj);
+#pragma unroll
+                for (int u = 0; u < HALF; u++) {
+                    const int j = jj * 2 * HALF + u;
+                    gs_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
+                }
+            }
+        }
+    }
+}
+
+template <class SH, int B, int EP, bool LASTG, int I = 0>
+__device__ __forceinline__ void inv_compute(uint64_t (&x)[SH::E], const Ctx &c) {
+    if constexpr (I < EP) {
+        inv_stage<SH, B, EP, I, LASTG>(x, c);
+        inv_compute<SH, B, EP, LASTG, I + 1>(x, c);
+    }
+}
+
+// Cross-CTA GS stages: stride bit LOGM + S, pairs (j1, j1 + 2^S).
+template <class SH, int S>
+__device__ __forceinline__ void cross_inv(uint64_t (&x)[SH::E], const Ctx &c) {
+    if constexpr (S < SH::LOGC) {
+        constexpr int C = SH::C, COLS = SH::E / C, H = 1 << S;
+        if constexpr (S == SH::LOGC - 1) {
+            const uint64_t ni = c.kc[K_NINV], nip = c.kc[K_NINV_S], wn = c.kc[K_W1NINV], wnp = c.kc[K_W1NINV_S];
+#pragma unroll
+            for (int j1 = 0; j1 < C; j1++) {
+                if (j1 & H) continue;
+#pragma unroll
+                for (int col = 0; col < COLS; col++)
+                    gs_bfly_last(x[col * C + j1], x[col * C + j1 + H], ni, nip, wn, wnp, c.q);
+            }
+        } else {
+#pragma unroll
+            for (int j1 = 0; j1 < C; j1++) {
+                if (j1 & H) continue;
+                const ulonglong2 w = __ldg(c.tw + (C >> (S + 1)) + (j1 >> (S + 1)));
+#pragma unroll
+                for (int col = 0; col < COLS; col++) gs_bfly(x[col * C + j1], x[col * C + j1 + H], w.x, w.y, c.q);
+            }
+        }
+        cross_inv<SH, S + 1>(x, c);
+    }
+}
+
+template <class SH, int PI>
+__device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, uint64_t *data,
+                                           const Ctx &c) {
+    constexpr int LOGE = SH::LOGE;
+    constexpr int B = PI * LOGE;
+    constexpr int EP = PI == SH::P - 1 ? SH::EREM : LOGE;
+    constexpr bool LASTG = (SH::C == 1) && (PI == SH::P - 1);
+    inv_compute<SH, B, EP, LASTG>(x, c);
+    if constexpr (PI + 1 < SH::P) {
+        smem_store<SH, B, EP>(x, sm, c.t);
+        __syncthreads();
+        constexpr int EP2 = PI + 1 == SH::P - 1 ? SH::EREM : LOGE;
+        smem_load<SH, B + LOGE, EP2>(x, sm, c.t);
+        inv_passes<SH, PI + 1>(x, sm, blk, data, c);
+    } else if constexpr (SH::C == 1) {
+#pragma unroll
+        for (int i = 0; i < SH::E; i++) x[i] = reduce4(x[i], c.q);
+        global_store<SH, B, EP>(x, blk, c.t);
+    } else {
+        constexpr int C = SH::C, PAIRS = SH::E / C / 2;
+        smem_store<SH, B, EP>(x, sm, c.t);
+        cluster_arrive();
+        cluster_wait();
+        cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+        for (int j1 = 0; j1 < C; j1++) {
+            const uint64_t *src = cl.map_shared_rank(sm, (unsigned)j1);
+#pragma unroll
+            for (int cp = 0; cp < PAIRS; cp++) {
+                const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(src + swz<LOGE>(col_j2<SH>(cp, c.t, c.r)));
+                x[(2 * cp) * C + j1] = v.x;
+                x[(2 * cp + 1) * C + j1] = v.y;
+            }
+        }
+        cross_inv<SH, 0>(x, c);
+#pragma unroll
+        for (int i = 0; i < SH::E; i++) x[i] = reduce4(x[i], c.q);
+#pragma unroll
+        for (int cp = 0; cp < PAIRS; cp++) {
+            const int j2 = col_j2<SH>(cp, c.t, c.r);
+#pragma unroll
+            for (int j1 = 0; j1 < C; j1++)
+                __stcs(reinterpret_cast<ulonglong2 *>(data + (long)j1 * SH::M + j2),
+                       make_ulonglong2(x[(2 * cp) * C + j1], x[(2 * cp + 1) * C + j1]));
+        }
+        cluster_arrive();   // keep this CTA's shared memory alive until every peer has read it
+        cluster_wait();
+    }
+}
+
+template <int LOGN, int LOGC, int LOGT, int LOGE>
+__global__ void __launch_bounds__(1 << LOGT)
+k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    extern __shared__ __align__(16) uint64_t sm[];
+    Ctx c;
+    c.t = threadIdx.x;
+    c.r = SH::C > 1 ? (int)(blockIdx.x & (SH::C - 1)) : 0;
+    const long row = (long)(blockIdx.x >> LOGC);
+    const int l = (int)(row % L);
+    uint64_t *data = res + row * SH::N;
+    c.tw = tw + (long)l * SH::N;
+    c.kc = consts + (long)l * K_COUNT;
+    c.q = c.kc[K_Q];
+    uint64_t x[SH::E];
+    uint64_t *blk = data + (long)c.r * SH::M;
+    global_load<SH, 0, (SH::P == 1 ? SH::EREM : LOGE)>(x, blk, c.t);
+    inv_passes<SH, 0>(x, sm, blk, data, c);
+}
+
+// ---------------------------------------------------------------- launch --
+
+template <int LOGN, int LOGC, int LOGT, int LOGE>
+int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool inverse, cudaStream_t st) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    void (*kern)(uint64_t *, int, const ulonglong2 *, const uint64_t *) =
+        inverse ? k_ntt_inv<LOGN, LOGC, LOGT, LOGE> : k_ntt_fwd<LOGN, LOGC, LOGT, LOGE>;
+    const size_t smem = (size_t)SH::M * sizeof(uint64_t);
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * SH::C));
+    cfg.blockDim = dim3(SH::T);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = SH::C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = SH::C > 1 ? 1 : 0;
+    const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(inverse ? t->inv : t->fwd);
+    if (cudaLaunchKernelEx(&cfg, kern, res, L, tw, t->consts) != cudaSuccess) return -1;
+    return 1;
+}
+
+}  // namespace
+
+int launch_ntt(uint64_t *res, int log_n, int L, long rows, const fhe_ntt_tables *t, bool inverse, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (log_n) {
+        //                        LOGN LOGC LOGT LOGE
+        case 1: return launch_shape<1, 0, 0, 1>(res, L, rows, t, inverse, st);
+        case 2: return launch_shape<2, 0, 0, 2>(res, L, rows, t, inverse, st);
+        case 3: return launch_shape<3, 0, 0, 3>(res, L, rows, t, inverse, st);
+        case 4: return launch_shape<4, 0, 1, 3>(res, L, rows, t, inverse, st);
+        case 5: return launch_shape<5, 0, 2, 3>(res, L, rows, t, inverse, st);
+        case 6: return launch_shape<6, 0, 3, 3>(res, L, rows, t, inverse, st);
+        case 7: return launch_shape<7, 0, 4, 3>(res, L, rows, t, inverse, st);
+        case 8: return launch_shape<8, 0, 5, 3>(res, L, rows, t, inverse, st);
+        case 9: return launch_shape<9, 0, 6, 3>(res, L, rows, t, inverse, st);
+        case 10: return launch_shape<10, 0, 7, 3>(res, L, rows, t, inverse, st);
+        case 11: return launch_shape<11, 0, 7, 4>(res, L, rows, t, inverse, st);
+        case 12: return launch_shape<12, 0, 8, 4>(res, L, rows, t, inverse, st);
+        case 13: return launch_shape<13, 0, 8, 5>(res, L, rows, t, inverse, st);
+        case 14: return launch_shape<14, 1, 8, 5>(res, L, rows, t, inverse, st);
+        case 15: return launch_shape<15, 2, 8, 5>(res, L, rows, t, inverse, st);
+        case 16: return launch_shape<16, 3, 8, 5>(res, L, rows, t, inverse, st);
+        case 17: return launch_shape<17, 3, 9, 5>(res, L, rows, t, inverse, st);
+        default: return -1;
+    }
+}
+
+}  // namespace fhe

@@ -1,0 +1,125 @@
+// pointwise.cu -- NTT-domain coefficient-wise kernels: pointwise product,
+// ciphertext tensor product and the key-switch inner product.  All are
+// HBM-streaming: one pass per operand, 16-byte accesses, persistent grids of
+// a few CTAs per SM with grid-stride loops.  Variable x variable products use
+// Barrett reduction (fhe_arith.cuh); sums of products are accumulated exactly
+// in 128 bits and reduced once.
+#include <cuda_runtime.h>
+
+#include "fhe_arith.cuh"
+#include "fhe_internal.h"
+#include "launch_util.h"
+
+namespace fhe {
+namespace {
+
+constexpr int kThreads = 256;
+
+// out = a * b mod q_l over [rows][n], rows = batch * L; processed in pairs.
+__global__ void __launch_bounds__(kThreads)
+k_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
+      const uint64_t *__restrict__ consts) {
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+        const long e = 2 * i;
+        const int l = (int)((e >> log_n) % L);
+        const uint64_t q = __ldg(consts + l * K_COUNT + K_Q), mu = __ldg(consts + l * K_COUNT + K_MU12);
+        const ulonglong2 va = __ldcs(reinterpret_cast<const ulonglong2 *>(a + e));
+        const ulonglong2 vb = __ldcs(reinterpret_cast<const ulonglong2 *>(b + e));
+        __stcs(reinterpret_cast<ulonglong2 *>(out + e), make_ulonglong2(mulmod(va.x, vb.x, q, mu), mulmod(va.y, vb.y, q, mu)));
+    }
+}
+
+// d0 = a0 b0, d1 = a0 b1 + a1 b0, d2 = a1 b1 per batch item.
+__global__ void __launch_bounds__(kThreads)
+k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
+         const uint64_t *__restrict__ consts) {
+    const long plane = (long)L << log_n;
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+        const long e = 2 * i;                  // flat index over [batch][L][n]
+        const long row = e >> log_n;
+        const long bi = row / L;
+        const int l = (int)(row - bi * L);
+        const long in_off = e + bi * plane;    // [batch][2][L][n]
+        const long out_off = e + 2 * bi * plane;  // [batch][3][L][n]
+        const uint64_t *kc = consts + l * K_COUNT;
+        const uint64_t q = __ldg(kc + K_Q), mu = __ldg(kc + K_MU12);
+        const uint32_t c58 = (uint32_t)__ldg(kc + K_C58);
+        const ulonglong2 a0 = __ldcs(reinterpret_cast<const ulonglong2 *>(a + in_off));
+        const ulonglong2 a1 = __ldcs(reinterpret_cast<const ulonglong2 *>(a + in_off + plane));
+        const ulonglong2 b0 = __ldcs(reinterpret_cast<const ulonglong2 *>(b + in_off));
+        const ulonglong2 b1 = __ldcs(reinterpret_cast<const ulonglong2 *>(b + in_off + plane));
+        uint64_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+        mac128(h0, l0, a0.x, b1.x);
+        mac128(h0, l0, a1.x, b0.x);
+        mac128(h1, l1, a0.y, b1.y);
+        mac128(h1, l1, a1.y, b0.y);
+        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off),
+               make_ulonglong2(mulmod(a0.x, b0.x, q, mu), mulmod(a0.y, b0.y, q, mu)));
+        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + plane),
+               make_ulonglong2(barrett_reduce128(h0, l0, q, mu, c58), barrett_reduce128(h1, l1, q, mu, c58)));
+        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + 2 * plane),
+               make_ulonglong2(mulmod(a1.x, b1.x, q, mu), mulmod(a1.y, b1.y, q, mu)));
+    }
+}
+
+// out[b][c][l][i] = sum_j ext[b][j][l][i] * keys[j][c][l][i] mod p_l.
+// One thread owns a pair of coefficients of one limb for every batch item,
+// so each key word is fetched from HBM once per call.
+__global__ void __launch_bounds__(kThreads)
+k_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, long pairs, int log_n, int LK, int dnum,
+        int batch, const uint64_t *__restrict__ consts) {
+    const long plane = (long)LK << log_n;      // one [LK][n] block
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+        const long e = 2 * i;                   // flat index over [LK][n]
+        const int l = (int)(e >> log_n);
+        const uint64_t *kc = consts + l * K_COUNT;
+        const uint64_t q = __ldg(kc + K_Q), mu = __ldg(kc + K_MU12);
+        const uint32_t c58 = (uint32_t)__ldg(kc + K_C58);
+        for (int bi = 0; bi < batch; bi++) {
+            uint64_t h0x = 0, l0x = 0, h0y = 0, l0y = 0, h1x = 0, l1x = 0, h1y = 0, l1y = 0;
+            for (int j = 0; j < dnum; j++) {
+                const ulonglong2 dv = __ldcs(reinterpret_cast<const ulonglong2 *>(ext + ((long)bi * dnum + j) * plane + e));
+                const ulonglong2 k0 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j) * plane + e));
+                const ulonglong2 k1 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j + 1) * plane + e));
+                mac128(h0x, l0x, dv.x, k0.x);
+                mac128(h0y, l0y, dv.y, k0.y);
+                mac128(h1x, l1x, dv.x, k1.x);
+                mac128(h1y, l1y, dv.y, k1.y);
+            }
+            uint64_t *o = out + (long)bi * 2 * plane + e;
+            __stcs(reinterpret_cast<ulonglong2 *>(o),
+                   make_ulonglong2(barrett_reduce128(h0x, l0x, q, mu, c58), barrett_reduce128(h0y, l0y, q, mu, c58)));
+            __stcs(reinterpret_cast<ulonglong2 *>(o + plane),
+                   make_ulonglong2(barrett_reduce128(h1x, l1x, q, mu, c58), barrett_reduce128(h1y, l1y, q, mu, c58)));
+        }
+    }
+}
+
+}  // namespace
+
+int launch_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, int log_n, int L, long rows,
+               const fhe_ntt_tables *t, void *stream) {
+    const long pairs = (rows << log_n) / 2;
+    k_mul<<<stream_grid(pairs, kThreads, 8), kThreads, 0, (cudaStream_t)stream>>>(out, a, b, pairs, log_n, L, t->consts);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, int log_n, int L, int batch,
+                  const fhe_ntt_tables *t, void *stream) {
+    const long pairs = ((long)batch * L << log_n) / 2;
+    k_tensor<<<stream_grid(pairs, kThreads, 8), kThreads, 0, (cudaStream_t)stream>>>(d, a, b, pairs, log_n, L, t->consts);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,
+                 const fhe_ntt_tables *t, void *stream) {
+    const long pairs = ((long)LK << log_n) / 2;
+    k_ks_ip<<<stream_grid(pairs, kThreads, 8), kThreads, 0, (cudaStream_t)stream>>>(out, ext, keys, pairs, log_n, LK,
+                                                                                     dnum, batch, t->consts);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace fhe

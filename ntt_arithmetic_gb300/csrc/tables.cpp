@@ -1,0 +1,317 @@
+// tables.cpp -- host-side table builders of libfhe_ntt.so: prime search,
+// roots of unity, twiddle tables with Shoup companions, per-prime constants,
+// and the Garner / mixed-radix constants of the key-switch basis extension.
+// Host code only; the blobs it writes are copied to the device by the caller.
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "fhe_arith.cuh"
+#include "fhe_internal.h"
+
+namespace {
+
+using u128 = unsigned __int128;
+
+uint64_t mul_mod(uint64_t a, uint64_t b, uint64_t m) { return (uint64_t)((u128)a * b % m); }
+
+uint64_t pow_mod(uint64_t b, uint64_t e, uint64_t m) {
+    uint64_t r = 1 % m;
+    b %= m;
+    for (; e; e >>= 1) {
+        if (e & 1) r = mul_mod(r, b, m);
+        b = mul_mod(b, b, m);
+    }
+    return r;
+}
+
+uint64_t inv_mod(uint64_t a, uint64_t p) { return pow_mod(a % p, p - 2, p); }
+
+// Deterministic Miller-Rabin for all 64-bit n with the seven witnesses
+// {2, 325, 9375, 28178, 450775, 9780504, 1795265022} (J. Sinclair, 2011).
+bool is_prime_u64(uint64_t n) {
+    if (n < 2) return false;
+    for (uint64_t p : {2ull, 3ull, 5ull, 7ull, 11ull, 13ull, 17ull, 19ull, 23ull, 29ull, 31ull, 37ull}) {
+        if (n % p == 0) return n == p;
+    }
+    uint64_t d = n - 1;
+    int s = __builtin_ctzll(d);
+    d >>= s;
+    for (uint64_t a : {2ull, 325ull, 9375ull, 28178ull, 450775ull, 9780504ull, 1795265022ull}) {
+        uint64_t x = pow_mod(a % n, d, n);
+        if (a % n == 0 || x == 1 || x == n - 1) continue;
+        bool witness = true;
+        for (int i = 1; i < s && witness; i++) {
+            x = mul_mod(x, x, n);
+            if (x == n - 1) witness = false;
+        }
+        if (witness) return false;
+    }
+    return true;
+}
+
+uint64_t shoup(uint64_t w, uint64_t q) { return (uint64_t)(((u128)w << 64) / q); }
+
+uint32_t bit_reverse(uint32_t x, int bits) {
+    uint32_t r = 0;
+    for (int i = 0; i < bits; i++) r |= ((x >> i) & 1u) << (bits - 1 - i);
+    return r;
+}
+
+bool modulus_ok(uint64_t q, int log_n) {
+    const uint64_t two_n = 2ull << log_n;
+    return q > (1ull << 48) && q < (1ull << 50) && q % two_n == 1 && is_prime_u64(q);
+}
+
+// Smallest element of multiplicative order exactly 2n: every such element is
+// g^t (t odd) for one g of order 2n, and g = c^((q-1)/2n) has order 2n as
+// soon as c is a quadratic non-residue (then g^n = c^((q-1)/2) = -1).
+uint64_t smallest_primitive_root(uint64_t q, int log_n) {
+    const uint64_t two_n = 2ull << log_n, n = 1ull << log_n;
+    uint64_t g = 0;
+    for (uint64_t c = 2; c < q; c++) {
+        g = pow_mod(c, (q - 1) / two_n, q);
+        if (pow_mod(g, n, q) == q - 1) break;
+    }
+    const uint64_t g2 = mul_mod(g, g, q);
+    uint64_t best = g, cur = g;
+    for (uint64_t t = 3; t < two_n; t += 2) {
+        cur = mul_mod(cur, g2, q);
+        if (cur < best) best = cur;
+    }
+    return best;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+namespace fhe {
+
+NttLayout ntt_layout(int log_n, int L) {
+    NttLayout s;
+    const size_t n = (size_t)1 << log_n;
+    s.off_q = 0;
+    s.off_consts = align256(s.off_q + (size_t)L * 8);
+    s.off_fwd = align256(s.off_consts + (size_t)L * K_COUNT * 8);
+    s.off_inv = align256(s.off_fwd + (size_t)L * n * 16);
+    s.bytes = align256(s.off_inv + (size_t)L * n * 16);
+    return s;
+}
+
+ModupLayout modup_layout(int L, int K, int dnum) {
+    ModupLayout s;
+    s.alpha = (L + dnum - 1) / dnum;
+    const int LK = L + K;
+    s.off_digits = 0;
+    s.off_garner = align256((size_t)dnum * sizeof(ModupDigit));
+    s.off_mr = align256(s.off_garner + (size_t)dnum * s.alpha * s.alpha * 16);
+    s.bytes = align256(s.off_mr + (size_t)dnum * LK * s.alpha * 16);
+    return s;
+}
+
+bool modup_shape_ok(int L, int K, int dnum) {
+    if (L < 1 || K < 0 || dnum < 1 || dnum > L || L + K > kMaxBasis) return false;
+    const int alpha = (L + dnum - 1) / dnum;
+    if (alpha > kMaxAlpha) return false;
+    return (dnum - 1) * alpha < L;   // every digit non-empty
+}
+
+int selftest_arith(uint64_t seed, int iters);
+
+}  // namespace fhe
+
+using namespace fhe;
+
+extern "C" int fhe_find_primes(int log_n, int bits, int count, uint64_t below, uint64_t *out) {
+    if (log_n < 1 || log_n > kMaxLogN || bits < 2 || bits > 62 || count < 1 || !out) return FHE_EINVAL;
+    const uint64_t m = 2ull << log_n;
+    const uint64_t top = 1ull << bits;
+    if (below == 0 || below > top) below = top;
+    if (below <= m + 1) return FHE_EINVAL;
+    uint64_t c = ((below - 2) / m) * m + 1;   // largest c < below with c = 1 mod m
+    int found = 0;
+    for (; found < count && c > m; c -= m) {
+        if (is_prime_u64(c)) out[found++] = c;
+    }
+    return found == count ? FHE_OK : FHE_EINVAL;
+}
+
+extern "C" int fhe_root_of_unity(uint64_t q, int log_n, uint64_t *psi) {
+    if (!psi || log_n < 1 || log_n > kMaxLogN) return FHE_EINVAL;
+    const uint64_t two_n = 2ull << log_n;
+    if (q < 3 || q % two_n != 1 || !is_prime_u64(q)) return FHE_EINVAL;
+    *psi = smallest_primitive_root(q, log_n);
+    return FHE_OK;
+}
+
+extern "C" int fhe_ntt_tables_bytes(int log_n, int L, size_t *bytes) {
+    if (!bytes || log_n < 1 || log_n > kMaxLogN || L < 1 || L > kMaxTableL) return FHE_EINVAL;
+    *bytes = ntt_layout(log_n, L).bytes;
+    return FHE_OK;
+}
+
+extern "C" int fhe_ntt_tables_build_host(int log_n, int L, const uint64_t *q, void *host_blob, size_t bytes) {
+    if (!q || !host_blob || log_n < 1 || log_n > kMaxLogN || L < 1 || L > kMaxTableL) return FHE_EINVAL;
+    const NttLayout lay = ntt_layout(log_n, L);
+    if (bytes < lay.bytes) return FHE_ESPACE;
+    for (int l = 0; l < L; l++)
+        if (!modulus_ok(q[l], log_n)) return FHE_EINVAL;
+    const uint64_t n = 1ull << log_n;
+    char *base = (char *)host_blob;
+    std::memset(base, 0, lay.bytes);
+    uint64_t *qv = (uint64_t *)(base + lay.off_q);
+    uint64_t *kc = (uint64_t *)(base + lay.off_consts);
+    uint64_t *fwd = (uint64_t *)(base + lay.off_fwd);
+    uint64_t *inv = (uint64_t *)(base + lay.off_inv);
+    std::vector<uint64_t> pw(n), ipw(n);
+    for (int l = 0; l < L; l++) {
+        const uint64_t ql = q[l];
+        const uint64_t psi = smallest_primitive_root(ql, log_n);
+        const uint64_t psi_inv = inv_mod(psi, ql);
+        pw[0] = ipw[0] = 1;
+        for (uint64_t i = 1; i < n; i++) {
+            pw[i] = mul_mod(pw[i - 1], psi, ql);
+            ipw[i] = mul_mod(ipw[i - 1], psi_inv, ql);
+        }
+        uint64_t *f = fwd + (size_t)l * n * 2, *g = inv + (size_t)l * n * 2;
+        for (uint64_t k = 0; k < n; k++) {
+            // k-th twiddle = psi^brv(k) (forward) and psi^-brv(k) (inverse), brv over log_n bits
+            const uint64_t w = pw[bit_reverse((uint32_t)k, log_n)];
+            const uint64_t wi = ipw[bit_reverse((uint32_t)k, log_n)];
+            f[2 * k] = w;
+            f[2 * k + 1] = shoup(w, ql);
+            g[2 * k] = wi;
+            g[2 * k + 1] = shoup(wi, ql);
+        }
+        uint64_t *c = kc + (size_t)l * K_COUNT;
+        const uint64_t ninv = inv_mod(n % ql, ql);
+        const uint64_t w1ninv = mul_mod(ipw[bit_reverse(1, log_n)], ninv, ql);
+        qv[l] = ql;
+        c[K_Q] = ql;
+        c[K_MU12] = (uint64_t)(((u128)1 << 100) / ql) << 12;
+        c[K_C58] = (uint64_t)((1ull << 58) / ql);
+        c[K_NINV] = ninv;
+        c[K_NINV_S] = shoup(ninv, ql);
+        c[K_W1NINV] = w1ninv;
+        c[K_W1NINV_S] = shoup(w1ninv, ql);
+        c[K_PSI] = psi;
+    }
+    return FHE_OK;
+}
+
+extern "C" int fhe_ntt_tables_bind(const void *dev_blob, size_t bytes, int log_n, int L, fhe_ntt_tables *out) {
+    if (!dev_blob || !out || log_n < 1 || log_n > kMaxLogN || L < 1 || L > kMaxTableL) return FHE_EINVAL;
+    const NttLayout lay = ntt_layout(log_n, L);
+    if (bytes < lay.bytes) return FHE_ESPACE;
+    if (((uintptr_t)dev_blob & 15) != 0) return FHE_EINVAL;
+    const char *base = (const char *)dev_blob;
+    out->log_n = log_n;
+    out->L = L;
+    out->q = (const uint64_t *)(base + lay.off_q);
+    out->consts = (const uint64_t *)(base + lay.off_consts);
+    out->fwd = (const uint64_t *)(base + lay.off_fwd);
+    out->inv = (const uint64_t *)(base + lay.off_inv);
+    out->blob = dev_blob;
+    out->bytes = lay.bytes;
+    return FHE_OK;
+}
+
+extern "C" int fhe_modup_tables_bytes(int L, int K, int dnum, size_t *bytes) {
+    if (!bytes || !modup_shape_ok(L, K, dnum)) return FHE_EINVAL;
+    *bytes = modup_layout(L, K, dnum).bytes;
+    return FHE_OK;
+}
+
+// Constants of the exact basis extension of digit j with primes d_0..d_{a-1}:
+//  Garner (mixed radix):  v_0 = x_0,  v_i = (((x_i - v_0) d_0^-1 - v_1) d_1^-1 ...
+//                          - v_{i-1}) d_{i-1}^-1  mod d_i           -> garner[i][k] = d_k^-1 mod d_i
+//  Extension:             X mod p = v_0 + sum_{i>=1} v_i (d_0 ... d_{i-1} mod p)
+//                                                                    -> mr[l][i] = d_0..d_{i-1} mod p_l
+// Both with Shoup companions (pairs of words).
+extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_t *qp, void *host_blob,
+                                           size_t bytes) {
+    if (!qp || !host_blob || !modup_shape_ok(L, K, dnum)) return FHE_EINVAL;
+    const ModupLayout lay = modup_layout(L, K, dnum);
+    if (bytes < lay.bytes) return FHE_ESPACE;
+    const int LK = L + K, alpha = lay.alpha;
+    for (int l = 0; l < LK; l++) {
+        if (qp[l] <= (1ull << 48) || qp[l] >= (1ull << 50) || !is_prime_u64(qp[l])) return FHE_EINVAL;
+        for (int m = 0; m < l; m++)
+            if (qp[m] == qp[l]) return FHE_EINVAL;
+    }
+    char *base = (char *)host_blob;
+    std::memset(base, 0, lay.bytes);
+    ModupDigit *dg = (ModupDigit *)(base + lay.off_digits);
+    uint64_t *garner = (uint64_t *)(base + lay.off_garner);
+    uint64_t *mr = (uint64_t *)(base + lay.off_mr);
+    for (int j = 0; j < dnum; j++) {
+        const int lo = j * alpha, hi = (lo + alpha < L) ? lo + alpha : L;
+        dg[j].lo = lo;
+        dg[j].count = hi - lo;
+        uint64_t *gj = garner + (size_t)j * alpha * alpha * 2;
+        for (int i = 0; i < hi - lo; i++) {
+            const uint64_t di = qp[lo + i];
+            for (int k = 0; k < i; k++) {
+                const uint64_t c = inv_mod(qp[lo + k] % di, di);
+                gj[(i * alpha + k) * 2] = c;
+                gj[(i * alpha + k) * 2 + 1] = shoup(c, di);
+            }
+        }
+        uint64_t *mj = mr + (size_t)j * LK * alpha * 2;
+        for (int l = 0; l < LK; l++) {
+            const uint64_t p = qp[l];
+            uint64_t prod = 1 % p;
+            for (int i = 0; i < hi - lo; i++) {
+                mj[(l * alpha + i) * 2] = prod;
+                mj[(l * alpha + i) * 2 + 1] = shoup(prod, p);
+                prod = mul_mod(prod, qp[lo + i] % p, p);
+            }
+        }
+    }
+    return FHE_OK;
+}
+
+// ---- host self-test of the device arithmetic (same code, host build) ----
+
+namespace fhe {
+
+int selftest_arith(uint64_t seed, int iters) {
+    uint64_t s = seed ? seed : 0x9E3779B97F4A7C15ull;
+    auto next = [&]() {  // xorshift64*
+        s ^= s >> 12; s ^= s << 25; s ^= s >> 27;
+        return s * 2685821657736338717ull;
+    };
+    uint64_t primes[8];
+    if (fhe_find_primes(17, 50, 4, 0, primes) != FHE_OK) return 1;
+    if (fhe_find_primes(11, 49, 4, 0, primes + 4) != FHE_OK) return 2;
+    primes[7] = primes[7];
+    for (int pi = 0; pi < 8; pi++) {
+        const uint64_t q = primes[pi];
+        if (q <= (1ull << 48)) continue;
+        const uint64_t mu12 = (uint64_t)(((u128)1 << 100) / q) << 12;
+        const uint32_t c58 = (uint32_t)((1ull << 58) / q);
+        for (int it = 0; it < iters; it++) {
+            uint64_t a = next() % q, b = next() % q;
+            if (it < 4) { a = (it & 1) ? q - 1 : 0; b = (it & 2) ? q - 1 : 1; }
+            const uint64_t ref = mul_mod(a, b, q);
+            if (mulmod(a, b, q, mu12) != ref) return 10;
+            const uint64_t y = next() >> (2 + (it % 8));      // up to 62 bits
+            const uint64_t r = shoup_lazy(y, a, shoup(a, q), q);
+            if (r >= 4 * q || r % q != mul_mod(y % q, a, q)) return 11;
+            const uint64_t x = next() >> 6;                     // < 2^58
+            if (reduce_small(x, q, c58) != x % q) return 12;
+            uint64_t h = 0, l = 0;
+            for (int k = 0; k < 1 + it % 24; k++) mac128(h, l, next() % q, next() % q);
+            const u128 T = ((u128)h << 64) | l;
+            if (barrett_reduce128(h, l, q, mu12, c58) != (uint64_t)(T % q)) return 13;
+        }
+    }
+    return 0;
+}
+
+}  // namespace fhe
+
+extern "C" int fhe_selftest_host(uint64_t seed, int iters) {
+    return fhe::selftest_arith(seed, iters) == 0 ? FHE_OK : FHE_EINVAL;
+}
