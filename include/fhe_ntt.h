@@ -205,6 +205,41 @@ int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const 
                      int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
                      const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream);
 
+/* ---- key switch without device allocation ----------------------------- */
+
+/* The pages have no counterpart to this entry point; it serves callers of
+ * this library that cannot allocate device memory: code that runs where
+ * cudaMalloc/cudaFree are not allowed (they can synchronise the device),
+ * services whose GPU memory is partitioned once at start-up, and runtimes
+ * that embed the library without an allocator.
+ *
+ * fhe_keyswitch_ip_noalloc computes exactly what fhe_keyswitch_ip computes
+ * (same arguments minus the workspace, same validation, kernels and
+ * results), taking its workspace from one fixed array in the library's own
+ * device memory of fhe_keyswitch_noalloc_max_bytes() bytes (16 MiB), which
+ * every GPU that loads the library holds until the process exits.
+ *   - Sizes: if fhe_keyswitch_workspace_bytes(log_n, L, K, dnum, batch)
+ *     exceeds that maximum the call returns FHE_ESPACE before any launch
+ *     (e.g. n = 2^13, L+K = 32, dnum = 3 needs 6 MiB and fits; n = 2^16
+ *     with the same basis needs 48 MiB and does not -- use
+ *     fhe_keyswitch_ip with a caller workspace).
+ *   - Allocation: none -- no cudaMalloc, cudaFree or allocating library
+ *     routine is called.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents.  Nothing in it has to start at zero (each call
+ *     writes every word it later reads), but calls whose kernels overlap on
+ *     the GPU (different streams without ordering between them) race on the
+ *     array and give wrong results: order them on one stream or with events. */
+int fhe_keyswitch_ip_noalloc(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
+                             int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
+                             const void *modup, void *stream);
+
+/* Bytes of the fixed workspace behind fhe_keyswitch_ip_noalloc (16 MiB). */
+size_t fhe_keyswitch_noalloc_max_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -63,6 +63,9 @@ SIGNATURES = {
     "fhe_keyswitch_workspace_bytes": (_int, [_int, _int, _int, _int, _int, ctypes.POINTER(_size)]),
     "fhe_keyswitch_ip": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int, ctypes.POINTER(NttTables),
                                 _vp, _vp, _size, _vp]),
+    "fhe_keyswitch_ip_noalloc": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int,
+                                        ctypes.POINTER(NttTables), _vp, _vp]),
+    "fhe_keyswitch_noalloc_max_bytes": (_size, []),
 }
 
 _lib = None

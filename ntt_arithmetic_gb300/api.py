@@ -220,3 +220,24 @@ def keyswitch_ip(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, L: int,
            _ptr(modup.blob), _ptr(workspace), workspace.numel() * workspace.element_size(),
            _stream(x.device, stream))
     return out
+
+
+def keyswitch_ip_noalloc(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, L: int, K: int, dnum: int,
+                         tables_qp: NttTables, modup: ModupTables, stream=None) -> torch.Tensor:
+    """keyswitch_ip without a workspace argument and without any device
+    allocation: the library uses its fixed 16 MiB device array instead (for
+    callers that cannot allocate; see fhe_keyswitch_ip_noalloc in the C
+    header for the size limit and the rule that overlapping calls race).
+    x: [batch, L, n] contiguous; keys: [dnum, 2, L+K, n]; out: [batch, 2, L+K, n]."""
+    for t, nm in ((out, "out"), (x, "x"), (keys, "keys")):
+        _residues(t, nm)
+    n = keys.shape[-1]
+    log_n = _log2(n)
+    if tuple(keys.shape) != (dnum, 2, L + K, n) or x.shape[-2:] != (L, n):
+        raise ValueError("x must be [..., L, n] and keys [dnum, 2, L+K, n]")
+    batch = x.numel() // (L * n)
+    if out.numel() != batch * 2 * (L + K) * n:
+        raise ValueError("out must be [batch, 2, L+K, n]")
+    N.call("fhe_keyswitch_ip_noalloc", _ptr(out), _ptr(x), 0, _ptr(keys), log_n, L, K, dnum, batch,
+           tables_qp.ref(), _ptr(modup.blob), _stream(x.device, stream))
+    return out
