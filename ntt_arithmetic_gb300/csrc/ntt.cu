@@ -232,8 +232,8 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
     }
 }
 
-template <int LOGN, int LOGC, int LOGT, int LOGE>
-__global__ void __launch_bounds__(1 << LOGT)
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+__global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
@@ -400,8 +400,8 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
     }
 }
 
-template <int LOGN, int LOGC, int LOGT, int LOGE>
-__global__ void __launch_bounds__(1 << LOGT)
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+__global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
@@ -422,11 +422,11 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
 
 // ---------------------------------------------------------------- launch --
 
-template <int LOGN, int LOGC, int LOGT, int LOGE>
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool inverse, cudaStream_t st) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     void (*kern)(uint64_t *, int, const ulonglong2 *, const uint64_t *) =
-        inverse ? k_ntt_inv<LOGN, LOGC, LOGT, LOGE> : k_ntt_fwd<LOGN, LOGC, LOGT, LOGE>;
+        inverse ? k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB> : k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
     const size_t smem = (size_t)SH::M * sizeof(uint64_t);
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -451,27 +451,61 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
 
 }  // namespace
 
+// Launch shape per log2(n): cluster size (log2 C), threads per CTA (log2 T),
+// residues per thread (log2 E, = radix of a register pass) and the minimum
+// number of resident CTAs per SM the register allocation must allow.
+#define FHE_SHAPE_1 0, 0, 1, 1
+#define FHE_SHAPE_2 0, 0, 2, 1
+#define FHE_SHAPE_3 0, 0, 3, 1
+#define FHE_SHAPE_4 0, 1, 3, 1
+#define FHE_SHAPE_5 0, 2, 3, 1
+#define FHE_SHAPE_6 0, 3, 3, 1
+#define FHE_SHAPE_7 0, 4, 3, 1
+#define FHE_SHAPE_8 0, 5, 3, 1
+#define FHE_SHAPE_9 0, 6, 3, 1
+#define FHE_SHAPE_10 0, 7, 3, 1
+#ifndef FHE_SHAPE_11
+#define FHE_SHAPE_11 0, 7, 4, 4
+#endif
+#ifndef FHE_SHAPE_12
+#define FHE_SHAPE_12 0, 8, 4, 2
+#endif
+#ifndef FHE_SHAPE_13
+#define FHE_SHAPE_13 0, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_14
+#define FHE_SHAPE_14 1, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_15
+#define FHE_SHAPE_15 2, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_16
+#define FHE_SHAPE_16 3, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_17
+#define FHE_SHAPE_17 3, 9, 5, 1
+#endif
+
 int launch_ntt(uint64_t *res, int log_n, int L, long rows, const fhe_ntt_tables *t, bool inverse, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     switch (log_n) {
-        //                        LOGN LOGC LOGT LOGE
-        case 1: return launch_shape<1, 0, 0, 1>(res, L, rows, t, inverse, st);
-        case 2: return launch_shape<2, 0, 0, 2>(res, L, rows, t, inverse, st);
-        case 3: return launch_shape<3, 0, 0, 3>(res, L, rows, t, inverse, st);
-        case 4: return launch_shape<4, 0, 1, 3>(res, L, rows, t, inverse, st);
-        case 5: return launch_shape<5, 0, 2, 3>(res, L, rows, t, inverse, st);
-        case 6: return launch_shape<6, 0, 3, 3>(res, L, rows, t, inverse, st);
-        case 7: return launch_shape<7, 0, 4, 3>(res, L, rows, t, inverse, st);
-        case 8: return launch_shape<8, 0, 5, 3>(res, L, rows, t, inverse, st);
-        case 9: return launch_shape<9, 0, 6, 3>(res, L, rows, t, inverse, st);
-        case 10: return launch_shape<10, 0, 7, 3>(res, L, rows, t, inverse, st);
-        case 11: return launch_shape<11, 0, 7, 4>(res, L, rows, t, inverse, st);
-        case 12: return launch_shape<12, 0, 8, 4>(res, L, rows, t, inverse, st);
-        case 13: return launch_shape<13, 0, 8, 5>(res, L, rows, t, inverse, st);
-        case 14: return launch_shape<14, 1, 8, 5>(res, L, rows, t, inverse, st);
-        case 15: return launch_shape<15, 2, 8, 5>(res, L, rows, t, inverse, st);
-        case 16: return launch_shape<16, 3, 8, 5>(res, L, rows, t, inverse, st);
-        case 17: return launch_shape<17, 3, 9, 5>(res, L, rows, t, inverse, st);
+        case 1: return launch_shape<1, FHE_SHAPE_1>(res, L, rows, t, inverse, st);
+        case 2: return launch_shape<2, FHE_SHAPE_2>(res, L, rows, t, inverse, st);
+        case 3: return launch_shape<3, FHE_SHAPE_3>(res, L, rows, t, inverse, st);
+        case 4: return launch_shape<4, FHE_SHAPE_4>(res, L, rows, t, inverse, st);
+        case 5: return launch_shape<5, FHE_SHAPE_5>(res, L, rows, t, inverse, st);
+        case 6: return launch_shape<6, FHE_SHAPE_6>(res, L, rows, t, inverse, st);
+        case 7: return launch_shape<7, FHE_SHAPE_7>(res, L, rows, t, inverse, st);
+        case 8: return launch_shape<8, FHE_SHAPE_8>(res, L, rows, t, inverse, st);
+        case 9: return launch_shape<9, FHE_SHAPE_9>(res, L, rows, t, inverse, st);
+        case 10: return launch_shape<10, FHE_SHAPE_10>(res, L, rows, t, inverse, st);
+        case 11: return launch_shape<11, FHE_SHAPE_11>(res, L, rows, t, inverse, st);
+        case 12: return launch_shape<12, FHE_SHAPE_12>(res, L, rows, t, inverse, st);
+        case 13: return launch_shape<13, FHE_SHAPE_13>(res, L, rows, t, inverse, st);
+        case 14: return launch_shape<14, FHE_SHAPE_14>(res, L, rows, t, inverse, st);
+        case 15: return launch_shape<15, FHE_SHAPE_15>(res, L, rows, t, inverse, st);
+        case 16: return launch_shape<16, FHE_SHAPE_16>(res, L, rows, t, inverse, st);
+        case 17: return launch_shape<17, FHE_SHAPE_17>(res, L, rows, t, inverse, st);
         default: return -1;
     }
 }
