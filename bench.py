@@ -62,11 +62,51 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def ntt_fwd_traffic():
+    """DRAM bytes per forward-NTT launch from the committed ncu capture, or
+    None when the kernel source has changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)["k_ntt_fwd"]
+        h = hashlib.sha256()
+        for path in rec["source_files"]:
+            with open(os.path.join(ROOT, path), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != rec["source_sha256_16"] or rec["rows_per_launch"] != NPOLY * L:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank transforms its own shard of ciphertexts (weak scaling, no
+    data exchange): rank r draws its inputs from seed 3 + 1000 r."""
+    return 3 + 1000 * rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank time over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, max_ms: float) -> float:
+    """Units processed by all ranks per second of the slowest rank."""
+    return units_per_rank * world / (max_ms * 1e-3)
 
 
 # --------------------------------------------------------------- clocks ---
@@ -126,7 +166,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
-def build_state(device):
+def build_state(device, seed: int = 3):
     import torch
     from ntt_arithmetic_gb300 import api, inputs
     q = api.find_primes(LOG_N, L)
@@ -136,8 +176,8 @@ def build_state(device):
     st["tq"] = api.NttTables(LOG_N, q, device)
     st["tqp"] = api.NttTables(LOG_N, qp, device)
     st["modup"] = api.ModupTables(L, K, DNUM, qp, device)
-    x_host = inputs.uniform_residues((2, PAIRS, 2, L, N), q, seed=3, buffer=0)
-    keys_host = inputs.uniform_residues((DNUM, 2, L + K, N), qp, seed=3, buffer=1)
+    x_host = inputs.uniform_residues((2, PAIRS, 2, L, N), q, seed=seed, buffer=0)
+    keys_host = inputs.uniform_residues((DNUM, 2, L + K, N), qp, seed=seed, buffer=1)
     st["x_pinned"] = torch.from_numpy(x_host).pin_memory()
     st["X"] = st["x_pinned"].to(device)
     st["keys"] = torch.from_numpy(keys_host).to(device)
@@ -187,7 +227,7 @@ def ours(args):
         B.build()
     if ws > 1:
         dist.barrier()
-    st = build_state(device)
+    st = build_state(device, rank_seed(rank))
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -212,10 +252,7 @@ def ours(args):
     ms = start.elapsed_time(stop) / args.steps
     per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)]
     kern = [statistics.mean(p[j] for p in per) for j in range(6)]
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, device)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's input, the whole step, D2H of its key-switch output
@@ -229,11 +266,7 @@ def ours(args):
         st["ks_pinned"].copy_(st["KS"], non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-    if ws > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
 
     clocks = clk.summary()
     hbm, hbm_kind = peaks()
@@ -241,7 +274,7 @@ def ours(args):
     achieved_bfly = BFLY_PER_FWD / fwd_s
     line = {
         "metric": METRIC,
-        "value": UNITS * ws / (ms_max * 1e-3),
+        "value": whole_job_rate(UNITS, ws, ms_max),
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
@@ -262,12 +295,13 @@ def ours(args):
         "ntt_fwd_hbm_frac": NTT_BYTES_PER_FWD / fwd_s / 1e9 / hbm,
         "keyswitch_ops_per_s": PAIRS / (kern[5] * 1e-3) * ws,
         "roofline": {"bound": "alu", "achieved": achieved_bfly / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
-                     "unit": "Gbutterfly/s", "frac": achieved_bfly / ALU_PEAK_BFLY, "traffic": None,
+                     "unit": "Gbutterfly/s", "frac": achieved_bfly / ALU_PEAK_BFLY, "traffic": ntt_fwd_traffic(),
+                     "traffic_unit": "bytes/launch", "algorithmic_bytes": NTT_BYTES_PER_FWD,
                      "kernel": "k_ntt_fwd<16,3,8,5> (cluster NTT, n=2^16, 384 rows)",
                      "hbm_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9, "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind},
         "clocks": clocks,
         "gpu_launches": launches,
-        "e2e": {"value": UNITS * ws / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": whole_job_rate(UNITS, ws, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": st["x_pinned"].numel() * 8, "d2h_bytes_per_step": st["ks_pinned"].numel() * 8},
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
