@@ -99,7 +99,8 @@ typedef struct fhe_ntt_tables {
     const uint64_t *q;        /* [L] moduli */
     const uint64_t *consts;   /* [L][16] per-prime constants */
     const uint64_t *fwd;      /* [L][n][2] forward twiddles and Shoup companions */
-    const uint64_t *inv;      /* [L][n][2] inverse twiddles and Shoup companions */
+    const uint64_t *inv;      /* [L][n][2] inverse (cyclic) twiddles and companions */
+    const uint64_t *twist;    /* [L][n][2] n^-1 psi^-j and companions */
     const void *blob;         /* base of the device blob */
     size_t bytes;             /* blob size */
 } fhe_ntt_tables;

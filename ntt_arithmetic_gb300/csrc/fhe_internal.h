@@ -14,7 +14,7 @@ constexpr int kMaxBasis = 64;     // L + K of a key switch
 constexpr int kMaxAlpha = 16;     // primes per key-switch digit
 
 struct NttLayout {
-    size_t off_q, off_consts, off_fwd, off_inv, bytes;
+    size_t off_q, off_consts, off_fwd, off_inv, off_twist, bytes;
 };
 NttLayout ntt_layout(int log_n, int L);
 

@@ -18,12 +18,14 @@
 //   * local stages s >= LOGC run in passes of up to LOGE stages: a thread
 //     holds 2^LOGE residues (radix-2^LOGE in registers), with one shared-
 //     memory round trip and one __syncthreads between passes.
-// Inverse (bit-reversed -> natural, Gentleman-Sande with psi^-brv, n^-1 in
-//   the last stage): the mirror image -- local passes first, cross stages last.
+// Inverse (bit-reversed -> natural): cyclic Cooley-Tukey (decimation in time)
+//   with omega^-1 = psi^-2 followed by the twist n^-1 psi^-j; local passes
+//   first (spans 1, 2, 4, ...), cross stages last -- the mirror image.
 //
-// Arithmetic: lazy Shoup butterflies (fhe_arith.cuh).  Forward values grow by
-// < 4q per stage with no comparisons (< 69 q < 2^57 after 17 stages) and are
-// reduced once before the store; inverse values stay below 4q.
+// Arithmetic: lazy Shoup butterflies (fhe_arith.cuh).  Values grow by < 4q
+// per stage with no comparisons (forward: < 69 q after 17 stages; inverse:
+// < 128 q, the twiddle-1 butterflies of its first pass doubling instead) and
+// are reduced once, before the store.
 //
 // Shared-memory index swizzle: index p is stored at p ^ (((p >> LOGE) & 7) << 1),
 // which makes every pass's accesses bank-conflict-free (two wavefronts per
@@ -234,7 +236,8 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
 
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
-k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
+k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts,
+          const ulonglong2 *__restrict__) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
@@ -283,90 +286,121 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
 }
 
 // ---------------------------------------------------------------- inverse --
+//
+// Cyclic Cooley-Tukey (decimation in time) on the bit-reversed input, then the
+// twist n^-1 psi^-j on natural-order output j:
+//   a_j = n^-1 psi^-j sum_k A_k omega^-jk,  omega = psi^2,  A[k] stored at brv(k).
+// The stage of span h = 2^e pairs p and p + h (p mod 2h < h) and multiplies the
+// second by omega_2h^-(p mod h) = inv[h + (p mod h)], so all butterflies are the
+// comparison-free lazy Cooley-Tukey kind; values grow by < 4q per stage.  In
+// the first register pass (spans 1 .. 2^(LOGE-1)) the twiddles are the same
+// for every thread and one in 2^i butterflies of stage i has twiddle 1, whose
+// multiplication is skipped.
 
-// Local GS stage I of a pass over bits [B, B+EP): stride bit KB = B + I,
-// twiddle psi^-brv(n/2^(KB+1) + (p >> (KB+1))), 2^(EP-1-I) per group.
-template <class SH, int B, int EP, int I, bool LASTG>
+// Bound, in units of q, of the values entering stage I of the first pass:
+// inputs are < q; a twiddle-1 butterfly doubles the bound, the others add 4q.
+template <int I>
+struct FirstBound {
+    static constexpr int prev = FirstBound<I - 1>::value;
+    static constexpr int value = 2 * prev > prev + 4 ? 2 * prev : prev + 4;
+};
+template <>
+struct FirstBound<0> {
+    static constexpr int value = 1;
+};
+
+// Local stage I of an inverse pass over bits [B, B+EP): span 2^(B+I), register
+// distance 2^I, twiddle inv[2^(B+I) + (p mod 2^(B+I))].
+template <class SH, int B, int EP, int I>
 __device__ __forceinline__ void inv_stage(uint64_t (&x)[SH::E], const Ctx &c) {
     constexpr int G = SH::E >> EP, EPN = 1 << EP;
     constexpr int KB = B + I;
     constexpr int HALF = 1 << I;
-    constexpr int NW = 1 << (EP - 1 - I);
-    constexpr bool LAST = LASTG && (I == EP - 1);
+    constexpr int NH = EPN / (2 * HALF);
 #pragma unroll
     for (int k = 0; k < G; k++) {
         const int g = c.t + SH::T * k;
-        if constexpr (LAST) {
-            const uint64_t ni = c.kc[K_NINV], nip = c.kc[K_NINV_S], wn = c.kc[K_W1NINV], wnp = c.kc[K_W1NINV_S];
+        const int gl = g & ((1 << B) - 1);
 #pragma unroll
-            for (int u = 0; u < HALF; u++) gs_bfly_last(x[k * EPN + u], x[k * EPN + u + HALF], ni, nip, wn, wnp, c.q);
-        } else {
-            const int base = (SH::N >> (KB + 1)) + (c.r << (SH::LOGM - KB - 1)) + ((g >> B) << (EP - I - 1));
+        for (int jl = 0; jl < HALF; jl++) {
+            if (B == 0 && jl == 0) {
+                const uint64_t bnd = (uint64_t)FirstBound<I>::value * c.q;
 #pragma unroll
-            for (int jj = 0; jj < NW; jj++) {
-                const ulonglong2 w = __ldg(c.tw + base + jj);
+                for (int jh = 0; jh < NH; jh++) {
+                    const int j = jh * 2 * HALF;
+                    ct_bfly_one(x[k * EPN + j], x[k * EPN + j + HALF], bnd);
+                }
+            } else {
+                const ulonglong2 w = __ldg(c.tw + (1 << KB) + gl + (jl << B));
 #pragma unroll
-                for (int u = 0; u < HALF; u++) {
-                    const int j = jj * 2 * HALF + u;
-                    gs_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
+                for (int jh = 0; jh < NH; jh++) {
+                    const int j = jh * 2 * HALF + jl;
+                    ct_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
                 }
             }
         }
     }
 }
 
-template <class SH, int B, int EP, bool LASTG, int I = 0>
+template <class SH, int B, int EP, int I = 0>
 __device__ __forceinline__ void inv_compute(uint64_t (&x)[SH::E], const Ctx &c) {
     if constexpr (I < EP) {
-        inv_stage<SH, B, EP, I, LASTG>(x, c);
-        inv_compute<SH, B, EP, LASTG, I + 1>(x, c);
+        inv_stage<SH, B, EP, I>(x, c);
+        inv_compute<SH, B, EP, I + 1>(x, c);
     }
 }
 
-// Cross-CTA GS stages: stride bit LOGM + S, pairs (j1, j1 + 2^S).
+// Cross-CTA stages: span M 2^S, pairs (j1, j1 + 2^S) of every column,
+// twiddle inv[M (2^S + (j1 mod 2^S)) + j2].
 template <class SH, int S>
 __device__ __forceinline__ void cross_inv(uint64_t (&x)[SH::E], const Ctx &c) {
     if constexpr (S < SH::LOGC) {
-        constexpr int C = SH::C, COLS = SH::E / C, H = 1 << S;
-        if constexpr (S == SH::LOGC - 1) {
-            const uint64_t ni = c.kc[K_NINV], nip = c.kc[K_NINV_S], wn = c.kc[K_W1NINV], wnp = c.kc[K_W1NINV_S];
+        constexpr int C = SH::C, PAIRS = SH::E / C / 2, H = 1 << S;
 #pragma unroll
-            for (int j1 = 0; j1 < C; j1++) {
-                if (j1 & H) continue;
+        for (int cp = 0; cp < PAIRS; cp++) {
+            const int j2 = col_j2<SH>(cp, c.t, c.r);
 #pragma unroll
-                for (int col = 0; col < COLS; col++)
-                    gs_bfly_last(x[col * C + j1], x[col * C + j1 + H], ni, nip, wn, wnp, c.q);
-            }
-        } else {
+            for (int jlo = 0; jlo < H; jlo++) {
+                const ulonglong2 *tw = c.tw + (long)SH::M * (H + jlo) + j2;
+                const ulonglong2 w0 = __ldg(tw), w1 = __ldg(tw + 1);
 #pragma unroll
-            for (int j1 = 0; j1 < C; j1++) {
-                if (j1 & H) continue;
-                const ulonglong2 w = __ldg(c.tw + (C >> (S + 1)) + (j1 >> (S + 1)));
-#pragma unroll
-                for (int col = 0; col < COLS; col++) gs_bfly(x[col * C + j1], x[col * C + j1 + H], w.x, w.y, c.q);
+                for (int jhi = 0; jhi < C / (2 * H); jhi++) {
+                    const int j1 = jhi * 2 * H + jlo;
+                    ct_bfly(x[(2 * cp) * C + j1], x[(2 * cp) * C + j1 + H], w0.x, w0.y, c.q);
+                    ct_bfly(x[(2 * cp + 1) * C + j1], x[(2 * cp + 1) * C + j1 + H], w1.x, w1.y, c.q);
+                }
             }
         }
         cross_inv<SH, S + 1>(x, c);
     }
 }
 
+// x <- x * n^-1 psi^-p mod q, fully reduced (x < 2^57 on entry)
+__device__ __forceinline__ uint64_t twist(uint64_t x, ulonglong2 t, uint64_t q) {
+    return reduce4(shoup_lazy(x, t.x, t.y, q), q);
+}
+
 template <class SH, int PI>
 __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, uint64_t *data,
-                                           const Ctx &c) {
+                                           const ulonglong2 *tws, const Ctx &c) {
     constexpr int LOGE = SH::LOGE;
     constexpr int B = PI * LOGE;
     constexpr int EP = PI == SH::P - 1 ? SH::EREM : LOGE;
-    constexpr bool LASTG = (SH::C == 1) && (PI == SH::P - 1);
-    inv_compute<SH, B, EP, LASTG>(x, c);
+    inv_compute<SH, B, EP>(x, c);
     if constexpr (PI + 1 < SH::P) {
         smem_store<SH, B, EP>(x, sm, c.t);
         __syncthreads();
         constexpr int EP2 = PI + 1 == SH::P - 1 ? SH::EREM : LOGE;
         smem_load<SH, B + LOGE, EP2>(x, sm, c.t);
-        inv_passes<SH, PI + 1>(x, sm, blk, data, c);
+        inv_passes<SH, PI + 1>(x, sm, blk, data, tws, c);
     } else if constexpr (SH::C == 1) {
+        constexpr int G = SH::E >> EP, EPN = 1 << EP;
 #pragma unroll
-        for (int i = 0; i < SH::E; i++) x[i] = reduce4(x[i], c.q);
+        for (int k = 0; k < G; k++) {
+            const int g = c.t + SH::T * k;
+#pragma unroll
+            for (int j = 0; j < EPN; j++) x[k * EPN + j] = twist(x[k * EPN + j], __ldg(tws + pass_pos<B, EP>(g, j)), c.q);
+        }
         global_store<SH, B, EP>(x, blk, c.t);
     } else {
         constexpr int C = SH::C, PAIRS = SH::E / C / 2;
@@ -386,14 +420,15 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         }
         cross_inv<SH, 0>(x, c);
 #pragma unroll
-        for (int i = 0; i < SH::E; i++) x[i] = reduce4(x[i], c.q);
-#pragma unroll
         for (int cp = 0; cp < PAIRS; cp++) {
             const int j2 = col_j2<SH>(cp, c.t, c.r);
 #pragma unroll
-            for (int j1 = 0; j1 < C; j1++)
-                __stcs(reinterpret_cast<ulonglong2 *>(data + (long)j1 * SH::M + j2),
-                       make_ulonglong2(x[(2 * cp) * C + j1], x[(2 * cp + 1) * C + j1]));
+            for (int j1 = 0; j1 < C; j1++) {
+                const long p = (long)j1 * SH::M + j2;
+                const uint64_t y0 = twist(x[(2 * cp) * C + j1], __ldg(tws + p), c.q);
+                const uint64_t y1 = twist(x[(2 * cp + 1) * C + j1], __ldg(tws + p + 1), c.q);
+                __stcs(reinterpret_cast<ulonglong2 *>(data + p), make_ulonglong2(y0, y1));
+            }
         }
         cluster_arrive();   // keep this CTA's shared memory alive until every peer has read it
         cluster_wait();
@@ -402,7 +437,8 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
 
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
-k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
+k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts,
+          const ulonglong2 *__restrict__ twist_tab) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
@@ -417,7 +453,7 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
     uint64_t x[SH::E];
     uint64_t *blk = data + (long)c.r * SH::M;
     global_load<SH, 0, (SH::P == 1 ? SH::EREM : LOGE)>(x, blk, c.t);
-    inv_passes<SH, 0>(x, sm, blk, data, c);
+    inv_passes<SH, 0>(x, sm, blk, data, twist_tab + (long)l * SH::N, c);   // indexed by global position
 }
 
 // ---------------------------------------------------------------- launch --
@@ -425,7 +461,7 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool inverse, cudaStream_t st) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
-    void (*kern)(uint64_t *, int, const ulonglong2 *, const uint64_t *) =
+    void (*kern)(uint64_t *, int, const ulonglong2 *, const uint64_t *, const ulonglong2 *) =
         inverse ? k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB> : k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
     const size_t smem = (size_t)SH::M * sizeof(uint64_t);
     if (smem > 48 * 1024) {
@@ -445,7 +481,8 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
     cfg.attrs = attr;
     cfg.numAttrs = SH::C > 1 ? 1 : 0;
     const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(inverse ? t->inv : t->fwd);
-    if (cudaLaunchKernelEx(&cfg, kern, res, L, tw, t->consts) != cudaSuccess) return -1;
+    const ulonglong2 *twist_tab = reinterpret_cast<const ulonglong2 *>(t->twist);
+    if (cudaLaunchKernelEx(&cfg, kern, res, L, tw, t->consts, twist_tab) != cudaSuccess) return -1;
     return 1;
 }
 

@@ -95,7 +95,8 @@ NttLayout ntt_layout(int log_n, int L) {
     s.off_consts = align256(s.off_q + (size_t)L * 8);
     s.off_fwd = align256(s.off_consts + (size_t)L * K_COUNT * 8);
     s.off_inv = align256(s.off_fwd + (size_t)L * n * 16);
-    s.bytes = align256(s.off_inv + (size_t)L * n * 16);
+    s.off_twist = align256(s.off_inv + (size_t)L * n * 16);
+    s.bytes = align256(s.off_twist + (size_t)L * n * 16);
     return s;
 }
 
@@ -164,6 +165,7 @@ extern "C" int fhe_ntt_tables_build_host(int log_n, int L, const uint64_t *q, vo
     uint64_t *kc = (uint64_t *)(base + lay.off_consts);
     uint64_t *fwd = (uint64_t *)(base + lay.off_fwd);
     uint64_t *inv = (uint64_t *)(base + lay.off_inv);
+    uint64_t *twist = (uint64_t *)(base + lay.off_twist);
     std::vector<uint64_t> pw(n), ipw(n);
     for (int l = 0; l < L; l++) {
         const uint64_t ql = q[l];
@@ -174,27 +176,34 @@ extern "C" int fhe_ntt_tables_build_host(int log_n, int L, const uint64_t *q, vo
             pw[i] = mul_mod(pw[i - 1], psi, ql);
             ipw[i] = mul_mod(ipw[i - 1], psi_inv, ql);
         }
-        uint64_t *f = fwd + (size_t)l * n * 2, *g = inv + (size_t)l * n * 2;
+        uint64_t *f = fwd + (size_t)l * n * 2, *g = inv + (size_t)l * n * 2, *tw = twist + (size_t)l * n * 2;
+        const uint64_t ninv = inv_mod(n % ql, ql);
         for (uint64_t k = 0; k < n; k++) {
-            // k-th twiddle = psi^brv(k) (forward) and psi^-brv(k) (inverse), brv over log_n bits
+            // forward (psi-merged, bit-reversed): fwd[k] = psi^brv(k), brv over log_n bits
             const uint64_t w = pw[bit_reverse((uint32_t)k, log_n)];
-            const uint64_t wi = ipw[bit_reverse((uint32_t)k, log_n)];
             f[2 * k] = w;
             f[2 * k + 1] = shoup(w, ql);
-            g[2 * k] = wi;
-            g[2 * k + 1] = shoup(wi, ql);
+            // twist of the inverse: twist[j] = n^-1 psi^-j
+            const uint64_t tj = mul_mod(ninv, ipw[k], ql);
+            tw[2 * k] = tj;
+            tw[2 * k + 1] = shoup(tj, ql);
+        }
+        // cyclic inverse: inv[h + j] = omega_2h^-j = psi^(-j n / h) for h = 2^e < n, j < h
+        g[0] = 1;
+        g[1] = shoup(1, ql);
+        for (uint64_t h = 1; h < n; h <<= 1) {
+            for (uint64_t j = 0; j < h; j++) {
+                const uint64_t wi = ipw[(j * (n / h)) % n];   // j n / h < n
+                g[2 * (h + j)] = wi;
+                g[2 * (h + j) + 1] = shoup(wi, ql);
+            }
         }
         uint64_t *c = kc + (size_t)l * K_COUNT;
-        const uint64_t ninv = inv_mod(n % ql, ql);
-        const uint64_t w1ninv = mul_mod(ipw[bit_reverse(1, log_n)], ninv, ql);
         qv[l] = ql;
         c[K_Q] = ql;
         c[K_MU12] = (uint64_t)(((u128)1 << 100) / ql) << 12;
         c[K_C58] = (uint64_t)((1ull << 58) / ql);
         c[K_NINV] = ninv;
-        c[K_NINV_S] = shoup(ninv, ql);
-        c[K_W1NINV] = w1ninv;
-        c[K_W1NINV_S] = shoup(w1ninv, ql);
         c[K_PSI] = psi;
     }
     return FHE_OK;
@@ -212,6 +221,7 @@ extern "C" int fhe_ntt_tables_bind(const void *dev_blob, size_t bytes, int log_n
     out->consts = (const uint64_t *)(base + lay.off_consts);
     out->fwd = (const uint64_t *)(base + lay.off_fwd);
     out->inv = (const uint64_t *)(base + lay.off_inv);
+    out->twist = (const uint64_t *)(base + lay.off_twist);
     out->blob = dev_blob;
     out->bytes = lay.bytes;
     return FHE_OK;

@@ -78,8 +78,10 @@ def test_root_of_unity_matches_oracle(lib, log_n):
 
 
 def test_tables_contents(lib):
-    """Spot-check the table blob against the definition: fwd[k] = psi^brv(k),
-    inv[k] = psi^-brv(k), Shoup companions floor(w 2^64 / q)."""
+    """Spot-check the table blob against the definitions: fwd[k] = psi^brv(k)
+    (merged forward), inv[h + j] = psi^(-j n / h) for h = 2^e (cyclic inverse
+    twiddles omega_2h^-j), twist[j] = n^-1 psi^-j, each with its Shoup
+    companion floor(w 2^64 / q)."""
     log_n, L = 6, 3
     n = 1 << log_n
     qs = [int(v) for v in oracle.primes(2 * n, L)]
@@ -95,13 +97,18 @@ def test_tables_contents(lib):
     assert list(words(t.q, L)) == qs
     fwd = words(t.fwd, L * n * 2).reshape(L, n, 2)
     inv = words(t.inv, L * n * 2).reshape(L, n, 2)
+    twi = words(t.twist, L * n * 2).reshape(L, n, 2)
     for l, q in enumerate(qs):
         psi = oracle.psi(q, 2 * n)
         for k in range(1, n):
-            e = oracle.brv(k, log_n)
-            w, wi = pow(psi, e, q), pow(psi, -e, q)
+            w = pow(psi, oracle.brv(k, log_n), q)
             assert int(fwd[l, k, 0]) == w and int(fwd[l, k, 1]) == (w << 64) // q
+            h = 1 << (k.bit_length() - 1)
+            wi = pow(psi, -(k - h) * (n // h), q)
             assert int(inv[l, k, 0]) == wi and int(inv[l, k, 1]) == (wi << 64) // q
+        for j in range(n):
+            tj = pow(n, -1, q) * pow(psi, -j, q) % q
+            assert int(twi[l, j, 0]) == tj and int(twi[l, j, 1]) == (tj << 64) // q
 
 
 def test_table_builder_rejects_bad_moduli(lib):
