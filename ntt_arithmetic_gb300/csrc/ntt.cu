@@ -49,7 +49,10 @@ struct Shape {
     static constexpr int P = (LOGM + LOGE - 1) / LOGE;     // local passes
     static constexpr int EREM = LOGM - (P - 1) * LOGE;     // stages in the odd-sized pass
     static_assert(LOGM == LOGT + LOGE, "M = T * E");
-    static_assert(LOGC == 0 || (E / C) % 2 == 0, "cross phase moves 16-byte column pairs");
+    static_assert(LOGC <= LOGE, "a thread holds at least one whole column");
+    // cross phase: each thread owns COLS columns of C residues, moved in
+    // groups of W adjacent columns (16-byte accesses when W = 2)
+    static constexpr int COLS = E / C, W = COLS % 2 == 0 ? 2 : 1, NG = COLS / W;
 };
 
 struct Ctx {
@@ -158,6 +161,30 @@ __device__ __forceinline__ void global_store(const uint64_t (&x)[SH::E], uint64_
     }
 }
 
+// Coalesced copies of the CTA's block between HBM (natural order) and shared
+// memory (swizzled): each warp instruction moves 512 contiguous bytes.  The
+// register passes that touch the lowest index bits hold 2^LOGE consecutive
+// residues per thread, so reading or writing HBM straight from them would
+// scatter every warp access over 32 lines; staging through shared memory
+// (conflict-free under the swizzle) avoids that.
+template <class SH>
+__device__ __forceinline__ void block_load_coalesced(uint64_t *sm, const uint64_t *blk, int t) {
+#pragma unroll
+    for (int k = 0; k < SH::E / 2; k++) {
+        const int p = 2 * (t + SH::T * k);
+        *reinterpret_cast<ulonglong2 *>(sm + swz<SH::LOGE>(p)) = __ldcs(reinterpret_cast<const ulonglong2 *>(blk + p));
+    }
+}
+
+template <class SH>
+__device__ __forceinline__ void block_store_coalesced(const uint64_t *sm, uint64_t *blk, int t) {
+#pragma unroll
+    for (int k = 0; k < SH::E / 2; k++) {
+        const int p = 2 * (t + SH::T * k);
+        __stcs(reinterpret_cast<ulonglong2 *>(blk + p), *reinterpret_cast<const ulonglong2 *>(sm + swz<SH::LOGE>(p)));
+    }
+}
+
 // ---------------------------------------------------------------- forward --
 
 // Local stage I of a pass over bits [B, B+EP): global stage s = LOGN-B-EP+I,
@@ -208,10 +235,39 @@ __device__ __forceinline__ void cross_fwd(uint64_t (&x)[SH::E], const Ctx &c) {
     }
 }
 
-// Column j2 of thread-local column index col: pairs of adjacent columns.
+// First column j2 of the thread's column group cg (W adjacent columns).
 template <class SH>
-__device__ __forceinline__ int col_j2(int cp, int t, int r) {
-    return r * (SH::M / SH::C) + 2 * (cp * SH::T + t);
+__device__ __forceinline__ int col_j2(int cg, int t, int r) {
+    return r * (SH::M / SH::C) + SH::W * (cg * SH::T + t);
+}
+
+// Column-group access: residues (j1, j2 .. j2 + W - 1) <-> x[(W cg + h) C + j1].
+template <class SH>
+__device__ __forceinline__ void col_get(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
+    if constexpr (SH::W == 2) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(p);
+        x[(2 * cg) * SH::C + j1] = v.x;
+        x[(2 * cg + 1) * SH::C + j1] = v.y;
+    } else {
+        x[cg * SH::C + j1] = *p;
+    }
+}
+template <class SH>
+__device__ __forceinline__ void col_get_cs(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
+    if constexpr (SH::W == 2) {
+        const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(p));
+        x[(2 * cg) * SH::C + j1] = v.x;
+        x[(2 * cg + 1) * SH::C + j1] = v.y;
+    } else {
+        x[cg * SH::C + j1] = __ldcs(p);
+    }
+}
+template <class SH>
+__device__ __forceinline__ void col_put(const uint64_t (&x)[SH::E], int cg, int j1, uint64_t *p) {
+    if constexpr (SH::W == 2)
+        *reinterpret_cast<ulonglong2 *>(p) = make_ulonglong2(x[(2 * cg) * SH::C + j1], x[(2 * cg + 1) * SH::C + j1]);
+    else
+        *p = x[cg * SH::C + j1];
 }
 
 template <class SH, int PI>
@@ -230,7 +286,13 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         const uint32_t c58 = (uint32_t)c.kc[K_C58];
 #pragma unroll
         for (int i = 0; i < SH::E; i++) x[i] = reduce_small(x[i], c.q, c58);
-        global_store<SH, B, EP>(x, blk, c.t);
+        if constexpr (B == 0 && SH::E >= 2) {
+            smem_store<SH, B, EP>(x, sm, c.t);   // each thread rewrites the positions it read
+            __syncthreads();
+            block_store_coalesced<SH>(sm, blk, c.t);
+        } else {
+            global_store<SH, B, EP>(x, blk, c.t);
+        }
     }
 }
 
@@ -251,17 +313,13 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
     c.q = c.kc[K_Q];
     uint64_t x[SH::E];
     if constexpr (SH::C > 1) {
-        constexpr int C = SH::C, PAIRS = SH::E / C / 2;
+        constexpr int C = SH::C;
         cluster_arrive_relaxed();
 #pragma unroll
-        for (int cp = 0; cp < PAIRS; cp++) {
-            const int j2 = col_j2<SH>(cp, c.t, c.r);
+        for (int cg = 0; cg < SH::NG; cg++) {
+            const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
-            for (int j1 = 0; j1 < C; j1++) {
-                const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(data + (long)j1 * SH::M + j2));
-                x[(2 * cp) * C + j1] = v.x;
-                x[(2 * cp + 1) * C + j1] = v.y;
-            }
+            for (int j1 = 0; j1 < C; j1++) col_get_cs<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
         }
         cross_fwd<SH, 0>(x, c);
         cluster_wait();   // every CTA of the cluster has started: DSMEM is live
@@ -270,11 +328,7 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
         for (int j1 = 0; j1 < C; j1++) {
             uint64_t *dst = cl.map_shared_rank(sm, (unsigned)j1);
 #pragma unroll
-            for (int cp = 0; cp < PAIRS; cp++) {
-                const int j2 = col_j2<SH>(cp, c.t, c.r);
-                *reinterpret_cast<ulonglong2 *>(dst + swz<LOGE>(j2)) =
-                    make_ulonglong2(x[(2 * cp) * C + j1], x[(2 * cp + 1) * C + j1]);
-            }
+            for (int cg = 0; cg < SH::NG; cg++) col_put<SH>(x, cg, j1, dst + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
         }
         cluster_arrive();
         cluster_wait();
@@ -355,19 +409,22 @@ __device__ __forceinline__ void inv_compute(uint64_t (&x)[SH::E], const Ctx &c) 
 template <class SH, int S>
 __device__ __forceinline__ void cross_inv(uint64_t (&x)[SH::E], const Ctx &c) {
     if constexpr (S < SH::LOGC) {
-        constexpr int C = SH::C, PAIRS = SH::E / C / 2, H = 1 << S;
+        constexpr int C = SH::C, H = 1 << S;
 #pragma unroll
-        for (int cp = 0; cp < PAIRS; cp++) {
-            const int j2 = col_j2<SH>(cp, c.t, c.r);
+        for (int cg = 0; cg < SH::NG; cg++) {
+            const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
             for (int jlo = 0; jlo < H; jlo++) {
                 const ulonglong2 *tw = c.tw + (long)SH::M * (H + jlo) + j2;
-                const ulonglong2 w0 = __ldg(tw), w1 = __ldg(tw + 1);
 #pragma unroll
-                for (int jhi = 0; jhi < C / (2 * H); jhi++) {
-                    const int j1 = jhi * 2 * H + jlo;
-                    ct_bfly(x[(2 * cp) * C + j1], x[(2 * cp) * C + j1 + H], w0.x, w0.y, c.q);
-                    ct_bfly(x[(2 * cp + 1) * C + j1], x[(2 * cp + 1) * C + j1 + H], w1.x, w1.y, c.q);
+                for (int h = 0; h < SH::W; h++) {
+                    const ulonglong2 w = __ldg(tw + h);
+                    const int col = SH::W * cg + h;
+#pragma unroll
+                    for (int jhi = 0; jhi < C / (2 * H); jhi++) {
+                        const int j1 = jhi * 2 * H + jlo;
+                        ct_bfly(x[col * C + j1], x[col * C + j1 + H], w.x, w.y, c.q);
+                    }
                 }
             }
         }
@@ -403,7 +460,7 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         }
         global_store<SH, B, EP>(x, blk, c.t);
     } else {
-        constexpr int C = SH::C, PAIRS = SH::E / C / 2;
+        constexpr int C = SH::C;
         smem_store<SH, B, EP>(x, sm, c.t);
         cluster_arrive();
         cluster_wait();
@@ -412,22 +469,24 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         for (int j1 = 0; j1 < C; j1++) {
             const uint64_t *src = cl.map_shared_rank(sm, (unsigned)j1);
 #pragma unroll
-            for (int cp = 0; cp < PAIRS; cp++) {
-                const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(src + swz<LOGE>(col_j2<SH>(cp, c.t, c.r)));
-                x[(2 * cp) * C + j1] = v.x;
-                x[(2 * cp + 1) * C + j1] = v.y;
-            }
+            for (int cg = 0; cg < SH::NG; cg++) col_get<SH>(x, cg, j1, src + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
         }
         cross_inv<SH, 0>(x, c);
 #pragma unroll
-        for (int cp = 0; cp < PAIRS; cp++) {
-            const int j2 = col_j2<SH>(cp, c.t, c.r);
+        for (int cg = 0; cg < SH::NG; cg++) {
+            const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
             for (int j1 = 0; j1 < C; j1++) {
                 const long p = (long)j1 * SH::M + j2;
-                const uint64_t y0 = twist(x[(2 * cp) * C + j1], __ldg(tws + p), c.q);
-                const uint64_t y1 = twist(x[(2 * cp + 1) * C + j1], __ldg(tws + p + 1), c.q);
-                __stcs(reinterpret_cast<ulonglong2 *>(data + p), make_ulonglong2(y0, y1));
+#pragma unroll
+                for (int h = 0; h < SH::W; h++) {
+                    const int col = SH::W * cg + h;
+                    x[col * C + j1] = twist(x[col * C + j1], __ldg(tws + p + h), c.q);
+                }
+                if constexpr (SH::W == 2)
+                    __stcs(reinterpret_cast<ulonglong2 *>(data + p), make_ulonglong2(x[(2 * cg) * C + j1], x[(2 * cg + 1) * C + j1]));
+                else
+                    __stcs(data + p, x[cg * C + j1]);
             }
         }
         cluster_arrive();   // keep this CTA's shared memory alive until every peer has read it
@@ -452,7 +511,14 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
     c.q = c.kc[K_Q];
     uint64_t x[SH::E];
     uint64_t *blk = data + (long)c.r * SH::M;
-    global_load<SH, 0, (SH::P == 1 ? SH::EREM : LOGE)>(x, blk, c.t);
+    constexpr int EP0 = SH::P == 1 ? SH::EREM : LOGE;
+    if constexpr (SH::E >= 2) {
+        block_load_coalesced<SH>(sm, blk, c.t);
+        __syncthreads();
+        smem_load<SH, 0, EP0>(x, sm, c.t);
+    } else {
+        global_load<SH, 0, EP0>(x, blk, c.t);
+    }
     inv_passes<SH, 0>(x, sm, blk, data, twist_tab + (long)l * SH::N, c);   // indexed by global position
 }
 
@@ -467,6 +533,9 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
+    }
+    if (SH::C > 8) {   // clusters of 16 CTAs are a non-portable size
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return -1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * SH::C));
@@ -520,7 +589,7 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
 #define FHE_SHAPE_16 3, 8, 5, 2
 #endif
 #ifndef FHE_SHAPE_17
-#define FHE_SHAPE_17 3, 9, 5, 1
+#define FHE_SHAPE_17 4, 8, 5, 2
 #endif
 
 int launch_ntt(uint64_t *res, int log_n, int L, long rows, const fhe_ntt_tables *t, bool inverse, void *stream) {
