@@ -384,6 +384,61 @@ def reference(args):
     print(json.dumps(line), flush=True)
 
 
+def sweep(args):
+    """Per-point times of the sweep workload (n = 2^11..2^17, L in {1, 8, 24,
+    64}, batch in {1, 16, 64}): forward NTT, inverse NTT and pointwise product,
+    each timed with CUDA events on the launch stream after 3 warm-up runs,
+    with L2 flushed (256 MB write) before every timed repetition.  One JSON
+    line per point; these are measurements, not the headline bench line."""
+    import torch
+    from ntt_arithmetic_gb300 import api, inputs
+    from ntt_arithmetic_gb300 import build as B
+    B.build()
+    dev = torch.device("cuda", 0)
+    hbm, hbm_kind = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for log_n in range(11, 18):
+        n = 1 << log_n
+        for L in (1, 8, 24, 64):
+            qs = api.find_primes(log_n, L)
+            t = api.NttTables(log_n, qs, dev)
+            pool = torch.from_numpy(inputs.uniform_residues((2, L, n), qs, 5000 + log_n, buffer=L)).to(dev)
+            for batch in (1, 16, 64):
+                x = pool.repeat((batch + 1) // 2, 1, 1)[:batch].contiguous()
+                y = x.clone()
+                times = {"fwd": [], "inv": [], "mul": []}
+                for rep in range(3 + args.sweep_reps):
+                    for name in ("fwd", "inv", "mul"):
+                        flush.zero_()
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        if name == "fwd":
+                            api.ntt_fwd(x, t)
+                        elif name == "inv":
+                            api.ntt_inv(x, t)
+                        else:
+                            api.mul_ntt(x, x, y, t)
+                        e1.record(stream)
+                        torch.cuda.synchronize(dev)
+                        if rep >= 3:
+                            times[name].append(e0.elapsed_time(e1) * 1e3)
+                med = {k: statistics.median(v) for k, v in times.items()}
+                residues = batch * L * n
+                bfly = batch * L * (n // 2) * log_n
+                print(json.dumps({
+                    "sweep_point": {"n": n, "L": L, "batch": batch}, "bytes": residues * 8,
+                    "fwd_us": round(med["fwd"], 2), "inv_us": round(med["inv"], 2), "mul_us": round(med["mul"], 2),
+                    "fwd_gbs": round(16 * residues / med["fwd"] / 1e3, 1), "inv_gbs": round(16 * residues / med["inv"] / 1e3, 1),
+                    "mul_gbs": round(24 * residues / med["mul"] / 1e3, 1),
+                    "fwd_hbm_frac": round(16 * residues / med["fwd"] / 1e3 / hbm, 3),
+                    "mul_hbm_frac": round(24 * residues / med["mul"] / 1e3 / hbm, 3),
+                    "fwd_alu_frac": round(bfly / (med["fwd"] * 1e-6) / ALU_PEAK_BFLY, 3),
+                    "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind, "l2": "flushed before every timed run"}), flush=True)
+                del x, y
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,8 +447,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=2)
+    ap.add_argument("--sweep", action="store_true", help="time every point of the n / L / batch sweep instead")
+    ap.add_argument("--sweep-reps", type=int, default=5)
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.sweep:
+        sweep(args)
+    elif args.impl == "reference":
         reference(args)
     else:
         ours(args)
