@@ -2,19 +2,21 @@
 //
 // One (polynomial, prime) row of n = 2^LOGN residues is transformed by a
 // thread-block cluster of C = 2^LOGC CTAs (C = 1 for n <= 2^13).  Each CTA
-// owns M = n / C residues in shared memory, so a row crosses HBM exactly once
-// in each direction: the "compact grouped" / "fixed-radix shared-memory"
-// execution FHElium describes for its CUDA NTT families ("Eager, Compile, and
-// native execution", table "Native operator families"), here built on
-// Blackwell clusters and distributed shared memory.
+// owns M = n / C residues in shared memory: the "compact grouped" /
+// "fixed-radix shared-memory" execution FHElium describes for its CUDA NTT
+// families ("Eager, Compile, and native execution", table "Native operator
+// families"), here built on Blackwell thread-block clusters.
 //
 // Forward (natural -> bit-reversed, psi-merged Cooley-Tukey):
 //   stage s (s = 0 .. LOGN-1) pairs positions p and p + n/2^(s+1) inside blocks
 //   of n/2^s and multiplies by psi^brv(2^s + block) (table fwd[2^s + block]).
 //   * cross stages s < LOGC: the C elements {j1 M + j2 : j1 < C} of a column
 //     j2 live in C different CTAs; each thread loads whole columns from HBM,
-//     applies the LOGC stages in registers and scatters element j1 into CTA
-//     j1's shared memory (DSMEM), then one cluster barrier;
+//     applies the LOGC stages in registers and hands element j1 to CTA j1,
+//     either through the row's own positions in L2 (global stores, one
+//     cluster barrier with release/acquire semantics, L1-bypassing loads;
+//     the default, measured faster on GB300 than remote shared-memory
+//     stores) or through distributed shared memory;
 //   * local stages s >= LOGC run in passes of up to LOGE stages: a thread
 //     holds 2^LOGE residues (radix-2^LOGE in registers), with one shared-
 //     memory round trip and one __syncthreads between passes.
@@ -37,6 +39,14 @@
 #include "fhe_internal.h"
 
 namespace cg = cooperative_groups;
+
+// Cross-CTA exchange of the cluster NTT: 0 = distributed shared memory
+// (remote stores / loads), 1 = through the row's own HBM positions, which
+// are L2-resident at these sizes (global stores, a cluster barrier with
+// release/acquire semantics, then L1-bypassing loads).
+#ifndef FHE_XCHG_L2
+#define FHE_XCHG_L2 1
+#endif
 
 namespace fhe {
 namespace {
@@ -185,6 +195,34 @@ __device__ __forceinline__ void block_store_coalesced(const uint64_t *sm, uint64
     }
 }
 
+template <class SH>
+__device__ __forceinline__ void col_put_cg(const uint64_t (&x)[SH::E], int cg, int j1, uint64_t *p) {
+    if constexpr (SH::W == 2)
+        __stcg(reinterpret_cast<ulonglong2 *>(p), make_ulonglong2(x[(2 * cg) * SH::C + j1], x[(2 * cg + 1) * SH::C + j1]));
+    else
+        __stcg(p, x[cg * SH::C + j1]);
+}
+template <class SH>
+__device__ __forceinline__ void col_get_cg(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
+    if constexpr (SH::W == 2) {
+        const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2 *>(p));
+        x[(2 * cg) * SH::C + j1] = v.x;
+        x[(2 * cg + 1) * SH::C + j1] = v.y;
+    } else {
+        x[cg * SH::C + j1] = __ldcg(p);
+    }
+}
+template <class SH, int B, int EP>
+__device__ __forceinline__ void global_load_cg(uint64_t (&x)[SH::E], const uint64_t *blk, int t) {
+    constexpr int G = SH::E >> EP, EPN = 1 << EP;
+#pragma unroll
+    for (int k = 0; k < G; k++) {
+        const int g = t + SH::T * k;
+#pragma unroll
+        for (int j = 0; j < EPN; j++) x[k * EPN + j] = __ldcg(blk + pass_pos<B, EP>(g, j));
+    }
+}
+
 // ---------------------------------------------------------------- forward --
 
 // Local stage I of a pass over bits [B, B+EP): global stage s = LOGN-B-EP+I,
@@ -195,17 +233,35 @@ __device__ __forceinline__ void fwd_stage(uint64_t (&x)[SH::E], const Ctx &c) {
     constexpr int S = SH::LOGN - B - EP + I;
     constexpr int HALF = 1 << (EP - 1 - I);
     constexpr int NW = 1 << I;
-#pragma unroll
-    for (int k = 0; k < G; k++) {
-        const int g = c.t + SH::T * k;
-        const int base = (1 << S) + (c.r << (SH::LOGM - B - EP + I)) + ((g >> B) << I);
+    if constexpr (B + EP == SH::LOGM && G > 1) {
+        // first local pass: g >> B is 0 for every group, so the twiddles are
+        // the same for all groups of the CTA -- load them once
+        const int base = (1 << S) + (c.r << (SH::LOGM - B - EP + I));
 #pragma unroll
         for (int jj = 0; jj < NW; jj++) {
             const ulonglong2 w = __ldg(c.tw + base + jj);
 #pragma unroll
-            for (int u = 0; u < HALF; u++) {
-                const int j = jj * 2 * HALF + u;
-                ct_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
+            for (int k = 0; k < G; k++) {
+#pragma unroll
+                for (int u = 0; u < HALF; u++) {
+                    const int j = jj * 2 * HALF + u;
+                    ct_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < G; k++) {
+            const int g = c.t + SH::T * k;
+            const int base = (1 << S) + (c.r << (SH::LOGM - B - EP + I)) + ((g >> B) << I);
+#pragma unroll
+            for (int jj = 0; jj < NW; jj++) {
+                const ulonglong2 w = __ldg(c.tw + base + jj);
+#pragma unroll
+                for (int u = 0; u < HALF; u++) {
+                    const int j = jj * 2 * HALF + u;
+                    ct_bfly(x[k * EPN + j], x[k * EPN + j + HALF], w.x, w.y, c.q);
+                }
             }
         }
     }
@@ -314,7 +370,7 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
     uint64_t x[SH::E];
     if constexpr (SH::C > 1) {
         constexpr int C = SH::C;
-        cluster_arrive_relaxed();
+        if constexpr (!FHE_XCHG_L2) cluster_arrive_relaxed();
 #pragma unroll
         for (int cg = 0; cg < SH::NG; cg++) {
             const int j2 = col_j2<SH>(cg, c.t, c.r);
@@ -322,17 +378,29 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
             for (int j1 = 0; j1 < C; j1++) col_get_cs<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
         }
         cross_fwd<SH, 0>(x, c);
-        cluster_wait();   // every CTA of the cluster has started: DSMEM is live
-        cg::cluster_group cl = cg::this_cluster();
+        if constexpr (FHE_XCHG_L2) {
 #pragma unroll
-        for (int j1 = 0; j1 < C; j1++) {
-            uint64_t *dst = cl.map_shared_rank(sm, (unsigned)j1);
+            for (int cg = 0; cg < SH::NG; cg++) {
+                const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
-            for (int cg = 0; cg < SH::NG; cg++) col_put<SH>(x, cg, j1, dst + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
+                for (int j1 = 0; j1 < C; j1++) col_put_cg<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
+            }
+            cluster_arrive();   // release: this CTA's columns are in L2
+            cluster_wait();     // acquire: every CTA's columns are
+            global_load_cg<SH, (SH::P - 1) * LOGE, SH::EREM>(x, data + (long)c.r * SH::M, c.t);
+        } else {
+            cluster_wait();   // every CTA of the cluster has started: DSMEM is live
+            cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+            for (int j1 = 0; j1 < C; j1++) {
+                uint64_t *dst = cl.map_shared_rank(sm, (unsigned)j1);
+#pragma unroll
+                for (int cg = 0; cg < SH::NG; cg++) col_put<SH>(x, cg, j1, dst + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
+            }
+            cluster_arrive();
+            cluster_wait();
+            smem_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, sm, c.t);
         }
-        cluster_arrive();
-        cluster_wait();
-        smem_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, sm, c.t);
     } else {
         global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, data, c.t);
     }
@@ -461,15 +529,34 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         global_store<SH, B, EP>(x, blk, c.t);
     } else {
         constexpr int C = SH::C;
-        smem_store<SH, B, EP>(x, sm, c.t);
-        cluster_arrive();
-        cluster_wait();
-        cg::cluster_group cl = cg::this_cluster();
+        if constexpr (FHE_XCHG_L2) {
+            // this CTA's block of the row, in place; pass B holds bits >= B: coalesced
+            constexpr int G = SH::E >> EP, EPN = 1 << EP;
 #pragma unroll
-        for (int j1 = 0; j1 < C; j1++) {
-            const uint64_t *src = cl.map_shared_rank(sm, (unsigned)j1);
+            for (int k = 0; k < G; k++) {
+                const int g = c.t + SH::T * k;
 #pragma unroll
-            for (int cg = 0; cg < SH::NG; cg++) col_get<SH>(x, cg, j1, src + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
+                for (int j = 0; j < EPN; j++) __stcg(blk + pass_pos<B, EP>(g, j), x[k * EPN + j]);
+            }
+            cluster_arrive();   // release: this block is in L2
+            cluster_wait();     // acquire: every block is
+#pragma unroll
+            for (int cg = 0; cg < SH::NG; cg++) {
+                const int j2 = col_j2<SH>(cg, c.t, c.r);
+#pragma unroll
+                for (int j1 = 0; j1 < C; j1++) col_get_cg<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
+            }
+        } else {
+            smem_store<SH, B, EP>(x, sm, c.t);
+            cluster_arrive();
+            cluster_wait();
+            cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+            for (int j1 = 0; j1 < C; j1++) {
+                const uint64_t *src = cl.map_shared_rank(sm, (unsigned)j1);
+#pragma unroll
+                for (int cg = 0; cg < SH::NG; cg++) col_get<SH>(x, cg, j1, src + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
+            }
         }
         cross_inv<SH, 0>(x, c);
 #pragma unroll
@@ -489,8 +576,10 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
                     __stcs(data + p, x[cg * C + j1]);
             }
         }
-        cluster_arrive();   // keep this CTA's shared memory alive until every peer has read it
-        cluster_wait();
+        if constexpr (!FHE_XCHG_L2) {
+            cluster_arrive();   // keep this CTA's shared memory alive until every peer has read it
+            cluster_wait();
+        }
     }
 }
 
