@@ -56,6 +56,7 @@ def _load():
         "oracle_automorph_batch": (None, [_u64p, _u64p, _int, _int, _int, _u64p, _u64p, _u64, _int, _int]),
         "oracle_modup_batch": (None, [_u64p, _u64p, _u64p, _int, _int, _int, _int, _int, _int]),
         "oracle_keyswitch_batch": (None, [_u64p, _u64p, _u64p, _u64p, _u64p, _int, _int, _int, _int, _int, _int]),
+        "oracle_moddown_batch": (None, [_u64p, _u64p, _u64p, _int, _int, _int, _int, _int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -245,3 +246,24 @@ def keyswitch_batch(a, keys, qp, psi_qp, L: int, K: int, dnum: int, threads: int
     _load().oracle_keyswitch_batch(_p(a), _p(keys), _p(out), _p(qp), _p(ps), _log2(n), L, K, dnum,
                                    batch, threads or default_threads())
     return out
+
+
+def moddown_batch(a, qp, L: int, K: int, nearest: bool) -> np.ndarray:
+    """a: [batch][L+K][n] coefficient domain over (q_0..q_{L-1}, p_0..p_{K-1})
+    -> [batch][L][n]: floor((X + h) / P) mod q_l, h = (P-1)/2 if nearest else 0.
+    Rescale is the case K = 1 with P = the last prime."""
+    a, qp = _arr(a), _arr(qp)
+    n = a.shape[-1]
+    batch = a.size // ((L + K) * n)
+    out = np.zeros((batch, L, n), dtype=np.uint64)
+    _load().oracle_moddown_batch(_p(a), _p(out), _p(qp), _log2(n), L, K, batch, int(nearest))
+    return out
+
+
+def moddown_ntt_batch(a, qp, psi_qp, L: int, K: int, nearest: bool, threads: int | None = None) -> np.ndarray:
+    """The same in the NTT domain, by definition: NTT_Q(moddown(INTT_QP(a)))."""
+    a = _arr(a)
+    n = a.shape[-1]
+    coeff = ntt_batch(a, qp, psi_qp, inverse=True, threads=threads)
+    md = moddown_batch(coeff, qp, L, K, nearest)
+    return ntt_batch(md, _arr(qp)[:L], _arr(psi_qp)[:L], threads=threads)

@@ -469,6 +469,52 @@ void oracle_modup_batch(const uint64_t *in, uint64_t *out, const uint64_t *qp, i
     run_units(modup_unit, &c, (long)batch * dnum, threads);
 }
 
+/* ------------------------------------------------------------------------ */
+/* ModDown (QP -> Q) and rescale: divide by P with rounding.                  */
+/* ------------------------------------------------------------------------ */
+
+/* For one coefficient with residues x[0..L+K) over (q_0..q_{L-1}, p_0..p_{K-1})
+ * of X in [0, QP), P = p_0 ... p_{K-1}:
+ *   out[l] = floor((X + h) / P) mod q_l,   h = (P - 1)/2 (nearest) or 0.
+ * Identity used: with c = (X + h) mod P (a value in [0, P), obtained exactly
+ * from the P residues of X + h by Garner's mixed radix),
+ *   floor((X + h) / P) = (X + h - c) / P,
+ * and the right side is reduced mod q_l with P^-1 mod q_l. */
+static void moddown_coeff(const uint64_t *x, const uint64_t *qp, int L, int K, int nearest, uint64_t *out) {
+    const uint64_t *P = qp + L;
+    uint64_t y[64], v[64];
+    for (int k = 0; k < K; k++) {
+        /* h mod p_k = (P - 1)/2 mod p_k = (p_k - 1)/2 since P = 0 mod p_k */
+        uint64_t h = nearest ? (P[k] - 1) / 2 : 0;
+        y[k] = addmod(x[L + k] % P[k], h, P[k]);
+    }
+    garner_digits(y, P, K, v);
+    for (int l = 0; l < L; l++) {
+        uint64_t q = qp[l];
+        uint64_t Pm = 1 % q;
+        for (int k = 0; k < K; k++) Pm = mulmod(Pm, P[k] % q, q);
+        /* h mod q = (P mod q - 1) / 2 mod q */
+        uint64_t h = nearest ? mulmod(submod(Pm, 1 % q, q), invmod(2, q), q) : 0;
+        uint64_t c = mixed_radix_mod(v, P, K, q);
+        uint64_t num = submod(addmod(x[l] % q, h, q), c, q);
+        out[l] = mulmod(num, invmod(Pm, q), q);
+    }
+}
+
+/* in: [batch][L+K][n] coefficient domain; out: [batch][L][n] coefficient domain. */
+void oracle_moddown_batch(const uint64_t *in, uint64_t *out, const uint64_t *qp, int log_n, int L, int K,
+                          int batch, int nearest) {
+    uint64_t n = (uint64_t)1 << log_n;
+    uint64_t xs[256], r[256];
+    for (int b = 0; b < batch; b++) {
+        for (uint64_t i = 0; i < n; i++) {
+            for (int l = 0; l < L + K; l++) xs[l] = in[((uint64_t)b * (L + K) + l) * n + i];
+            moddown_coeff(xs, qp, L, K, nearest, r);
+            for (int l = 0; l < L; l++) out[((uint64_t)b * L + l) * n + i] = r[l];
+        }
+    }
+}
+
 /* Hybrid key-switch inner product, before ModDown:
  *   out[b][c][l] = sum_j NTT_l(ModUp_j(in[b]))[l] * keys[j][c][l]  mod qp_l
  * in: [batch][L][n] coefficient domain; keys: [dnum][2][L+K][n] NTT domain;

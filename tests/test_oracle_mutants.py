@@ -5,8 +5,8 @@ scratch directory), rebuilds it there and runs the oracle pin tests against
 the copy; the run must fail.  Mistakes: a wrong twist root, a missing output
 bit reversal, a '+' for the negacyclic '-', a lost automorphism sign, a
 Garner radix error, a non-minimal root, a missing 1/n, swapped key
-components, a wrong tensor cross term, a wrong prime step and a dropped
-Miller-Rabin round.
+components, a wrong tensor cross term, a wrong prime step, a dropped
+Miller-Rabin round, and two ModDown rounding mistakes.
 """
 import os
 import shutil
@@ -48,13 +48,19 @@ MUTANTS = {
     "prime_scan_skips": (
         "        c -= m;\n    }\n    return found;",
         "        c -= 2 * m;\n    }\n    return found;"),
+    "moddown_rounding_sign": (
+        "uint64_t num = submod(addmod(x[l] % q, h, q), c, q);",
+        "uint64_t num = submod(submod(x[l] % q, h, q), c, q);"),
+    "moddown_rounding_missing_on_p": (
+        "uint64_t h = nearest ? (P[k] - 1) / 2 : 0;",
+        "uint64_t h = 0;"),
     "miller_rabin_one_round": (
         "    for (int i = 0; i < 12; i++) {\n        uint64_t x = powmod(small[i], d, n);",
         "    for (int i = 0; i < 1; i++) {\n        uint64_t x = powmod(small[i], d, n);"),
 }
 
 PIN_FILES = ["test_oracle_primes_psi.py", "test_oracle_ntt.py", "test_oracle_automorph.py",
-             "test_oracle_keyswitch.py"]
+             "test_oracle_keyswitch.py", "test_oracle_moddown.py"]
 
 
 @pytest.fixture(scope="module")
