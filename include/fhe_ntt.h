@@ -206,6 +206,50 @@ int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const 
                      int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
                      const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream);
 
+/* ---- ModDown and rescale ---------------------------------------------- */
+
+#define FHE_ROUND_TRUNCATE 0
+#define FHE_ROUND_NEAREST 1
+
+/* Division by P = p_0 ... p_{K-1} with rounding (FHElium "QP-to-Q ModDown"
+ * and "nearest and truncating rescale kernels", "Eager, Compile, and native
+ * execution", section "CUDA execution"; kestrel-llm vllm_ckks.c rescale,
+ * overview section 3).  Basis qp = (q_0..q_{L-1}, p_0..p_{K-1}), 1 <= K <= 16.
+ * Per coefficient, with X the exact CRT value in [0, QP):
+ *   out_l = floor((X + h) / P) mod q_l,  h = (P-1)/2 (FHE_ROUND_NEAREST) or 0
+ *   (FHE_ROUND_TRUNCATE).
+ * Computed as (x_l - (((X + h) mod P) - h)) P^-1 mod q_l with (X + h) mod P
+ * obtained exactly from the P residues by Garner's mixed radix. */
+
+/* Size of the constant blob for (L, K). */
+int fhe_moddown_tables_bytes(int L, int K, size_t *bytes);
+
+/* Build the constants for basis qp[L+K] (host) into host memory; copy the
+ * blob unchanged to a 16-byte aligned device buffer and pass it as `md`. */
+int fhe_moddown_tables_build_host(int L, int K, const uint64_t *qp, void *host_blob, size_t bytes);
+
+/* Workspace bytes of fhe_moddown: batch * (L + K) * n * 8. */
+int fhe_moddown_workspace_bytes(int log_n, int L, int K, int batch, size_t *bytes);
+
+/* in: [batch][L+K][n] over qp; out: [batch][L][n] over q_0..q_{L-1}; both in
+ * `domain` (FHE_DOMAIN_COEFF or FHE_DOMAIN_NTT; the NTT-domain result is the
+ * NTT over Q of the coefficient-domain result of the INTT over QP of `in`).
+ * t_qp: NTT tables covering at least the L+K primes of qp in that order.
+ * workspace: at least fhe_moddown_workspace_bytes, contents ignored.  out
+ * must not overlap in, workspace or the tables; in must not overlap the
+ * workspace (FHE_EALIAS). */
+int fhe_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, int batch, int domain,
+                int rounding, const fhe_ntt_tables *t_qp, const void *md, uint64_t *workspace,
+                size_t ws_bytes, void *stream);
+
+/* Rescale: drop the last of L primes, out = floor((X + h) / q_{L-1}) over
+ * q_0..q_{L-2}; exactly fhe_moddown with (L-1, 1).  in: [batch][L][n];
+ * out: [batch][L-1][n]; rs = fhe_moddown_tables_build_host(L-1, 1, q).
+ * Workspace: fhe_moddown_workspace_bytes(log_n, L-1, 1, batch). */
+int fhe_rescale(uint64_t *out, const uint64_t *in, int log_n, int L, int batch, int domain, int rounding,
+                const fhe_ntt_tables *t_q, const void *rs, uint64_t *workspace, size_t ws_bytes,
+                void *stream);
+
 /* ---- key switch without device allocation ----------------------------- */
 
 /* The pages have no counterpart to this entry point; it serves callers of

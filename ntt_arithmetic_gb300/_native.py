@@ -20,6 +20,8 @@ FHE_ESPACE = -4
 FHE_EDEVICE = -5
 FHE_DOMAIN_COEFF = 0
 FHE_DOMAIN_NTT = 1
+FHE_ROUND_TRUNCATE = 0
+FHE_ROUND_NEAREST = 1
 
 _u64 = ctypes.c_uint64
 _u64p = ctypes.POINTER(ctypes.c_uint64)
@@ -64,6 +66,13 @@ SIGNATURES = {
     "fhe_keyswitch_workspace_bytes": (_int, [_int, _int, _int, _int, _int, ctypes.POINTER(_size)]),
     "fhe_keyswitch_ip": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int, ctypes.POINTER(NttTables),
                                 _vp, _vp, _size, _vp]),
+    "fhe_moddown_tables_bytes": (_int, [_int, _int, ctypes.POINTER(_size)]),
+    "fhe_moddown_tables_build_host": (_int, [_int, _int, _u64p, _vp, _size]),
+    "fhe_moddown_workspace_bytes": (_int, [_int, _int, _int, _int, ctypes.POINTER(_size)]),
+    "fhe_moddown": (_int, [_vp, _vp, _int, _int, _int, _int, _int, _int, ctypes.POINTER(NttTables), _vp, _vp,
+                           _size, _vp]),
+    "fhe_rescale": (_int, [_vp, _vp, _int, _int, _int, _int, _int, ctypes.POINTER(NttTables), _vp, _vp, _size,
+                           _vp]),
     "fhe_keyswitch_ip_noalloc": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int,
                                         ctypes.POINTER(NttTables), _vp, _vp]),
     "fhe_keyswitch_noalloc_max_bytes": (_size, []),

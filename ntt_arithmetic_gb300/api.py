@@ -241,3 +241,57 @@ def keyswitch_ip_noalloc(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor,
     N.call("fhe_keyswitch_ip_noalloc", _ptr(out), _ptr(x), 0, _ptr(keys), log_n, L, K, dnum, batch,
            tables_qp.ref(), _ptr(modup.blob), _stream(x.device, stream))
     return out
+
+
+# ------------------------------------------------------------ ModDown ------
+
+class ModdownTables:
+    """Constants of the division by P = p_0..p_{K-1} for basis
+    qp = (q_0..q_{L-1}, p_0..p_{K-1}).  Rescale uses (L-1, 1) over the chain."""
+
+    def __init__(self, L: int, K: int, qp: Sequence[int], device="cuda"):
+        self.L, self.K = int(L), int(K)
+        if len(qp) != self.L + self.K:
+            raise ValueError("qp must list L + K primes")
+        nbytes = ctypes.c_size_t()
+        N.call("fhe_moddown_tables_bytes", self.L, self.K, ctypes.byref(nbytes))
+        host = np.zeros(nbytes.value, dtype=np.uint8)
+        arr = (ctypes.c_uint64 * len(qp))(*[int(v) for v in qp])
+        N.call("fhe_moddown_tables_build_host", self.L, self.K, arr, host.ctypes.data_as(ctypes.c_void_p),
+               nbytes.value)
+        self.blob = torch.from_numpy(host).to(torch.device(device))
+
+
+def moddown_workspace_bytes(log_n: int, L: int, K: int, batch: int) -> int:
+    v = ctypes.c_size_t()
+    N.call("fhe_moddown_workspace_bytes", log_n, L, K, batch, ctypes.byref(v))
+    return int(v.value)
+
+
+def moddown(out: torch.Tensor, x: torch.Tensor, L: int, K: int, tables_qp: NttTables, md: ModdownTables,
+            domain: str = "ntt", nearest: bool = True, workspace: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """out = floor((X + h) / P) mod q_l: x [batch, L+K, n] -> out [batch, L, n]."""
+    _residues(out, "out")
+    _residues(x, "x")
+    n = x.shape[-1]
+    log_n = _log2(n)
+    if x.shape[-2] != L + K or out.shape[-2] != L or out.numel() * (L + K) != x.numel() * L:
+        raise ValueError("x must be [batch, L+K, n] and out [batch, L, n]")
+    batch = x.numel() // ((L + K) * n)
+    dom = {"ntt": N.FHE_DOMAIN_NTT, "coeff": N.FHE_DOMAIN_COEFF}[domain]
+    need = moddown_workspace_bytes(log_n, L, K, batch)
+    if workspace is None:
+        workspace = torch.empty(need // 8, dtype=torch.uint64, device=x.device)
+    N.call("fhe_moddown", _ptr(out), _ptr(x), log_n, L, K, batch, dom,
+           N.FHE_ROUND_NEAREST if nearest else N.FHE_ROUND_TRUNCATE, tables_qp.ref(), _ptr(md.blob),
+           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(x.device, stream))
+    return out
+
+
+def rescale(out: torch.Tensor, x: torch.Tensor, tables_q: NttTables, rs: ModdownTables, domain: str = "ntt",
+            nearest: bool = True, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Drop the last prime: x [batch, L, n] -> out [batch, L-1, n], dividing by it with rounding."""
+    L = x.shape[-2]
+    return moddown(out, x, L - 1, 1, tables_q, rs, domain=domain, nearest=nearest, workspace=workspace,
+                   stream=stream)

@@ -207,3 +207,39 @@ extern "C" int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_str
     launched += r;
     return finish(launched);
 }
+
+extern "C" int fhe_moddown_workspace_bytes(int log_n, int L, int K, int batch, size_t *bytes) {
+    if (!bytes || log_n < 1 || log_n > kMaxLogN || L < 1 || K < 1 || K > kMaxAlpha || batch < 1) return FHE_EINVAL;
+    *bytes = ((size_t)batch * (L + K) << log_n) * 8;
+    return FHE_OK;
+}
+
+extern "C" int fhe_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, int batch, int domain,
+                           int rounding, const fhe_ntt_tables *t_qp, const void *md, uint64_t *workspace,
+                           size_t ws_bytes, void *stream) {
+    size_t need = 0;
+    int s = fhe_moddown_workspace_bytes(log_n, L, K, batch, &need);
+    if (s) return s;
+    if ((s = check_shape(log_n, L + K, batch))) return s;
+    if ((s = check_tables(t_qp, log_n, L + K))) return s;
+    if (domain != FHE_DOMAIN_COEFF && domain != FHE_DOMAIN_NTT) return FHE_EINVAL;
+    if (rounding != FHE_ROUND_TRUNCATE && rounding != FHE_ROUND_NEAREST) return FHE_EINVAL;
+    if (!out || !in || !md || !workspace) return FHE_EINVAL;
+    if (!aligned16(out) || !aligned16(in) || !aligned16(md) || !aligned16(workspace)) return FHE_EINVAL;
+    if (ws_bytes < need) return FHE_ESPACE;
+    if ((s = select_device({out, in, md, workspace, t_qp->blob}))) return s;
+    const Span so{out, ((size_t)batch * L << log_n) * 8}, si{in, ((size_t)batch * (L + K) << log_n) * 8},
+        sw{workspace, need}, tb{t_qp->blob, t_qp->bytes}, sm{md, moddown_layout(L, K).bytes};
+    if (overlap(so, si) || overlap(so, sw) || overlap(so, tb) || overlap(so, sm) || overlap(si, sw) ||
+        overlap(sw, tb) || overlap(sw, sm))
+        return FHE_EALIAS;
+    return finish(launch_moddown(out, in, log_n, L, K, batch, domain == FHE_DOMAIN_NTT,
+                                 rounding == FHE_ROUND_NEAREST, t_qp, md, workspace, stream));
+}
+
+extern "C" int fhe_rescale(uint64_t *out, const uint64_t *in, int log_n, int L, int batch, int domain, int rounding,
+                           const fhe_ntt_tables *t_q, const void *rs, uint64_t *workspace, size_t ws_bytes,
+                           void *stream) {
+    if (L < 2) return FHE_EINVAL;
+    return fhe_moddown(out, in, log_n, L - 1, 1, batch, domain, rounding, t_q, rs, workspace, ws_bytes, stream);
+}

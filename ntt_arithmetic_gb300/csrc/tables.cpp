@@ -111,6 +111,29 @@ ModupLayout modup_layout(int L, int K, int dnum) {
     return s;
 }
 
+ModdownLayout moddown_layout(int L, int K) {
+    ModdownLayout s;
+    s.off_garner = 0;
+    s.off_mr = align256((size_t)K * K * 16);
+    s.off_hp = align256(s.off_mr + (size_t)L * K * 16);
+    s.off_hq = align256(s.off_hp + (size_t)K * 8);
+    s.off_pinv = align256(s.off_hq + (size_t)L * 8);
+    s.bytes = align256(s.off_pinv + (size_t)L * 16);
+    return s;
+}
+
+fhe_ntt_tables tables_slice(const fhe_ntt_tables *t, int first, int count) {
+    fhe_ntt_tables s = *t;
+    const size_t n = (size_t)1 << t->log_n;
+    s.L = count;
+    s.q = t->q + first;
+    s.consts = t->consts + (size_t)first * K_COUNT;
+    s.fwd = t->fwd + (size_t)first * n * 2;
+    s.inv = t->inv + (size_t)first * n * 2;
+    s.twist = t->twist + (size_t)first * n * 2;
+    return s;
+}
+
 bool modup_shape_ok(int L, int K, int dnum) {
     if (L < 1 || K < 0 || dnum < 1 || dnum > L || L + K > kMaxBasis) return false;
     const int alpha = (L + dnum - 1) / dnum;
@@ -278,6 +301,58 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
                 prod = mul_mod(prod, qp[lo + i] % p, p);
             }
         }
+    }
+    return FHE_OK;
+}
+
+extern "C" int fhe_moddown_tables_bytes(int L, int K, size_t *bytes) {
+    if (!bytes || L < 1 || K < 1 || K > kMaxAlpha || L + K > kMaxTableL) return FHE_EINVAL;
+    *bytes = moddown_layout(L, K).bytes;
+    return FHE_OK;
+}
+
+// ModDown by P = p_0 ... p_{K-1}: Garner constants over P, the mixed-radix
+// weights prod_{b<a} p_b mod q_l, h = (P-1)/2 mod every prime (nearest
+// rounding) and P^-1 mod q_l, with Shoup companions where used as
+// multipliers.
+extern "C" int fhe_moddown_tables_build_host(int L, int K, const uint64_t *qp, void *host_blob, size_t bytes) {
+    if (!qp || !host_blob || L < 1 || K < 1 || K > kMaxAlpha || L + K > kMaxTableL) return FHE_EINVAL;
+    const ModdownLayout lay = moddown_layout(L, K);
+    if (bytes < lay.bytes) return FHE_ESPACE;
+    for (int l = 0; l < L + K; l++) {
+        if (qp[l] <= (1ull << 48) || qp[l] >= (1ull << 50) || !is_prime_u64(qp[l])) return FHE_EINVAL;
+        for (int m = 0; m < l; m++)
+            if (qp[m] == qp[l]) return FHE_EINVAL;
+    }
+    char *base = (char *)host_blob;
+    std::memset(base, 0, lay.bytes);
+    const uint64_t *P = qp + L;
+    uint64_t *g = (uint64_t *)(base + lay.off_garner);
+    uint64_t *mr = (uint64_t *)(base + lay.off_mr);
+    uint64_t *hp = (uint64_t *)(base + lay.off_hp);
+    uint64_t *hq = (uint64_t *)(base + lay.off_hq);
+    uint64_t *pinv = (uint64_t *)(base + lay.off_pinv);
+    for (int a = 0; a < K; a++) {
+        for (int b = 0; b < a; b++) {
+            const uint64_t c = inv_mod(P[b] % P[a], P[a]);
+            g[(a * K + b) * 2] = c;
+            g[(a * K + b) * 2 + 1] = shoup(c, P[a]);
+        }
+        hp[a] = (P[a] - 1) / 2;   // (P - 1)/2 mod p_a, as P = 0 mod p_a
+    }
+    for (int l = 0; l < L; l++) {
+        const uint64_t q = qp[l];
+        uint64_t prod = 1 % q;
+        for (int a = 0; a < K; a++) {
+            mr[(l * K + a) * 2] = prod;
+            mr[(l * K + a) * 2 + 1] = shoup(prod, q);
+            prod = mul_mod(prod, P[a] % q, q);
+        }
+        // prod = P mod q
+        hq[l] = mul_mod((prod + q - 1) % q, inv_mod(2, q), q);
+        const uint64_t pi = inv_mod(prod, q);
+        pinv[l * 2] = pi;
+        pinv[l * 2 + 1] = shoup(pi, q);
     }
     return FHE_OK;
 }
