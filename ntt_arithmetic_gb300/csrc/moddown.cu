@@ -12,9 +12,11 @@
 //      mixed radix (the same construction as the key-switch ModUp) and
 //      d_l = c - h mod q_l is written (coefficient domain);
 //   2. out_l = (x_l - d_l) P^-1 mod q_l.
-// In the NTT domain the P limbs are first brought back to coefficients
-// (inverse NTT of a copy) and d is transformed forward over Q before step 2;
-// the map is linear, so step 2 is the same in both domains.
+// In the coefficient domain both steps run in one pass (one read of every
+// input limb, one write of every output limb).  In the NTT domain the P limbs
+// are first brought back to coefficients (inverse NTT of a copy) and d is
+// transformed forward over Q before step 2; the map is linear, so step 2 is
+// the same in both domains.
 #include <cuda_runtime.h>
 
 #include "fhe_arith.cuh"
@@ -40,12 +42,14 @@ k_copy_limbs(uint64_t *__restrict__ ws, const uint64_t *__restrict__ in, long pa
 }
 
 // d[b][l][i] = ((X + h) mod P) - h  mod q_l, from the P residues
-// src[b * src_item + k * n + i] (k < K).
-template <int MAXK>
+// src[b * src_item + k * n + i] (k < K).  FUSED (coefficient domain): instead
+// of d, write out[b][l][i] = (x_l - d_l) P^-1 mod q_l directly, reading x_l
+// from src - L n (the Q limbs of the same batch item).
+template <int MAXK, bool FUSED>
 __global__ void __launch_bounds__(kThreads)
 k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long src_item, int log_n, int L, int K,
                int batch, int nearest, const ulonglong2 *__restrict__ garner, const ulonglong2 *__restrict__ mr,
-               const uint64_t *__restrict__ hp, const uint64_t *__restrict__ hq,
+               const uint64_t *__restrict__ hp, const uint64_t *__restrict__ hq, const ulonglong2 *__restrict__ pinv,
                const uint64_t *__restrict__ consts_q, const uint64_t *__restrict__ consts_p) {
     const long n = 1L << log_n;
     const long total = n * batch;
@@ -92,7 +96,13 @@ k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long 
                 const uint64_t h = __ldg(hq + l);
                 c = c >= h ? c - h : c + q - h;
             }
-            __stcg(d + ((b * L + l) << log_n) + i, c);
+            if constexpr (FUSED) {
+                const uint64_t x = __ldcs(src + b * src_item - ((long)(L - l) << log_n) + i);
+                const ulonglong2 pi = __ldg(pinv + l);
+                __stcs(d + ((b * L + l) << log_n) + i, reduce4(shoup_lazy(x + q - c, pi.x, pi.y, q), q));
+            } else {
+                __stcg(d + ((b * L + l) << log_n) + i, c);
+            }
         }
     }
 }
@@ -120,12 +130,15 @@ k_moddown_finish(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, co
 
 template <int MAXK>
 void launch_conv(uint64_t *d, const uint64_t *src, long src_item, int log_n, int L, int K, int batch, bool nearest,
-                 const ModdownLayout &lay, const char *md, const fhe_ntt_tables *t_qp, cudaStream_t st) {
+                 bool fused, const ModdownLayout &lay, const char *md, const fhe_ntt_tables *t_qp, cudaStream_t st) {
     const long total = (long)batch << log_n;
-    k_moddown_conv<MAXK><<<stream_grid(total, kThreads, 8), kThreads, 0, st>>>(
-        d, src, src_item, log_n, L, K, batch, nearest ? 1 : 0, (const ulonglong2 *)(md + lay.off_garner),
-        (const ulonglong2 *)(md + lay.off_mr), (const uint64_t *)(md + lay.off_hp),
-        (const uint64_t *)(md + lay.off_hq), t_qp->consts, t_qp->consts + (long)L * K_COUNT);
+    const unsigned grid = stream_grid(total, kThreads, 8);
+    auto kern = fused ? k_moddown_conv<MAXK, true> : k_moddown_conv<MAXK, false>;
+    kern<<<grid, kThreads, 0, st>>>(d, src, src_item, log_n, L, K, batch, nearest ? 1 : 0,
+                                    (const ulonglong2 *)(md + lay.off_garner), (const ulonglong2 *)(md + lay.off_mr),
+                                    (const uint64_t *)(md + lay.off_hp), (const uint64_t *)(md + lay.off_hq),
+                                    (const ulonglong2 *)(md + lay.off_pinv), t_qp->consts,
+                                    t_qp->consts + (long)L * K_COUNT);
 }
 
 }  // namespace
@@ -138,7 +151,7 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
     int launched = 0;
     const uint64_t *src = in + ((long)L << log_n);       // P limbs of batch item 0
     long src_item = (long)(L + K) << log_n;
-    uint64_t *d = ws;                                   // [batch][L][n]
+    uint64_t *d = ntt_domain ? ws : out;                // [batch][L][n]; the output itself when fused
     if (ntt_domain) {
         uint64_t *pl = ws + ((long)batch * L << log_n);   // [batch][K][n]
         const long pairs = ((long)batch * K << log_n) / 2;
@@ -152,19 +165,18 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
         src = pl;
         src_item = (long)K << log_n;
     }
-    if (K <= 1) launch_conv<1>(d, src, src_item, log_n, L, K, batch, nearest, lay, md, t_qp, st);
-    else if (K <= 2) launch_conv<2>(d, src, src_item, log_n, L, K, batch, nearest, lay, md, t_qp, st);
-    else if (K <= 4) launch_conv<4>(d, src, src_item, log_n, L, K, batch, nearest, lay, md, t_qp, st);
-    else if (K <= 8) launch_conv<8>(d, src, src_item, log_n, L, K, batch, nearest, lay, md, t_qp, st);
-    else launch_conv<16>(d, src, src_item, log_n, L, K, batch, nearest, lay, md, t_qp, st);
+    if (K <= 1) launch_conv<1>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+    else if (K <= 2) launch_conv<2>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+    else if (K <= 4) launch_conv<4>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+    else if (K <= 8) launch_conv<8>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+    else launch_conv<16>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
     if (cudaGetLastError() != cudaSuccess) return -1;
     launched++;
-    if (ntt_domain) {
-        const fhe_ntt_tables tq = tables_slice(t_qp, 0, L);
-        int r = launch_ntt(d, log_n, L, (long)batch * L, &tq, false, stream);
-        if (r < 0) return -1;
-        launched += r;
-    }
+    if (!ntt_domain) return launched;
+    const fhe_ntt_tables tq = tables_slice(t_qp, 0, L);
+    int r = launch_ntt(d, log_n, L, (long)batch * L, &tq, false, stream);
+    if (r < 0) return -1;
+    launched += r;
     const long pairs = ((long)batch * L << log_n) / 2;
     k_moddown_finish<<<stream_grid(pairs, kThreads, 8), kThreads, 0, st>>>(
         out, in, d, pairs, log_n, L, K, (const ulonglong2 *)(md + lay.off_pinv), t_qp->consts);

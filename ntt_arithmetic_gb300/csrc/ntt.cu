@@ -352,17 +352,28 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
     }
 }
 
+// Row (batch item b, limb l) of this CTA's cluster.  Clusters are numbered
+// limb-major (all batch items of limb 0, then of limb 1, ...), so the CTAs
+// resident at one time share a few primes' twiddle tables and a table is
+// fetched from DRAM about once per launch however long the chain is.
+template <int LOGC>
+__device__ __forceinline__ long row_of(int L, int batch, int &l) {
+    const long cl = (long)(blockIdx.x >> LOGC);
+    l = (int)(cl / batch);
+    return (cl - (long)l * batch) * L + l;
+}
+
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
-k_ntt_fwd(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts,
-          const ulonglong2 *__restrict__) {
+k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+          const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
     c.t = threadIdx.x;
     c.r = SH::C > 1 ? (int)(blockIdx.x & (SH::C - 1)) : 0;
-    const long row = (long)(blockIdx.x >> LOGC);
-    const int l = (int)(row % L);
+    int l;
+    const long row = row_of<LOGC>(L, batch, l);
     uint64_t *data = res + row * SH::N;
     c.tw = tw + (long)l * SH::N;
     c.kc = consts + (long)l * K_COUNT;
@@ -585,15 +596,15 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
 
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
-k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts,
-          const ulonglong2 *__restrict__ twist_tab) {
+k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+          const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__ twist_tab) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
     c.t = threadIdx.x;
     c.r = SH::C > 1 ? (int)(blockIdx.x & (SH::C - 1)) : 0;
-    const long row = (long)(blockIdx.x >> LOGC);
-    const int l = (int)(row % L);
+    int l;
+    const long row = row_of<LOGC>(L, batch, l);
     uint64_t *data = res + row * SH::N;
     c.tw = tw + (long)l * SH::N;
     c.kc = consts + (long)l * K_COUNT;
@@ -616,7 +627,7 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, const ulonglong2 *__restrict__ tw, 
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool inverse, cudaStream_t st) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
-    void (*kern)(uint64_t *, int, const ulonglong2 *, const uint64_t *, const ulonglong2 *) =
+    void (*kern)(uint64_t *, int, int, const ulonglong2 *, const uint64_t *, const ulonglong2 *) =
         inverse ? k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB> : k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
     const size_t smem = (size_t)SH::M * sizeof(uint64_t);
     if (smem > 48 * 1024) {
@@ -640,7 +651,8 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
     cfg.numAttrs = SH::C > 1 ? 1 : 0;
     const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(inverse ? t->inv : t->fwd);
     const ulonglong2 *twist_tab = reinterpret_cast<const ulonglong2 *>(t->twist);
-    if (cudaLaunchKernelEx(&cfg, kern, res, L, tw, t->consts, twist_tab) != cudaSuccess) return -1;
+    if (rows % L) return -1;
+    if (cudaLaunchKernelEx(&cfg, kern, res, L, (int)(rows / L), tw, t->consts, twist_tab) != cudaSuccess) return -1;
     return 1;
 }
 

@@ -57,6 +57,13 @@ def _load():
         "oracle_modup_batch": (None, [_u64p, _u64p, _u64p, _int, _int, _int, _int, _int, _int]),
         "oracle_keyswitch_batch": (None, [_u64p, _u64p, _u64p, _u64p, _u64p, _int, _int, _int, _int, _int, _int]),
         "oracle_moddown_batch": (None, [_u64p, _u64p, _u64p, _int, _int, _int, _int, _int]),
+        "oracle_bconv_coeff": (None, [_u64p, _u64p, _int, _u64p, _int, _int, _u64p]),
+        "oracle_bconv_batch": (None, [_u64p, _u64p, _u64p, _int, _u64p, _int, _int, _int, _int, _int]),
+        "oracle_modup_batch_ex": (None, [_u64p, _u64p, _u64p, _int, _int, _int, _int, _int, _int, _int]),
+        "oracle_keyswitch_batch_ex": (None, [_u64p, _u64p, _u64p, _u64p, _u64p, _int, _int, _int, _int, _int,
+                                             _int, _int]),
+        "oracle_keyswitch_hoisted_batch": (None, [_u64p, _u64p, _u64p, _int, _u64p, _u64p, _u64p, _int, _int,
+                                                  _int, _int, _int, _int, _int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -226,25 +233,75 @@ def automorph_batch(a, qs, psi_list, k: int, ntt_domain: bool, threads: int | No
     return out
 
 
-def modup_batch(a, qp, L: int, K: int, dnum: int, threads: int | None = None) -> np.ndarray:
-    """a: [batch][L][n] -> [batch][dnum][L+K][n] (coefficient domain)."""
+def modup_batch(a, qp, L: int, K: int, dnum: int, threads: int | None = None, approx: bool = False) -> np.ndarray:
+    """a: [batch][L][n] -> [batch][dnum][L+K][n] (coefficient domain); exact
+    Garner extension, or the approximate basis conversion if ``approx``."""
     a, qp = _arr(a), _arr(qp)
     n = a.shape[-1]
     batch = a.size // (L * n)
     out = np.zeros((batch, dnum, L + K, n), dtype=np.uint64)
-    _load().oracle_modup_batch(_p(a), _p(out), _p(qp), _log2(n), L, K, dnum, batch,
-                               threads or default_threads())
+    if approx:
+        _load().oracle_modup_batch_ex(_p(a), _p(out), _p(qp), _log2(n), L, K, dnum, batch, 1,
+                                      threads or default_threads())
+    else:
+        _load().oracle_modup_batch(_p(a), _p(out), _p(qp), _log2(n), L, K, dnum, batch,
+                                   threads or default_threads())
     return out
 
 
-def keyswitch_batch(a, keys, qp, psi_qp, L: int, K: int, dnum: int, threads: int | None = None) -> np.ndarray:
+def keyswitch_batch(a, keys, qp, psi_qp, L: int, K: int, dnum: int, threads: int | None = None,
+                    approx: bool = False) -> np.ndarray:
     """a: [batch][L][n] coeff; keys: [dnum][2][L+K][n] NTT -> [batch][2][L+K][n] NTT."""
     a, keys, qp, ps = _arr(a), _arr(keys), _arr(qp), _arr(psi_qp)
     n = a.shape[-1]
     batch = a.size // (L * n)
     out = np.zeros((batch, 2, L + K, n), dtype=np.uint64)
-    _load().oracle_keyswitch_batch(_p(a), _p(keys), _p(out), _p(qp), _p(ps), _log2(n), L, K, dnum,
-                                   batch, threads or default_threads())
+    if approx:
+        _load().oracle_keyswitch_batch_ex(_p(a), _p(keys), _p(out), _p(qp), _p(ps), _log2(n), L, K, dnum,
+                                          batch, 1, threads or default_threads())
+    else:
+        _load().oracle_keyswitch_batch(_p(a), _p(keys), _p(out), _p(qp), _p(ps), _log2(n), L, K, dnum,
+                                       batch, threads or default_threads())
+    return out
+
+
+def keyswitch_hoisted_batch(a, keys, ks, qp, psi_qp, L: int, K: int, dnum: int, threads: int | None = None,
+                            approx: bool = False) -> np.ndarray:
+    """Hoisted key switch for Galois elements ks[R]: a [batch][L][n] coeff;
+    keys [R][dnum][2][L+K][n] NTT -> [R][batch][2][L+K][n] NTT."""
+    a, keys, qp, ps = _arr(a), _arr(keys), _arr(qp), _arr(psi_qp)
+    ks = _arr([int(k) for k in ks])
+    n = a.shape[-1]
+    R = int(ks.size)
+    batch = a.size // (L * n)
+    assert keys.size == R * dnum * 2 * (L + K) * n
+    out = np.zeros((R, batch, 2, L + K, n), dtype=np.uint64)
+    _load().oracle_keyswitch_hoisted_batch(_p(a), _p(keys), _p(ks), R, _p(out), _p(qp), _p(ps), _log2(n), L, K,
+                                           dnum, batch, int(approx), threads or default_threads())
+    return out
+
+
+def bconv_coeff(x, src, dst, approx: bool) -> np.ndarray:
+    """One coefficient from basis ``src`` to ``dst``: exact (X in [0, Q)) or
+    approximate (X + e Q, 0 <= e < len(src))."""
+    x, s, d = _arr(x), _arr(src), _arr(dst)
+    assert x.size == s.size <= 64
+    out = np.zeros(d.size, dtype=np.uint64)
+    _load().oracle_bconv_coeff(_p(x), _p(s), int(s.size), _p(d), int(d.size), int(approx), _p(out))
+    return out
+
+
+def bconv_batch(a, src, dst, approx: bool = False, threads: int | None = None) -> np.ndarray:
+    """a: [batch][S][n] over ``src`` -> [batch][T][n] over ``dst`` (coefficient
+    domain).  Modraise is the exact case with ``src`` = the first S primes of
+    the chain and ``dst`` = the whole chain."""
+    a, s, d = _arr(a), _arr(src), _arr(dst)
+    S, T, n = int(s.size), int(d.size), a.shape[-1]
+    assert a.shape[-2] == S and S <= 64 and T <= 8192
+    batch = a.size // (S * n)
+    out = np.zeros((batch, T, n), dtype=np.uint64)
+    _load().oracle_bconv_batch(_p(a), _p(out), _p(s), S, _p(d), T, _log2(n), batch, int(approx),
+                               threads or default_threads())
     return out
 
 

@@ -31,7 +31,12 @@
  *    evaluation of a(X) at the n roots of X^n+1, stored in bit-reversed order;
  *  - inverse NTT: the exact inverse, including the 1/n factor;
  *  - ModUp: exact mixed-radix (Garner) CRT of a digit, then residues of that
- *    integer modulo every prime of the extended basis.
+ *    integer modulo every prime of the extended basis; the approximate
+ *    variant keeps the CRT sum's overflow e Q (0 <= e < digit size);
+ *  - modraise: the exact Garner extension from the first primes of the chain
+ *    to the whole chain, with the value taken in [0, Q_low) (no centring);
+ *  - hoisted rotations: one ModUp and NTT of the digits, then per Galois
+ *    element the automorphism of the extended digits and the inner product.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -317,6 +322,63 @@ void oracle_modup_coeff(const uint64_t *x, const uint64_t *d, int alpha,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Approximate (fast) basis conversion.                                      */
+/* ------------------------------------------------------------------------ */
+
+/* With Q = q_0 ... q_{S-1} and qhat_j = Q / q_j, the CRT sum
+ *   sum_j [x_j * qhat_j^-1]_{q_j} * qhat_j
+ * equals X + e Q for an integer 0 <= e < S (each bracket is below q_j, so the
+ * sum is below S Q).  Reducing it modulo a target prime p without the
+ * correction of e Q is the approximate basis conversion: one product per
+ * source limb, then one multiply-accumulate per (source, target) pair,
+ * instead of Garner's quadratic digit recursion.  The constants depend only
+ * on the bases: qinv[j] = qhat_j^-1 mod q_j and qhat[t][j] = qhat_j mod p_t. */
+static void fast_bconv_consts(const uint64_t *src, int S, const uint64_t *dst, int T, uint64_t *qinv,
+                              uint64_t *qhat) {
+    for (int j = 0; j < S; j++) {
+        uint64_t qj = src[j], h = 1 % qj;
+        for (int i = 0; i < S; i++)
+            if (i != j) h = mulmod(h, src[i] % qj, qj);
+        qinv[j] = invmod(h, qj);
+    }
+    for (int t = 0; t < T; t++) {
+        uint64_t p = dst[t];
+        for (int j = 0; j < S; j++) {
+            uint64_t h = 1 % p;
+            for (int i = 0; i < S; i++)
+                if (i != j) h = mulmod(h, src[i] % p, p);
+            qhat[(long)t * S + j] = h;
+        }
+    }
+}
+
+static void fast_bconv_apply(const uint64_t *x, const uint64_t *src, int S, const uint64_t *dst, int T,
+                             const uint64_t *qinv, const uint64_t *qhat, uint64_t *out) {
+    uint64_t y[64];
+    for (int j = 0; j < S; j++) y[j] = mulmod(x[j] % src[j], qinv[j], src[j]);
+    for (int t = 0; t < T; t++) {
+        uint64_t p = dst[t], acc = 0;
+        for (int j = 0; j < S; j++) acc = addmod(acc, mulmod(y[j] % p, qhat[(long)t * S + j], p), p);
+        out[t] = acc;
+    }
+}
+
+/* One coefficient from basis src[S] to basis dst[T]: exact (Garner, the
+ * value X in [0, Q)) or approximate (X + e Q, 0 <= e < S). */
+void oracle_bconv_coeff(const uint64_t *x, const uint64_t *src, int S, const uint64_t *dst, int T, int approx,
+                        uint64_t *out) {
+    if (!approx) {
+        oracle_modup_coeff(x, src, S, dst, T, out);
+        return;
+    }
+    uint64_t qinv[64];
+    uint64_t *qhat = (uint64_t *)malloc((size_t)T * S * sizeof(uint64_t));
+    fast_bconv_consts(src, S, dst, T, qinv, qhat);
+    fast_bconv_apply(x, src, S, dst, T, qinv, qhat, out);
+    free(qhat);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Batched drivers over the [batch][L][n] layout, threaded over independent  */
 /* (batch, limb) rows only.                                                  */
 /* ------------------------------------------------------------------------ */
@@ -439,6 +501,7 @@ static void digit_range(int L, int dnum, int j, int *lo, int *hi) {
 
 typedef struct {
     const uint64_t *in; uint64_t *out; const uint64_t *qp; int log_n; int L; int K; int dnum; int batch;
+    int approx;
 } modup_ctx;
 
 /* one unit = one (batch item, digit) pair: all n coefficients */
@@ -452,21 +515,68 @@ static void modup_unit(void *c, long u) {
     int alpha = hi - lo;
     const uint64_t *src = x->in + (uint64_t)bi * x->L * n;
     uint64_t *dst = x->out + ((uint64_t)bi * x->dnum + j) * LK * n;
-    uint64_t xs[64], res[256];
+    uint64_t xs[64], res[256], qinv[64];
+    uint64_t *qhat = NULL;
+    if (x->approx) {
+        qhat = (uint64_t *)malloc((size_t)LK * alpha * sizeof(uint64_t));
+        fast_bconv_consts(x->qp + lo, alpha, x->qp, LK, qinv, qhat);
+    }
     for (uint64_t i = 0; i < n; i++) {
         for (int a = 0; a < alpha; a++) xs[a] = src[(uint64_t)(lo + a) * n + i];
-        oracle_modup_coeff(xs, x->qp + lo, alpha, x->qp, LK, res);
+        if (x->approx) fast_bconv_apply(xs, x->qp + lo, alpha, x->qp, LK, qinv, qhat, res);
+        else oracle_modup_coeff(xs, x->qp + lo, alpha, x->qp, LK, res);
         for (int l = 0; l < LK; l++) dst[(uint64_t)l * n + i] = res[l];
     }
+    free(qhat);
 }
 
 /* ModUp of every digit: in [batch][L][n] (coefficient domain, basis q_0..q_{L-1})
  * -> out [batch][dnum][L+K][n] (coefficient domain, basis qp = q_0..q_{L-1},
  * p_0..p_{K-1}).  Limbs inside the digit reproduce the input residues. */
+void oracle_modup_batch_ex(const uint64_t *in, uint64_t *out, const uint64_t *qp, int log_n, int L,
+                           int K, int dnum, int batch, int approx, int threads) {
+    modup_ctx c = {in, out, qp, log_n, L, K, dnum, batch, approx};
+    run_units(modup_unit, &c, (long)batch * dnum, threads);
+}
+
 void oracle_modup_batch(const uint64_t *in, uint64_t *out, const uint64_t *qp, int log_n, int L,
                         int K, int dnum, int batch, int threads) {
-    modup_ctx c = {in, out, qp, log_n, L, K, dnum, batch};
-    run_units(modup_unit, &c, (long)batch * dnum, threads);
+    oracle_modup_batch_ex(in, out, qp, log_n, L, K, dnum, batch, 0, threads);
+}
+
+typedef struct {
+    const uint64_t *in; uint64_t *out; const uint64_t *src; int S; const uint64_t *dst; int T;
+    int log_n; int approx; const uint64_t *qinv; const uint64_t *qhat;
+} bconv_ctx;
+
+/* one unit = one batch item */
+static void bconv_unit(void *c, long u) {
+    bconv_ctx *x = (bconv_ctx *)c;
+    uint64_t n = (uint64_t)1 << x->log_n;
+    const uint64_t *src = x->in + (uint64_t)u * x->S * n;
+    uint64_t *dst = x->out + (uint64_t)u * x->T * n;
+    uint64_t xs[64], res[8192];
+    for (uint64_t i = 0; i < n; i++) {
+        for (int a = 0; a < x->S; a++) xs[a] = src[(uint64_t)a * n + i];
+        if (x->approx) fast_bconv_apply(xs, x->src, x->S, x->dst, x->T, x->qinv, x->qhat, res);
+        else oracle_modup_coeff(xs, x->src, x->S, x->dst, x->T, res);
+        for (int t = 0; t < x->T; t++) dst[(uint64_t)t * n + i] = res[t];
+    }
+}
+
+/* Basis conversion of every coefficient: in [batch][S][n] over src ->
+ * out [batch][T][n] over dst (coefficient domain).  Modraise -- the
+ * extension of a low-level ciphertext to the full chain that starts a
+ * bootstrap -- is the exact case with src the first S primes of the chain
+ * and dst the whole chain.  S <= 64, T <= 8192. */
+void oracle_bconv_batch(const uint64_t *in, uint64_t *out, const uint64_t *src, int S, const uint64_t *dst,
+                        int T, int log_n, int batch, int approx, int threads) {
+    uint64_t qinv[64];
+    uint64_t *qhat = (uint64_t *)malloc((size_t)T * S * sizeof(uint64_t));
+    fast_bconv_consts(src, S, dst, T, qinv, qhat);
+    bconv_ctx c = {in, out, src, S, dst, T, log_n, approx, qinv, qhat};
+    run_units(bconv_unit, &c, (long)batch, threads);
+    free(qhat);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -515,20 +625,12 @@ void oracle_moddown_batch(const uint64_t *in, uint64_t *out, const uint64_t *qp,
     }
 }
 
-/* Hybrid key-switch inner product, before ModDown:
- *   out[b][c][l] = sum_j NTT_l(ModUp_j(in[b]))[l] * keys[j][c][l]  mod qp_l
- * in: [batch][L][n] coefficient domain; keys: [dnum][2][L+K][n] NTT domain;
- * out: [batch][2][L+K][n] NTT domain. */
-void oracle_keyswitch_batch(const uint64_t *in, const uint64_t *keys, uint64_t *out,
-                            const uint64_t *qp, const uint64_t *psi_qp, int log_n, int L, int K,
-                            int dnum, int batch, int threads) {
+/* out[b][c][l] = sum_j ext[b][j][l] * keys[j][c][l] mod qp_l over the NTT-domain
+ * extended digits ext [batch][dnum][L+K][n]. */
+static void keyswitch_ip(const uint64_t *ext, const uint64_t *keys, uint64_t *out, const uint64_t *qp,
+                         int log_n, int LK, int dnum, int batch) {
     uint64_t n = (uint64_t)1 << log_n;
-    int LK = L + K;
     uint64_t plane = (uint64_t)LK * n;
-    uint64_t *ext = (uint64_t *)malloc((uint64_t)batch * dnum * plane * sizeof(uint64_t));
-    oracle_modup_batch(in, ext, qp, log_n, L, K, dnum, batch, threads);
-    /* every (batch, digit) block is one row set of LK limbs */
-    oracle_ntt_batch(ext, log_n, LK, batch * dnum, qp, psi_qp, 0, threads);
     for (int bi = 0; bi < batch; bi++) {
         for (int c = 0; c < 2; c++) {
             for (int l = 0; l < LK; l++) {
@@ -546,5 +648,56 @@ void oracle_keyswitch_batch(const uint64_t *in, const uint64_t *keys, uint64_t *
             }
         }
     }
+}
+
+/* Hybrid key-switch inner product, before ModDown:
+ *   out[b][c][l] = sum_j NTT_l(ModUp_j(in[b]))[l] * keys[j][c][l]  mod qp_l
+ * in: [batch][L][n] coefficient domain; keys: [dnum][2][L+K][n] NTT domain;
+ * out: [batch][2][L+K][n] NTT domain.  approx != 0 takes the approximate
+ * basis conversion for ModUp instead of the exact one. */
+void oracle_keyswitch_batch_ex(const uint64_t *in, const uint64_t *keys, uint64_t *out,
+                               const uint64_t *qp, const uint64_t *psi_qp, int log_n, int L, int K,
+                               int dnum, int batch, int approx, int threads) {
+    uint64_t n = (uint64_t)1 << log_n;
+    int LK = L + K;
+    uint64_t plane = (uint64_t)LK * n;
+    uint64_t *ext = (uint64_t *)malloc((uint64_t)batch * dnum * plane * sizeof(uint64_t));
+    oracle_modup_batch_ex(in, ext, qp, log_n, L, K, dnum, batch, approx, threads);
+    /* every (batch, digit) block is one row set of LK limbs */
+    oracle_ntt_batch(ext, log_n, LK, batch * dnum, qp, psi_qp, 0, threads);
+    keyswitch_ip(ext, keys, out, qp, log_n, LK, dnum, batch);
+    free(ext);
+}
+
+void oracle_keyswitch_batch(const uint64_t *in, const uint64_t *keys, uint64_t *out,
+                            const uint64_t *qp, const uint64_t *psi_qp, int log_n, int L, int K,
+                            int dnum, int batch, int threads) {
+    oracle_keyswitch_batch_ex(in, keys, out, qp, psi_qp, log_n, L, K, dnum, batch, 0, threads);
+}
+
+/* Hoisted key switch for R Galois elements k_r (the rotations of
+ * coeff_to_slot / slot_to_coeff): ModUp and the NTT of the digits are done
+ * once, then for each r the automorphism sigma_{k_r} acts on the extended
+ * digits in the NTT domain and the inner product uses that rotation's keys:
+ *   out[r][b][c][l] = sum_j sigma_{k_r}(NTT_l(ModUp_j(in[b])))[l] * keys[r][j][c][l]
+ * in: [batch][L][n] coefficient domain; keys: [R][dnum][2][L+K][n];
+ * out: [R][batch][2][L+K][n] NTT domain. */
+void oracle_keyswitch_hoisted_batch(const uint64_t *in, const uint64_t *keys, const uint64_t *ks, int R,
+                                    uint64_t *out, const uint64_t *qp, const uint64_t *psi_qp, int log_n,
+                                    int L, int K, int dnum, int batch, int approx, int threads) {
+    uint64_t n = (uint64_t)1 << log_n;
+    int LK = L + K;
+    uint64_t plane = (uint64_t)LK * n;
+    uint64_t rows = (uint64_t)batch * dnum * plane;
+    uint64_t *ext = (uint64_t *)malloc(rows * sizeof(uint64_t));
+    uint64_t *rot = (uint64_t *)malloc(rows * sizeof(uint64_t));
+    oracle_modup_batch_ex(in, ext, qp, log_n, L, K, dnum, batch, approx, threads);
+    oracle_ntt_batch(ext, log_n, LK, batch * dnum, qp, psi_qp, 0, threads);
+    for (int r = 0; r < R; r++) {
+        oracle_automorph_batch(ext, rot, log_n, LK, batch * dnum, qp, psi_qp, ks[r], 1, threads);
+        keyswitch_ip(rot, keys + (uint64_t)r * dnum * 2 * plane, out + (uint64_t)r * batch * 2 * plane, qp,
+                     log_n, LK, dnum, batch);
+    }
+    free(rot);
     free(ext);
 }

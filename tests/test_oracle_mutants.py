@@ -6,7 +6,8 @@ the copy; the run must fail.  Mistakes: a wrong twist root, a missing output
 bit reversal, a '+' for the negacyclic '-', a lost automorphism sign, a
 Garner radix error, a non-minimal root, a missing 1/n, swapped key
 components, a wrong tensor cross term, a wrong prime step, a dropped
-Miller-Rabin round, and two ModDown rounding mistakes.
+Miller-Rabin round, two ModDown rounding mistakes, two approximate basis
+conversion mistakes and two hoisted key-switch mistakes.
 """
 import os
 import shutil
@@ -54,13 +55,25 @@ MUTANTS = {
     "moddown_rounding_missing_on_p": (
         "uint64_t h = nearest ? (P[k] - 1) / 2 : 0;",
         "uint64_t h = 0;"),
+    "fast_bconv_missing_qhat_inverse": (
+        "for (int j = 0; j < S; j++) y[j] = mulmod(x[j] % src[j], qinv[j], src[j]);",
+        "for (int j = 0; j < S; j++) y[j] = x[j] % src[j];"),
+    "fast_bconv_qhat_keeps_own_prime": (
+        "if (i != j) h = mulmod(h, src[i] % p, p);",
+        "h = mulmod(h, src[i] % p, p);"),
+    "hoisted_skips_automorphism": (
+        "oracle_automorph_batch(ext, rot, log_n, LK, batch * dnum, qp, psi_qp, ks[r], 1, threads);",
+        "memcpy(rot, ext, rows * sizeof(uint64_t));"),
+    "hoisted_automorphism_in_wrong_domain": (
+        "oracle_automorph_batch(ext, rot, log_n, LK, batch * dnum, qp, psi_qp, ks[r], 1, threads);",
+        "oracle_automorph_batch(ext, rot, log_n, LK, batch * dnum, qp, psi_qp, ks[r], 0, threads);"),
     "miller_rabin_one_round": (
         "    for (int i = 0; i < 12; i++) {\n        uint64_t x = powmod(small[i], d, n);",
         "    for (int i = 0; i < 1; i++) {\n        uint64_t x = powmod(small[i], d, n);"),
 }
 
 PIN_FILES = ["test_oracle_primes_psi.py", "test_oracle_ntt.py", "test_oracle_automorph.py",
-             "test_oracle_keyswitch.py", "test_oracle_moddown.py"]
+             "test_oracle_keyswitch.py", "test_oracle_moddown.py", "test_oracle_bconv.py"]
 
 
 @pytest.fixture(scope="module")
