@@ -206,6 +206,65 @@ int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const 
                      int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
                      const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream);
 
+/* ModUp variants of the key switch. */
+#define FHE_MODUP_EXACT 0    /* Garner: X_j exactly, as above */
+#define FHE_MODUP_APPROX 1   /* approximate basis conversion (next paragraph) */
+
+/* fhe_keyswitch_ip with a choice of ModUp.  FHE_MODUP_APPROX replaces the
+ * exact X_j by the CRT sum sum_a [x_a (D_j/d_a)^-1]_{d_a} (D_j/d_a) = X_j + e D_j
+ * with 0 <= e < (primes in digit j), D_j the digit's modulus: alpha products
+ * and alpha multiply-accumulates per target instead of Garner's quadratic
+ * recursion; the extra e D_j is a multiple of the digit modulus (zero on the
+ * digit's own primes, which are copied in both variants).  The cheaper
+ * inexact ModUp of FHElium's "mixed-radix decomposition and basis extension"
+ * family ("Eager, Compile, and native execution", section "CUDA execution").
+ * Same arguments, workspace and rules as fhe_keyswitch_ip otherwise. */
+int fhe_keyswitch_ip_ex(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
+                        int log_n, int L, int K, int dnum, int batch, int modup_mode,
+                        const fhe_ntt_tables *t_qp, const void *modup, uint64_t *workspace,
+                        size_t ws_bytes, void *stream);
+
+/* Hoisted key switch for R Galois elements (the rotations of coeff_to_slot
+ * and slot_to_coeff, which kestrel-llm's boot profile reports as about 80% of
+ * a bootstrap; overview, section 4.2).  The digit ModUp and its NTT are
+ * computed once; then for every r < R the automorphism sigma_{galois[r]} of
+ * the extended digits (NTT domain, the index map of fhe_automorph) is fused
+ * into the inner product with that rotation's keys:
+ *   out[r][b][c][l] = sum_j sigma_{galois[r]}(NTT(X_j))[l] * keys[r][j][c][l]  mod qp_l
+ *   in:     as fhe_keyswitch_ip (coefficient domain, in_stride as there)
+ *   keys:   [R][dnum][2][L+K][n]    NTT domain, basis qp
+ *   out:    [R][batch][2][L+K][n]   NTT domain, basis qp
+ *   galois: HOST array of R odd elements in [1, 2n), 1 <= R <= 64 (a device
+ *           pointer gives FHE_EDEVICE)
+ * sigma_k(X_j) is congruent to the extension of sigma_k(in) modulo the digit's
+ * primes, so this is a valid key switch of each rotated input.  Workspace as
+ * fhe_keyswitch_ip (fhe_keyswitch_workspace_bytes, independent of R). */
+int fhe_keyswitch_hoisted(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
+                          const uint32_t *galois, int R, int log_n, int L, int K, int dnum, int batch,
+                          int modup_mode, const fhe_ntt_tables *t_qp, const void *modup,
+                          uint64_t *workspace, size_t ws_bytes, void *stream);
+
+/* ---- basis conversion and modraise ------------------------------------ */
+
+#define FHE_BCONV_EXACT 0    /* Garner: X in [0, Q) */
+#define FHE_BCONV_APPROX 1   /* CRT sum without correction: X + e Q, 0 <= e < S */
+
+/* Conversion of every coefficient from S source primes (Q = their product)
+ * to T target primes, coefficient domain.  Modraise -- kestrel-llm's
+ * bootstrap entry, the Garner extension that lifts a low-level ciphertext
+ * back to the full chain (overview, section 4.2) -- is FHE_BCONV_EXACT with
+ * the sources = the first S primes of the chain and the targets = the whole
+ * chain; the value taken is X in [0, Q) (no centring).  A target equal to a
+ * source reproduces the input limb in both modes.
+ *   in:  [batch][S][n]; out: [batch][T][n]; 1 <= S <= 16, 1 <= T <= 8192,
+ *   batch <= 65535; every prime in (2^48, 2^50), sources distinct.
+ * out must not overlap in or the tables (FHE_EALIAS). */
+int fhe_bconv_tables_bytes(int S, int T, size_t *bytes);
+int fhe_bconv_tables_build_host(int S, const uint64_t *src, int T, const uint64_t *dst, void *host_blob,
+                                size_t bytes);
+int fhe_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int batch, int mode,
+              const void *bconv, void *stream);
+
 /* ---- ModDown and rescale ---------------------------------------------- */
 
 #define FHE_ROUND_TRUNCATE 0

@@ -22,6 +22,10 @@ FHE_DOMAIN_COEFF = 0
 FHE_DOMAIN_NTT = 1
 FHE_ROUND_TRUNCATE = 0
 FHE_ROUND_NEAREST = 1
+FHE_MODUP_EXACT = 0
+FHE_MODUP_APPROX = 1
+FHE_BCONV_EXACT = 0
+FHE_BCONV_APPROX = 1
 
 _u64 = ctypes.c_uint64
 _u64p = ctypes.POINTER(ctypes.c_uint64)
@@ -66,6 +70,13 @@ SIGNATURES = {
     "fhe_keyswitch_workspace_bytes": (_int, [_int, _int, _int, _int, _int, ctypes.POINTER(_size)]),
     "fhe_keyswitch_ip": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int, ctypes.POINTER(NttTables),
                                 _vp, _vp, _size, _vp]),
+    "fhe_keyswitch_ip_ex": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int, _int,
+                                   ctypes.POINTER(NttTables), _vp, _vp, _size, _vp]),
+    "fhe_keyswitch_hoisted": (_int, [_vp, _vp, _size, _vp, ctypes.POINTER(ctypes.c_uint32), _int, _int, _int, _int,
+                                     _int, _int, _int, ctypes.POINTER(NttTables), _vp, _vp, _size, _vp]),
+    "fhe_bconv_tables_bytes": (_int, [_int, _int, ctypes.POINTER(_size)]),
+    "fhe_bconv_tables_build_host": (_int, [_int, _u64p, _int, _u64p, _vp, _size]),
+    "fhe_bconv": (_int, [_vp, _vp, _int, _int, _int, _int, _int, _vp, _vp]),
     "fhe_moddown_tables_bytes": (_int, [_int, _int, ctypes.POINTER(_size)]),
     "fhe_moddown_tables_build_host": (_int, [_int, _int, _u64p, _vp, _size]),
     "fhe_moddown_workspace_bytes": (_int, [_int, _int, _int, _int, ctypes.POINTER(_size)]),

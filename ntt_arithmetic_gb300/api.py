@@ -186,22 +186,7 @@ def keyswitch_workspace_bytes(log_n: int, L: int, K: int, dnum: int, batch: int)
     return int(v.value)
 
 
-def keyswitch_ip(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, L: int, K: int, dnum: int,
-                 tables_qp: NttTables, modup: ModupTables, workspace: torch.Tensor | None = None,
-                 stream=None, in_offset: int = 0, in_stride: int = 0, batch: int | None = None) -> torch.Tensor:
-    """Hybrid key-switch inner product (before ModDown).
-
-    x: coefficient-domain input, [batch, L, n] contiguous, or -- with
-    in_offset/in_stride (elements) and batch -- `batch` items of [L, n] at
-    x.flatten()[in_offset + b * in_stride:] (e.g. component d2 of a
-    [batch, 3, L, n] tensor product);  keys: [dnum, 2, L+K, n] NTT domain;
-    out: [batch, 2, L+K, n] NTT domain."""
-    for t, nm in ((out, "out"), (x, "x"), (keys, "keys")):
-        _residues(t, nm)
-    n = keys.shape[-1]
-    log_n = _log2(n)
-    if tuple(keys.shape) != (dnum, 2, L + K, n):
-        raise ValueError("keys must be [dnum, 2, L+K, n]")
+def _ks_input(x: torch.Tensor, L: int, n: int, in_offset: int, in_stride: int, batch: int | None) -> int:
     item = L * n
     if batch is None:
         if x.shape[-2:] != (L, n) or in_offset or in_stride:
@@ -210,15 +195,70 @@ def keyswitch_ip(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, L: int,
     stride = in_stride or item
     if in_offset < 0 or stride < item or in_offset + (batch - 1) * stride + item > x.numel():
         raise ValueError("in_offset/in_stride/batch reach outside x")
+    return batch
+
+
+def keyswitch_ip(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, L: int, K: int, dnum: int,
+                 tables_qp: NttTables, modup: ModupTables, workspace: torch.Tensor | None = None,
+                 stream=None, in_offset: int = 0, in_stride: int = 0, batch: int | None = None,
+                 approx: bool = False) -> torch.Tensor:
+    """Hybrid key-switch inner product (before ModDown).
+
+    x: coefficient-domain input, [batch, L, n] contiguous, or -- with
+    in_offset/in_stride (elements) and batch -- `batch` items of [L, n] at
+    x.flatten()[in_offset + b * in_stride:] (e.g. component d2 of a
+    [batch, 3, L, n] tensor product);  keys: [dnum, 2, L+K, n] NTT domain;
+    out: [batch, 2, L+K, n] NTT domain.  approx: approximate ModUp (the CRT
+    sum without its e D_j correction) instead of the exact Garner extension."""
+    for t, nm in ((out, "out"), (x, "x"), (keys, "keys")):
+        _residues(t, nm)
+    n = keys.shape[-1]
+    log_n = _log2(n)
+    if tuple(keys.shape) != (dnum, 2, L + K, n):
+        raise ValueError("keys must be [dnum, 2, L+K, n]")
+    batch = _ks_input(x, L, n, in_offset, in_stride, batch)
     if tuple(out.shape[-3:]) != (2, L + K, n) or out.numel() != batch * 2 * (L + K) * n:
         raise ValueError("out must be [batch, 2, L+K, n]")
     need = keyswitch_workspace_bytes(log_n, L, K, dnum, batch)
     if workspace is None:
         workspace = torch.empty(need // 8, dtype=torch.uint64, device=x.device)
     src = ctypes.c_void_p(x.data_ptr() + 8 * in_offset)
-    N.call("fhe_keyswitch_ip", _ptr(out), src, in_stride, _ptr(keys), log_n, L, K, dnum, batch, tables_qp.ref(),
-           _ptr(modup.blob), _ptr(workspace), workspace.numel() * workspace.element_size(),
-           _stream(x.device, stream))
+    ws = (_ptr(workspace), workspace.numel() * workspace.element_size(), _stream(x.device, stream))
+    if approx:
+        N.call("fhe_keyswitch_ip_ex", _ptr(out), src, in_stride, _ptr(keys), log_n, L, K, dnum, batch,
+               N.FHE_MODUP_APPROX, tables_qp.ref(), _ptr(modup.blob), *ws)
+    else:
+        N.call("fhe_keyswitch_ip", _ptr(out), src, in_stride, _ptr(keys), log_n, L, K, dnum, batch, tables_qp.ref(),
+               _ptr(modup.blob), *ws)
+    return out
+
+
+def keyswitch_hoisted(out: torch.Tensor, x: torch.Tensor, keys: torch.Tensor, galois: Sequence[int], L: int, K: int,
+                      dnum: int, tables_qp: NttTables, modup: ModupTables, workspace: torch.Tensor | None = None,
+                      stream=None, in_offset: int = 0, in_stride: int = 0, batch: int | None = None,
+                      approx: bool = False) -> torch.Tensor:
+    """Hoisted key switch for R = len(galois) rotations of the same input:
+    one ModUp + NTT of the digits, then per Galois element the automorphism
+    fused into the inner product.  keys: [R, dnum, 2, L+K, n] NTT domain;
+    out: [R, batch, 2, L+K, n] NTT domain; x as in keyswitch_ip."""
+    for t, nm in ((out, "out"), (x, "x"), (keys, "keys")):
+        _residues(t, nm)
+    R = len(galois)
+    n = keys.shape[-1]
+    log_n = _log2(n)
+    if tuple(keys.shape) != (R, dnum, 2, L + K, n):
+        raise ValueError("keys must be [R, dnum, 2, L+K, n]")
+    batch = _ks_input(x, L, n, in_offset, in_stride, batch)
+    if tuple(out.shape[-3:]) != (2, L + K, n) or out.numel() != R * batch * 2 * (L + K) * n:
+        raise ValueError("out must be [R, batch, 2, L+K, n]")
+    need = keyswitch_workspace_bytes(log_n, L, K, dnum, batch)
+    if workspace is None:
+        workspace = torch.empty(need // 8, dtype=torch.uint64, device=x.device)
+    gal = (ctypes.c_uint32 * max(R, 1))(*[int(k) for k in galois])
+    src = ctypes.c_void_p(x.data_ptr() + 8 * in_offset)
+    N.call("fhe_keyswitch_hoisted", _ptr(out), src, in_stride, _ptr(keys), gal, R, log_n, L, K, dnum, batch,
+           N.FHE_MODUP_APPROX if approx else N.FHE_MODUP_EXACT, tables_qp.ref(), _ptr(modup.blob), _ptr(workspace),
+           workspace.numel() * workspace.element_size(), _stream(x.device, stream))
     return out
 
 
@@ -295,3 +335,44 @@ def rescale(out: torch.Tensor, x: torch.Tensor, tables_q: NttTables, rs: Moddown
     L = x.shape[-2]
     return moddown(out, x, L - 1, 1, tables_q, rs, domain=domain, nearest=nearest, workspace=workspace,
                    stream=stream)
+
+
+# ------------------------------------------------------ basis conversion ---
+
+class BconvTables:
+    """Constants of the conversion from primes ``src`` to primes ``dst``."""
+
+    def __init__(self, src: Sequence[int], dst: Sequence[int], device="cuda"):
+        self.src = [int(v) for v in src]
+        self.dst = [int(v) for v in dst]
+        S, T = len(self.src), len(self.dst)
+        nbytes = ctypes.c_size_t()
+        N.call("fhe_bconv_tables_bytes", S, T, ctypes.byref(nbytes))
+        host = np.zeros(nbytes.value, dtype=np.uint8)
+        a = (ctypes.c_uint64 * S)(*self.src)
+        b = (ctypes.c_uint64 * T)(*self.dst)
+        N.call("fhe_bconv_tables_build_host", S, a, T, b, host.ctypes.data_as(ctypes.c_void_p), nbytes.value)
+        self.blob = torch.from_numpy(host).to(torch.device(device))
+
+
+def bconv(out: torch.Tensor, x: torch.Tensor, tables: BconvTables, approx: bool = False, stream=None) -> torch.Tensor:
+    """x [batch, S, n] over tables.src -> out [batch, T, n] over tables.dst
+    (coefficient domain); exact (X in [0, Q)) or approximate (X + e Q)."""
+    _residues(out, "out")
+    _residues(x, "x")
+    S, T = len(tables.src), len(tables.dst)
+    n = x.shape[-1]
+    log_n = _log2(n)
+    if x.shape[-2] != S or out.shape[-2] != T or out.shape[-1] != n or x.numel() * T != out.numel() * S:
+        raise ValueError("x must be [batch, S, n] and out [batch, T, n]")
+    batch = x.numel() // (S * n)
+    N.call("fhe_bconv", _ptr(out), _ptr(x), log_n, S, T, batch, N.FHE_BCONV_APPROX if approx else N.FHE_BCONV_EXACT,
+           _ptr(tables.blob), _stream(x.device, stream))
+    return out
+
+
+def modraise(out: torch.Tensor, x: torch.Tensor, tables: BconvTables, stream=None) -> torch.Tensor:
+    """Lift x [batch, S, n] over the first S primes of a chain to out
+    [batch, T, n] over the whole chain (exact Garner extension; tables built
+    with src = chain[:S], dst = chain)."""
+    return bconv(out, x, tables, approx=False, stream=stream)

@@ -171,26 +171,46 @@ extern "C" int fhe_keyswitch_workspace_bytes(int log_n, int L, int K, int dnum, 
     return FHE_OK;
 }
 
-extern "C" int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys, int log_n,
-                                int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp, const void *modup,
-                                uint64_t *workspace, size_t ws_bytes, void *stream) {
+namespace {
+
+// Validation and ModUp + NTT of the digits shared by the plain and the hoisted
+// key switch.  R = 0: plain (out [batch][2][L+K][n], keys [dnum][2][L+K][n]);
+// R >= 1: hoisted (out [R][batch][2][L+K][n], keys [R][dnum][2][L+K][n]).
+int keyswitch_call(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys, const uint32_t *galois,
+                   int R, int log_n, int L, int K, int dnum, int batch, int modup_mode, const fhe_ntt_tables *t_qp,
+                   const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream) {
     size_t need = 0;
     int s = fhe_keyswitch_workspace_bytes(log_n, L, K, dnum, batch, &need);
     if (s) return s;
     const int LK = L + K;
     if ((s = check_shape(log_n, LK, (long)batch * dnum))) return s;
     if ((s = check_tables(t_qp, log_n, LK))) return s;
+    if (modup_mode != FHE_MODUP_EXACT && modup_mode != FHE_MODUP_APPROX) return FHE_EINVAL;
     if (!out || !in || !keys || !modup || !workspace) return FHE_EINVAL;
     if (!aligned16(out) || !aligned16(in) || !aligned16(keys) || !aligned16(workspace) || !aligned16(modup))
         return FHE_EINVAL;
+    GaloisSet g = {};
+    if (R > 0) {
+        if (R > kMaxRotations || !galois) return FHE_EINVAL;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, galois) != cudaSuccess) cudaGetLastError();   // plain host memory
+        else if (a.type == cudaMemoryTypeDevice) return FHE_EDEVICE;                  // must be host-readable
+        const uint64_t two_n = 2ull << log_n;
+        for (int r = 0; r < R; r++) {
+            if (!(galois[r] & 1) || galois[r] >= two_n) return FHE_EINVAL;
+            g.k[r] = galois[r];
+        }
+    }
     if (ws_bytes < need) return FHE_ESPACE;
     const size_t item = (size_t)L << log_n;
     if (in_stride == 0) in_stride = item;
     if (in_stride < item || (in_stride & 1)) return FHE_EINVAL;
     if ((s = select_device({out, in, keys, modup, workspace, t_qp->blob}))) return s;
     const size_t plane = ((size_t)LK << log_n) * 8;
-    const Span so{out, 2 * plane * batch}, si{in, ((size_t)(batch - 1) * in_stride + item) * 8}, sk{keys, 2 * plane * dnum},
-        sw{workspace, need}, tb{t_qp->blob, t_qp->bytes}, sm{modup, modup_layout(L, K, dnum).bytes};
+    const size_t reps = R > 0 ? (size_t)R : 1;
+    const Span so{out, 2 * plane * batch * reps}, si{in, ((size_t)(batch - 1) * in_stride + item) * 8},
+        sk{keys, 2 * plane * dnum * reps}, sw{workspace, need}, tb{t_qp->blob, t_qp->bytes},
+        sm{modup, modup_layout(L, K, dnum).bytes};
     const Span all[6] = {so, si, sk, sw, tb, sm};
     for (int x = 0; x < 6; x++)
         for (int y = x + 1; y < 6; y++) {
@@ -198,15 +218,59 @@ extern "C" int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_str
             if (overlap(all[x], all[y])) return FHE_EALIAS;
         }
     int launched = 0, r;
-    if ((r = launch_modup(workspace, in, (long)in_stride, log_n, L, K, dnum, batch, t_qp, modup, stream)) < 0)
+    if ((r = launch_modup(workspace, in, (long)in_stride, log_n, L, K, dnum, batch, modup_mode == FHE_MODUP_APPROX,
+                          t_qp, modup, stream)) < 0)
         return finish(-1);
     launched += r;
     if ((r = launch_ntt(workspace, log_n, LK, (long)batch * dnum * LK, t_qp, false, stream)) < 0) return finish(-1);
     launched += r;
-    if ((r = launch_ks_ip(out, workspace, keys, log_n, LK, dnum, batch, t_qp, stream)) < 0) return finish(-1);
+    r = R > 0 ? launch_ks_ip_aut(out, workspace, keys, log_n, LK, dnum, batch, R, g, t_qp, stream)
+              : launch_ks_ip(out, workspace, keys, log_n, LK, dnum, batch, t_qp, stream);
+    if (r < 0) return finish(-1);
     launched += r;
     return finish(launched);
 }
+
+}  // namespace
+
+extern "C" int fhe_keyswitch_ip_ex(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
+                                   int log_n, int L, int K, int dnum, int batch, int modup_mode,
+                                   const fhe_ntt_tables *t_qp, const void *modup, uint64_t *workspace,
+                                   size_t ws_bytes, void *stream) {
+    return keyswitch_call(out, in, in_stride, keys, nullptr, 0, log_n, L, K, dnum, batch, modup_mode, t_qp, modup,
+                          workspace, ws_bytes, stream);
+}
+
+extern "C" int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys, int log_n,
+                                int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp, const void *modup,
+                                uint64_t *workspace, size_t ws_bytes, void *stream) {
+    return keyswitch_call(out, in, in_stride, keys, nullptr, 0, log_n, L, K, dnum, batch, FHE_MODUP_EXACT, t_qp,
+                          modup, workspace, ws_bytes, stream);
+}
+
+extern "C" int fhe_keyswitch_hoisted(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
+                                     const uint32_t *galois, int R, int log_n, int L, int K, int dnum, int batch,
+                                     int modup_mode, const fhe_ntt_tables *t_qp, const void *modup,
+                                     uint64_t *workspace, size_t ws_bytes, void *stream) {
+    if (R < 1) return FHE_EINVAL;
+    return keyswitch_call(out, in, in_stride, keys, galois, R, log_n, L, K, dnum, batch, modup_mode, t_qp, modup,
+                          workspace, ws_bytes, stream);
+}
+
+extern "C" int fhe_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int batch, int mode,
+                         const void *bconv, void *stream) {
+    size_t tb = 0;
+    int s = fhe_bconv_tables_bytes(S, T, &tb);
+    if (s) return s;
+    if (log_n < 1 || log_n > kMaxLogN || batch < 1 || batch > 65535) return FHE_EINVAL;
+    if (mode != FHE_BCONV_EXACT && mode != FHE_BCONV_APPROX) return FHE_EINVAL;
+    if (!out || !in || !bconv || !aligned16(out) || !aligned16(in) || !aligned16(bconv)) return FHE_EINVAL;
+    if ((s = select_device({out, in, bconv}))) return s;
+    const Span so{out, ((size_t)batch * T << log_n) * 8}, si{in, ((size_t)batch * S << log_n) * 8}, st{bconv, tb};
+    if (overlap(so, si) || overlap(so, st)) return FHE_EALIAS;
+    return finish(launch_bconv(out, in, log_n, S, T, batch, mode == FHE_BCONV_APPROX, bconv, stream));
+}
+
 
 extern "C" int fhe_moddown_workspace_bytes(int log_n, int L, int K, int batch, size_t *bytes) {
     if (!bytes || log_n < 1 || log_n > kMaxLogN || L < 1 || K < 1 || K > kMaxAlpha || batch < 1) return FHE_EINVAL;

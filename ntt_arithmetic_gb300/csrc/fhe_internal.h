@@ -24,7 +24,12 @@ struct ModupDigit {
 };
 struct ModupLayout {
     int alpha;
-    size_t off_digits, off_garner, off_mr, bytes;
+    size_t off_digits;   // [dnum] ModupDigit
+    size_t off_garner;   // [dnum][alpha][alpha] pairs: d_b^-1 mod d_a (b < a)       (exact)
+    size_t off_mr;       // [dnum][L+K][alpha] pairs: prod_{b<a} d_b mod qp_l         (exact)
+    size_t off_qinv;     // [dnum][alpha] pairs: (D_j / d_a)^-1 mod d_a                (approximate)
+    size_t off_qhat;     // [dnum][L+K][alpha] pairs: (D_j / d_a) mod qp_l             (approximate)
+    size_t bytes;
 };
 ModupLayout modup_layout(int L, int K, int dnum);
 bool modup_shape_ok(int L, int K, int dnum);
@@ -40,6 +45,25 @@ struct ModdownLayout {
 };
 ModdownLayout moddown_layout(int L, int K);
 
+// Basis conversion from S source primes to T target primes.
+constexpr int kMaxBconvSrc = 16;
+struct BconvLayout {
+    size_t off_src;      // [S] words: source primes
+    size_t off_dst;      // [T][2] words: target prime, floor(2^58 / prime)
+    size_t off_garner;   // [S][S] pairs: q_b^-1 mod q_a (b < a)                      (exact)
+    size_t off_mr;       // [T][S] pairs: prod_{b<a} q_b mod p_t                      (exact)
+    size_t off_qinv;     // [S] pairs: (Q / q_a)^-1 mod q_a                           (approximate)
+    size_t off_qhat;     // [T][S] pairs: (Q / q_a) mod p_t                           (approximate)
+    size_t bytes;
+};
+BconvLayout bconv_layout(int S, int T);
+
+// Galois elements of one hoisted key switch.
+constexpr int kMaxRotations = 64;
+struct GaloisSet {
+    uint32_t k[kMaxRotations];
+};
+
 // ---- kernel launchers (no validation; the ABI layer validates) ----------
 // Each returns the number of kernels enqueued, or -1 on a launch error.
 
@@ -52,7 +76,11 @@ int launch_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, int log_n, 
 int launch_automorph(uint64_t *out, const uint64_t *in, int log_n, int L, long rows, uint64_t k,
                      int domain, const fhe_ntt_tables *t, void *stream);
 int launch_modup(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
-                 const fhe_ntt_tables *t, const void *modup, void *stream);
+                 bool approx, const fhe_ntt_tables *t, const void *modup, void *stream);
+int launch_ks_ip_aut(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum,
+                     int batch, int R, const GaloisSet &g, const fhe_ntt_tables *t, void *stream);
+int launch_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int batch, bool approx,
+                 const void *bconv, void *stream);
 int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK,
                  int dnum, int batch, const fhe_ntt_tables *t, void *stream);
 

@@ -11,6 +11,11 @@
 // kestrel-llm chain (overview, section 4.2).  All constants are fixed per
 // basis, so every product is a lazy Shoup product; the extension sums stay
 // below 2^56 and are reduced once.
+//
+// The approximate variant replaces Garner's recursion by the CRT sum
+//   X + e D = sum_a [x_a (D / d_a)^-1]_{d_a} (D / d_a),   0 <= e < alpha,
+// reduced modulo each target prime without correcting e D: alpha products
+// for the brackets, then alpha multiply-accumulates per target.
 #include <cuda_runtime.h>
 
 #include "fhe_arith.cuh"
@@ -22,21 +27,34 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int MAXA>
+template <int MAXA, bool APPROX>
 __global__ void __launch_bounds__(kThreads)
 k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int dnum, int alpha,
         const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ garner, const ulonglong2 *__restrict__ mr,
         const uint64_t *__restrict__ consts) {
+    // APPROX: `garner` holds the bracket constants [dnum][alpha] and `mr` the
+    // CRT weights [dnum][LK][alpha] of the approximate conversion.
     const long n = 1L << log_n;
     const int j = blockIdx.y, bi = blockIdx.z;
     const int lo = dg[j].lo, cnt = dg[j].count;
-    const ulonglong2 *gj = garner + (long)j * alpha * alpha;
+    const ulonglong2 *gj = garner + (long)j * alpha * (APPROX ? 1 : alpha);
     const ulonglong2 *mj = mr + (long)j * LK * alpha;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
         uint64_t x[MAXA], v[MAXA];
         const uint64_t *src = in + (long)bi * in_stride + (long)lo * n + i;
 #pragma unroll
         for (int a = 0; a < MAXA; a++) x[a] = a < cnt ? __ldcs(src + a * n) : 0;
+        if constexpr (APPROX) {
+#pragma unroll
+            for (int a = 0; a < MAXA; a++) {
+                v[a] = 0;
+                if (a < cnt) {
+                    const uint64_t d = __ldg(consts + (long)(lo + a) * K_COUNT + K_Q);
+                    const ulonglong2 c = __ldg(gj + a);
+                    v[a] = reduce4(shoup_lazy(x[a], c.x, c.y, d), d);
+                }
+            }
+        } else {
         v[0] = x[0];
 #pragma unroll
         for (int a = 1; a < MAXA; a++) {
@@ -52,6 +70,7 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
                 v[a] = reduce4(u, d);
             }
         }
+        }
         uint64_t *dst = ext + ((long)bi * dnum + j) * LK * n + i;
 #pragma unroll
         for (int a = 0; a < MAXA; a++)
@@ -60,12 +79,12 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
             if (l >= lo && l < lo + cnt) continue;
             const uint64_t *kc = consts + (long)l * K_COUNT;
             const uint64_t p = __ldg(kc + K_Q);
-            uint64_t acc = v[0];
+            uint64_t acc = APPROX ? 0 : v[0];   // exact: the weight of v_0 is 1
 #pragma unroll
-            for (int a = 1; a < MAXA; a++) {
+            for (int a = APPROX ? 0 : 1; a < MAXA; a++) {
                 if (a < cnt) {
                     const ulonglong2 m = __ldg(mj + l * alpha + a);
-                    acc += shoup_lazy(v[a], m.x, m.y, p);
+                    acc += shoup_lazy(v[a], m.x, m.y, p);   // < 4p each: sum < 2^56
                 }
             }
             __stcs(dst + (long)l * n, reduce_small(acc, p, (uint32_t)__ldg(kc + K_C58)));
@@ -75,30 +94,31 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
 
 template <int MAXA>
 void launch_modup_t(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
-                    const fhe_ntt_tables *t, const void *modup, cudaStream_t st) {
+                    bool approx, const fhe_ntt_tables *t, const void *modup, cudaStream_t st) {
     const ModupLayout lay = modup_layout(L, K, dnum);
     const char *base = (const char *)modup;
     const long n = 1L << log_n;
     const long bx = (n + kThreads - 1) / kThreads;
     const long cap = ((long)sm_count() * 8 + (long)dnum * batch - 1) / ((long)dnum * batch);
     dim3 grid((unsigned)(bx < cap ? bx : (cap > 0 ? cap : 1)), (unsigned)dnum, (unsigned)batch);
-    k_modup<MAXA><<<grid, kThreads, 0, st>>>(ext, in, in_stride, log_n, L + K, dnum, lay.alpha,
-                                             (const ModupDigit *)(base + lay.off_digits),
-                                             (const ulonglong2 *)(base + lay.off_garner),
-                                             (const ulonglong2 *)(base + lay.off_mr), t->consts);
+    auto kern = approx ? k_modup<MAXA, true> : k_modup<MAXA, false>;
+    kern<<<grid, kThreads, 0, st>>>(ext, in, in_stride, log_n, L + K, dnum, lay.alpha,
+                                    (const ModupDigit *)(base + lay.off_digits),
+                                    (const ulonglong2 *)(base + (approx ? lay.off_qinv : lay.off_garner)),
+                                    (const ulonglong2 *)(base + (approx ? lay.off_qhat : lay.off_mr)), t->consts);
 }
 
 }  // namespace
 
 int launch_modup(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
-                 const fhe_ntt_tables *t, const void *modup, void *stream) {
+                 bool approx, const fhe_ntt_tables *t, const void *modup, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     const int alpha = modup_layout(L, K, dnum).alpha;
-    if (alpha <= 1) launch_modup_t<1>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
-    else if (alpha <= 2) launch_modup_t<2>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
-    else if (alpha <= 4) launch_modup_t<4>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
-    else if (alpha <= 8) launch_modup_t<8>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
-    else launch_modup_t<16>(ext, in, in_stride, log_n, L, K, dnum, batch, t, modup, st);
+    if (alpha <= 1) launch_modup_t<1>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);
+    else if (alpha <= 2) launch_modup_t<2>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);
+    else if (alpha <= 4) launch_modup_t<4>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);
+    else if (alpha <= 8) launch_modup_t<8>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);
+    else launch_modup_t<16>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

@@ -107,7 +107,21 @@ ModupLayout modup_layout(int L, int K, int dnum) {
     s.off_digits = 0;
     s.off_garner = align256((size_t)dnum * sizeof(ModupDigit));
     s.off_mr = align256(s.off_garner + (size_t)dnum * s.alpha * s.alpha * 16);
-    s.bytes = align256(s.off_mr + (size_t)dnum * LK * s.alpha * 16);
+    s.off_qinv = align256(s.off_mr + (size_t)dnum * LK * s.alpha * 16);
+    s.off_qhat = align256(s.off_qinv + (size_t)dnum * s.alpha * 16);
+    s.bytes = align256(s.off_qhat + (size_t)dnum * LK * s.alpha * 16);
+    return s;
+}
+
+BconvLayout bconv_layout(int S, int T) {
+    BconvLayout s;
+    s.off_src = 0;
+    s.off_dst = align256((size_t)S * 8);
+    s.off_garner = align256(s.off_dst + (size_t)T * 16);
+    s.off_mr = align256(s.off_garner + (size_t)S * S * 16);
+    s.off_qinv = align256(s.off_mr + (size_t)T * S * 16);
+    s.off_qhat = align256(s.off_qinv + (size_t)S * 16);
+    s.bytes = align256(s.off_qhat + (size_t)T * S * 16);
     return s;
 }
 
@@ -300,6 +314,89 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
                 mj[(l * alpha + i) * 2 + 1] = shoup(prod, p);
                 prod = mul_mod(prod, qp[lo + i] % p, p);
             }
+        }
+        // approximate conversion: qinv_a = (D_j / d_a)^-1 mod d_a, qhat[l][a] = (D_j / d_a) mod qp_l
+        uint64_t *qi = (uint64_t *)(base + lay.off_qinv) + (size_t)j * alpha * 2;
+        uint64_t *qh = (uint64_t *)(base + lay.off_qhat) + (size_t)j * LK * alpha * 2;
+        for (int a = 0; a < hi - lo; a++) {
+            const uint64_t da = qp[lo + a];
+            uint64_t h = 1 % da;
+            for (int b = 0; b < hi - lo; b++)
+                if (b != a) h = mul_mod(h, qp[lo + b] % da, da);
+            const uint64_t c = inv_mod(h, da);
+            qi[a * 2] = c;
+            qi[a * 2 + 1] = shoup(c, da);
+            for (int l = 0; l < LK; l++) {
+                const uint64_t p = qp[l];
+                uint64_t hp = 1 % p;
+                for (int b = 0; b < hi - lo; b++)
+                    if (b != a) hp = mul_mod(hp, qp[lo + b] % p, p);
+                qh[(l * alpha + a) * 2] = hp;
+                qh[(l * alpha + a) * 2 + 1] = shoup(hp, p);
+            }
+        }
+    }
+    return FHE_OK;
+}
+
+extern "C" int fhe_bconv_tables_bytes(int S, int T, size_t *bytes) {
+    if (!bytes || S < 1 || S > kMaxBconvSrc || T < 1 || T > kMaxTableL) return FHE_EINVAL;
+    *bytes = bconv_layout(S, T).bytes;
+    return FHE_OK;
+}
+
+// Constants of the conversion from src[S] to dst[T] (exact Garner and
+// approximate CRT sum); every prime in (2^48, 2^50), the sources distinct.
+extern "C" int fhe_bconv_tables_build_host(int S, const uint64_t *src, int T, const uint64_t *dst, void *host_blob,
+                                           size_t bytes) {
+    size_t need = 0;
+    if (fhe_bconv_tables_bytes(S, T, &need) != FHE_OK || !src || !dst || !host_blob) return FHE_EINVAL;
+    if (bytes < need) return FHE_ESPACE;
+    auto ok = [](uint64_t q) { return q > (1ull << 48) && q < (1ull << 50) && is_prime_u64(q); };
+    for (int a = 0; a < S; a++) {
+        if (!ok(src[a])) return FHE_EINVAL;
+        for (int b = 0; b < a; b++)
+            if (src[a] == src[b]) return FHE_EINVAL;
+    }
+    for (int t = 0; t < T; t++)
+        if (!ok(dst[t])) return FHE_EINVAL;
+    const BconvLayout lay = bconv_layout(S, T);
+    char *base = (char *)host_blob;
+    std::memset(base, 0, lay.bytes);
+    uint64_t *sp = (uint64_t *)(base + lay.off_src);
+    uint64_t *dp = (uint64_t *)(base + lay.off_dst);
+    uint64_t *garner = (uint64_t *)(base + lay.off_garner);
+    uint64_t *mr = (uint64_t *)(base + lay.off_mr);
+    uint64_t *qi = (uint64_t *)(base + lay.off_qinv);
+    uint64_t *qh = (uint64_t *)(base + lay.off_qhat);
+    for (int a = 0; a < S; a++) {
+        sp[a] = src[a];
+        for (int b = 0; b < a; b++) {
+            const uint64_t c = inv_mod(src[b] % src[a], src[a]);
+            garner[(a * S + b) * 2] = c;
+            garner[(a * S + b) * 2 + 1] = shoup(c, src[a]);
+        }
+        uint64_t h = 1 % src[a];
+        for (int b = 0; b < S; b++)
+            if (b != a) h = mul_mod(h, src[b] % src[a], src[a]);
+        const uint64_t c = inv_mod(h, src[a]);
+        qi[a * 2] = c;
+        qi[a * 2 + 1] = shoup(c, src[a]);
+    }
+    for (int t = 0; t < T; t++) {
+        const uint64_t p = dst[t];
+        dp[t * 2] = p;
+        dp[t * 2 + 1] = (1ull << 58) / p;
+        uint64_t prod = 1 % p;
+        for (int a = 0; a < S; a++) {
+            mr[((size_t)t * S + a) * 2] = prod;
+            mr[((size_t)t * S + a) * 2 + 1] = shoup(prod, p);
+            prod = mul_mod(prod, src[a] % p, p);
+            uint64_t hp = 1 % p;
+            for (int b = 0; b < S; b++)
+                if (b != a) hp = mul_mod(hp, src[b] % p, p);
+            qh[((size_t)t * S + a) * 2] = hp;
+            qh[((size_t)t * S + a) * 2 + 1] = shoup(hp, p);
         }
     }
     return FHE_OK;
