@@ -62,22 +62,27 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def ntt_fwd_traffic():
-    """DRAM bytes per forward-NTT launch from the committed ncu capture, or
-    None when the kernel source has changed since it was taken."""
+def kernel_traffic(key: str, rows_per_launch: int):
+    """DRAM bytes (read + write) per launch of a kernel from the committed ncu
+    capture, or None when the kernel's source has changed since it was taken
+    or the capture was of another launch size."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)["k_ntt_fwd"]
+            rec = json.load(f)[key]
         h = hashlib.sha256()
         for path in rec["source_files"]:
             with open(os.path.join(ROOT, path), "rb") as f:
                 h.update(f.read())
-        if h.hexdigest()[:16] != rec["source_sha256_16"] or rec["rows_per_launch"] != NPOLY * L:
+        if h.hexdigest()[:16] != rec["source_sha256_16"] or rec["rows_per_launch"] != rows_per_launch:
             return None
         return float(rec["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+def ntt_fwd_traffic():
+    return kernel_traffic("k_ntt_fwd", NPOLY * L)
 
 
 def dist_env():
@@ -439,6 +444,451 @@ def sweep(args):
             torch.cuda.empty_cache()
 
 
+# ------------------------------------------------- widened rows of the path --
+#
+# Each workload below is one more part of the key-switch / bootstrap path,
+# timed with the same rules as the headline step: warm-up, CUDA events on the
+# launch stream around exactly `steps` iterations with inputs larger than L2,
+# clocks sampled during the timed region, a live-timed roofline for the
+# row's dominant kernel, an end-to-end number with host buffers, and the
+# oracle on a bounded sample as the CPU baseline.
+
+SHOUP_PER_CLK_SM = BFLY_PER_CLK_SM        # a lazy Shoup product costs what a butterfly's multiply does
+ALU_PEAK_SHOUP = ALU_PEAK_BFLY
+
+
+def _events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _time_calls(fn, reps: int, warm: int = 3) -> float:
+    """Mean ms of `fn` over `reps` back-to-back calls on the current stream."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = _events(2)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _rand_dev(shape_lead, mods, n, seed, dev):
+    import torch
+    from ntt_arithmetic_gb300 import inputs
+    return torch.from_numpy(inputs.uniform_residues(tuple(shape_lead) + (len(mods), n), mods, seed, buffer=7)).to(dev)
+
+
+class RowBench:
+    """One widened workload: subclasses fill in the state, the step, the
+    dominant kernel's probe and the oracle sample."""
+    name = metric = unit = workload = ""
+    units_per_step = 1
+    l2 = "inputs larger than L2"
+
+    def setup(self, dev):
+        raise NotImplementedError
+
+    def step(self):
+        raise NotImplementedError
+
+    def probe(self):
+        """(callable launching the dominant kernel once, roofline dict sans achieved/frac)."""
+        raise NotImplementedError
+
+    def e2e_step(self):
+        """One step through the public API with the H2D copy of its input and
+        the D2H copy of its result; returns (h2d bytes, d2h bytes)."""
+        raise NotImplementedError
+
+    def oracle_setup(self):
+        """Host inputs of the oracle sample (oracle primes + the seeded generator only)."""
+        raise NotImplementedError
+
+    def oracle_sample(self):
+        """(seconds, units of the metric done, description) for a bounded sample."""
+        raise NotImplementedError
+
+    def config(self):
+        return {"workload": self.workload, "l2": self.l2}
+
+
+class ModdownRow(RowBench):
+    name = "moddown"
+    metric = "ModDown (QP->Q) polys/s, NTT domain, n=2^16, 24+8 primes"
+    unit = "poly/s"
+    workload = ("ModDown of the 4 key-switch outputs KS[4][2][32][n] of the headline step (NTT domain, nearest "
+                "rounding, P = 8 primes) -> [4][2][24][n]; n=2^16")
+    units_per_step = 8
+    traffic_rows = 8 * L         # output rows of the captured launch
+
+    def setup(self, dev):
+        import torch
+        from ntt_arithmetic_gb300 import api
+        q = api.find_primes(LOG_N, L)
+        self.qp = q + api.find_primes(LOG_N, K, below=q[-1])
+        self.t = api.NttTables(LOG_N, self.qp, dev)
+        self.md = api.ModdownTables(L, K, self.qp, dev)
+        self.x = _rand_dev((8,), self.qp, N, 31, dev)
+        self.out = torch.empty((8, L, N), dtype=torch.uint64, device=dev)
+        self.ws = torch.empty(api.moddown_workspace_bytes(LOG_N, L, K, 8) // 8, dtype=torch.uint64, device=dev)
+        self.x_pin = self.x.cpu().pin_memory()
+        self.o_pin = torch.empty(self.out.shape, dtype=torch.uint64).pin_memory()
+
+    def step(self):
+        from ntt_arithmetic_gb300 import api
+        api.moddown(self.out, self.x, L, K, self.t, self.md, domain="ntt", nearest=True, workspace=self.ws)
+
+    def probe(self):
+        from ntt_arithmetic_gb300 import api
+        per_coeff = K * (K - 1) // 2 + L * (K - 1) + L      # Garner + extension + final products
+        ops = 8 * N * per_coeff
+        fn = lambda: api.moddown(self.out, self.x, L, K, self.t, self.md, domain="coeff", nearest=True,
+                                 workspace=self.ws)
+        return fn, {"bound": "alu", "work": ops, "peak": ALU_PEAK_SHOUP / 1e9, "unit": "Gmodmul/s",
+                    "kernel": "k_moddown_conv<8,fused> (coefficient-domain ModDown, one pass, batch 8)",
+                    "work_note": f"{per_coeff} lazy Shoup products per coefficient x 8 x 2^16 coefficients",
+                    "algorithmic_bytes": 8 * N * (L + K + L) * 8}
+
+    def e2e_step(self):
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.step()
+        self.o_pin.copy_(self.out, non_blocking=True)
+        return self.x_pin.numel() * 8, self.o_pin.numel() * 8
+
+    def oracle_setup(self):
+        import oracle
+        from ntt_arithmetic_gb300 import inputs
+        self.o_qp = [int(v) for v in oracle.primes(2 * N, L + K)]
+        self.o_ps = oracle.psis(self.o_qp, N)
+        self.o_x = inputs.uniform_residues((2, L + K, N), self.o_qp, 31, buffer=7)
+
+    def oracle_sample(self):
+        import oracle
+        t0 = time.perf_counter()
+        oracle.moddown_ntt_batch(self.o_x, self.o_qp, self.o_ps, L, K, True)
+        return time.perf_counter() - t0, 2, "2 of the 8 polynomials (INTT over QP, ModDown, NTT over Q)"
+
+
+class HoistedRow(RowBench):
+    name = "hoisted"
+    metric = "hoisted rotations (key switches)/s, n=2^16, 24+8 primes, dnum=3, 16 Galois elements"
+    unit = "key switch/s"
+    R = 16
+    workload = ("16 hoisted rotations k = 5^(2^r) mod 2n (r < 16) of one ciphertext component [1][24][n]: one "
+                "ModUp + NTT of the 3 digits, then per rotation the automorphism fused into the inner product with "
+                "that rotation's keys [16][3][2][32][n]; n=2^16")
+    units_per_step = 16
+    traffic_rows = 16 * 2 * (L + K)
+
+    def setup(self, dev):
+        import torch
+        from ntt_arithmetic_gb300 import api
+        q = api.find_primes(LOG_N, L)
+        self.qp = q + api.find_primes(LOG_N, K, below=q[-1])
+        self.t = api.NttTables(LOG_N, self.qp, dev)
+        self.mt = api.ModupTables(L, K, DNUM, self.qp, dev)
+        self.ks = [pow(5, 1 << r, 2 * N) for r in range(self.R)]
+        self.x = _rand_dev((1,), q, N, 41, dev)
+        self.keys = _rand_dev((self.R, DNUM, 2), self.qp, N, 42, dev)
+        self.out = torch.empty((self.R, 1, 2, L + K, N), dtype=torch.uint64, device=dev)
+        self.ws = torch.empty(api.keyswitch_workspace_bytes(LOG_N, L, K, DNUM, 1) // 8, dtype=torch.uint64,
+                              device=dev)
+        self.digits = self.ws.view(1, DNUM, L + K, N)
+        self.x_pin = self.x.cpu().pin_memory()
+        self.o_pin = torch.empty(self.out.shape, dtype=torch.uint64).pin_memory()
+
+    def step(self):
+        from ntt_arithmetic_gb300 import api
+        api.keyswitch_hoisted(self.out, self.x, self.keys, self.ks, L, K, DNUM, self.t, self.mt, self.ws)
+
+    def separate_ms(self, reps):
+        from ntt_arithmetic_gb300 import api
+
+        def fn():
+            for r in range(self.R):
+                api.keyswitch_ip(self.out[r], self.x, self.keys[r], L, K, DNUM, self.t, self.mt, self.ws)
+        return _time_calls(fn, reps)
+
+    def probe(self):
+        from ntt_arithmetic_gb300 import api
+        api.keyswitch_decompose(self.digits, self.x, L, K, DNUM, self.t, self.mt)
+        plane = (L + K) * N * 8
+        bytes_ = self.R * DNUM * 2 * plane + self.R * 2 * plane + DNUM * plane
+        fn = lambda: api.keyswitch_apply(self.out, self.digits, self.keys, L, K, DNUM, self.t, galois=self.ks)
+        return fn, {"bound": "hbm", "work": bytes_, "unit": "GB/s",
+                    "kernel": "k_ks_ip_aut (automorphism fused into the key-switch inner product, 16 rotations)",
+                    "work_note": "keys 16x3x2x32xn + outputs 16x2x32xn + digits 3x32xn words, 8 B each"}
+
+    def e2e_step(self):
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.step()
+        self.o_pin.copy_(self.out, non_blocking=True)
+        return self.x_pin.numel() * 8, self.o_pin.numel() * 8
+
+    def oracle_setup(self):
+        import oracle
+        from ntt_arithmetic_gb300 import inputs
+        self.o_qp = [int(v) for v in oracle.primes(2 * N, L + K)]
+        self.o_ps = oracle.psis(self.o_qp, N)
+        self.o_x = inputs.uniform_residues((1, L, N), self.o_qp[:L], 41, buffer=7)
+        self.o_keys = inputs.uniform_residues((4, DNUM, 2, L + K, N), self.o_qp, 42, buffer=7)
+
+    def oracle_sample(self):
+        import oracle
+        ks = [pow(5, 1 << r, 2 * N) for r in range(4)]
+        t0 = time.perf_counter()
+        oracle.keyswitch_hoisted_batch(self.o_x, self.o_keys, ks, self.o_qp, self.o_ps, L, K, DNUM)
+        return time.perf_counter() - t0, 4, "4 of the 16 rotations (one ModUp + NTT of the digits, 4 x automorphism + IP)"
+
+
+CHAIN_LOG_N, CHAIN_L = 11, 2100
+
+
+class ModraiseRow(RowBench):
+    name = "modraise"
+    metric = "modraise polys/s, n=2^11, level-0 -> 2100-prime chain"
+    unit = "poly/s"
+    workload = ("modraise (exact Garner extension) of 4 level-0 ciphertexts [4][2][1][n] to the 2100-prime boot "
+                "chain [4][2][2100][n], n=2^11; also timed: the exact and approximate conversion of one 8-prime "
+                "key-switch digit to 32 primes at n=2^16")
+    units_per_step = 8
+    traffic_rows = 8 * CHAIN_L
+
+    def setup(self, dev):
+        import torch
+        from ntt_arithmetic_gb300 import api
+        self.chain = api.find_primes(CHAIN_LOG_N, CHAIN_L)
+        n = 1 << CHAIN_LOG_N
+        self.bt = api.BconvTables(self.chain[:1], self.chain, dev)
+        self.x = _rand_dev((8,), self.chain[:1], n, 51, dev)
+        self.out = torch.empty((8, CHAIN_L, n), dtype=torch.uint64, device=dev)
+        self.x_pin = self.x.cpu().pin_memory()
+        self.o_pin = torch.empty(self.out.shape, dtype=torch.uint64).pin_memory()
+        q = api.find_primes(LOG_N, L)
+        qp = q + api.find_primes(LOG_N, K, below=q[-1])
+        self.dt = api.BconvTables(qp[:8], qp, dev)
+        self.dx = _rand_dev((4,), qp[:8], N, 52, dev)
+        self.dout = torch.empty((4, L + K, N), dtype=torch.uint64, device=dev)
+
+    def step(self):
+        from ntt_arithmetic_gb300 import api
+        api.modraise(self.out, self.x, self.bt)
+
+    def extra(self, reps):
+        from ntt_arithmetic_gb300 import api
+        ex = _time_calls(lambda: api.bconv(self.dout, self.dx, self.dt), reps)
+        ap = _time_calls(lambda: api.bconv(self.dout, self.dx, self.dt, approx=True), reps)
+        return {"digit_bconv_8_to_32_n65536_batch4_ms": {"exact": ex, "approx": ap}}
+
+    def probe(self):
+        from ntt_arithmetic_gb300 import api
+        n = 1 << CHAIN_LOG_N
+        bytes_ = 8 * n * 8 + 8 * CHAIN_L * n * 8
+        fn = lambda: api.modraise(self.out, self.x, self.bt)
+        return fn, {"bound": "hbm", "work": bytes_, "unit": "GB/s",
+                    "kernel": "k_bconv<1,exact> (modraise, 8 polys, 1 -> 2100 primes)",
+                    "work_note": "8 input limbs + 8 x 2100 output limbs of 2^11 words"}
+
+    def e2e_step(self):
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.step()
+        self.o_pin.copy_(self.out, non_blocking=True)
+        return self.x_pin.numel() * 8, self.o_pin.numel() * 8
+
+    def oracle_setup(self):
+        import oracle
+        from ntt_arithmetic_gb300 import inputs
+        self.o_chain = [int(v) for v in oracle.primes(2 << CHAIN_LOG_N, CHAIN_L)]
+        self.o_x = inputs.uniform_residues((8, 1, 1 << CHAIN_LOG_N), self.o_chain[:1], 51, buffer=7)
+
+    def oracle_sample(self):
+        import oracle
+        t0 = time.perf_counter()
+        oracle.bconv_batch(self.o_x, self.o_chain[:1], self.o_chain)
+        return time.perf_counter() - t0, 8, "all 8 polynomials (1 -> 2100 primes)"
+
+
+class ChainRow(RowBench):
+    name = "chain2100"
+    metric = "NTT (poly x prime)/s on the 2100-prime chain, n=2^11"
+    unit = "NTT (poly x prime)/s"
+    workload = ("n=2^11, 2100-prime boot chain: fwd NTT of 16 polys (4 ciphertext pairs) -> tensor -> inv NTT of "
+                "the 12 product polys")
+    units_per_step = 28 * CHAIN_L
+    traffic_rows = 16 * CHAIN_L
+
+    def setup(self, dev):
+        import torch
+        from ntt_arithmetic_gb300 import api, inputs
+        self.chain = api.find_primes(CHAIN_LOG_N, CHAIN_L)
+        n = 1 << CHAIN_LOG_N
+        self.t = api.NttTables(CHAIN_LOG_N, self.chain, dev)
+        host = inputs.uniform_residues((2, PAIRS, 2, CHAIN_L, n), self.chain, 61, buffer=0)
+        self.x_pin = torch.from_numpy(host).pin_memory()
+        self.X = self.x_pin.to(dev)
+        self.D = torch.empty((PAIRS, 3, CHAIN_L, n), dtype=torch.uint64, device=dev)
+        self.o_pin = torch.empty(self.D.shape, dtype=torch.uint64).pin_memory()
+
+    def step(self):
+        from ntt_arithmetic_gb300 import api
+        api.ntt_fwd(self.X, self.t)
+        api.tensor(self.D, self.X[0], self.X[1], self.t)
+        api.ntt_inv(self.D, self.t)
+
+    def probe(self):
+        from ntt_arithmetic_gb300 import api
+        n = 1 << CHAIN_LOG_N
+        bfly = 16 * CHAIN_L * (n // 2) * CHAIN_LOG_N
+        fn = lambda: api.ntt_fwd(self.X, self.t)
+        return fn, {"bound": "alu", "work": bfly, "peak": ALU_PEAK_BFLY / 1e9, "unit": "Gbutterfly/s",
+                    "kernel": "k_ntt_fwd<11,0,7,4> (16 polys x 2100 primes)",
+                    "work_note": "16 x 2100 transforms x 1024 x 11 butterflies",
+                    "algorithmic_bytes": 16 * 16 * CHAIN_L * n}
+
+    def e2e_step(self):
+        self.X.copy_(self.x_pin, non_blocking=True)
+        self.step()
+        self.o_pin.copy_(self.D, non_blocking=True)
+        return self.x_pin.numel() * 8, self.o_pin.numel() * 8
+
+    SAMPLE_LIMBS = CHAIN_L
+
+    def oracle_setup(self):
+        import oracle
+        from ntt_arithmetic_gb300 import inputs
+        chain = [int(v) for v in oracle.primes(2 << CHAIN_LOG_N, CHAIN_L)]
+        self.o_qs = chain[:self.SAMPLE_LIMBS]
+        self.o_ps = oracle.psis(self.o_qs, 1 << CHAIN_LOG_N)
+        self.o_x = inputs.uniform_residues((2, 1, 2, self.SAMPLE_LIMBS, 1 << CHAIN_LOG_N), self.o_qs, 61, buffer=7)
+
+    def oracle_sample(self):
+        import oracle
+        threads = oracle.default_threads()
+        t0 = time.perf_counter()
+        X = oracle.ntt_batch(self.o_x, self.o_qs, self.o_ps, threads=threads)
+        D = oracle.tensor_batch(X[0], X[1], self.o_qs)
+        oracle.ntt_batch(D, self.o_qs, self.o_ps, inverse=True, threads=threads)
+        return (time.perf_counter() - t0, 7 * self.SAMPLE_LIMBS,
+                f"1 of the 4 ciphertext pairs on all {self.SAMPLE_LIMBS} primes, {threads} threads")
+
+
+ROWS = {r.name: r for r in (ModdownRow, HoistedRow, ModraiseRow, ChainRow)}
+
+
+def row_bench(args):
+    import torch
+    from ntt_arithmetic_gb300 import api
+    from ntt_arithmetic_gb300 import build as B
+    ws, rank, local = dist_env()
+    row = ROWS[args.workload]()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import build as OB
+        OB.build() if OB.stale() else None
+        import oracle
+        row.oracle_setup()
+        for _ in range(min(args.warmup, 1)):
+            row.oracle_sample()
+        samples = [row.oracle_sample() for _ in range(args.steps)]
+        dt = sum(s[0] for s in samples)
+        units = sum(s[1] for s in samples)
+        value = units / dt
+        print(json.dumps({
+            "impl": "reference", "metric": row.metric, "value": value, "unit": row.unit, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+            "data": "synthetic: seeded uniform residues in [0, q)", "config": row.config(),
+            "cpu_baseline": {"value": value, "unit": row.unit, "cores": oracle.default_threads(), "kind": "oracle",
+                             "sample": samples[0][2]},
+            "e2e": {"value": value, "unit": row.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+    import torch.distributed as dist
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(B.OUT):
+        B.build()
+    if ws > 1:
+        dist.barrier()
+    row.setup(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        row.step()
+    barrier()
+    launches0 = api.launch_count()
+    e0, e1 = _events(2)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            row.step()
+        e1.record(stream)
+        barrier()
+    launches = api.launch_count() - launches0
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    fn, roof = row.probe()
+    kms = _time_calls(fn, max(3, args.steps))
+    achieved = roof.pop("work") / (kms * 1e-3) / 1e9
+    hbm, hbm_kind = peaks()
+    if roof["bound"] == "hbm":
+        roof["peak"], roof["peak_kind"] = hbm, hbm_kind
+    else:
+        roof["peak_kind"] = "derived: measured integer-pipe rates x 152 SMs x 2070 MHz"
+    roof.update({"achieved": achieved, "frac": achieved / roof["peak"], "kernel_ms": kms,
+                 "traffic": kernel_traffic(row.name, row.traffic_rows), "traffic_unit": "bytes/launch"})
+    barrier()
+    e2e_steps = max(1, min(args.steps, 5))
+    f0, f1 = _events(2)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        h2d, d2h = row.e2e_step()
+    f1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
+    line = {
+        "metric": row.metric, "value": whole_job_rate(row.units_per_step, ws, ms), "unit": row.unit,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+        "data": "synthetic: seeded uniform residues in [0, q) (SplitMix64 counter generator)",
+        "config": dict(row.config(), parallelism=f"replicas x{ws}"),
+        "roofline": roof, "clocks": clk.summary(), "gpu_launches": launches,
+        "e2e": {"value": whole_job_rate(row.units_per_step, ws, e2e_ms), "unit": row.unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    if isinstance(row, HoistedRow):
+        sep = row.separate_ms(max(3, args.steps // 2))
+        line["separate_keyswitch_ms_per_step"] = sep
+        line["hoisting_speedup"] = sep / ms
+    if isinstance(row, ModraiseRow):
+        line.update(row.extra(max(3, args.steps)))
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        from oracle import build as OB
+        OB.build() if OB.stale() else None
+        row.oracle_setup()
+        dt, units, desc = row.oracle_sample()
+        line["cpu_baseline"] = {"value": units / dt, "unit": row.unit, "cores": oracle.default_threads(),
+                                "kind": "oracle", "sample": f"{desc}; {dt:.2f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,8 +899,12 @@ def main():
     ap.add_argument("--cpu-sample-steps", type=int, default=2)
     ap.add_argument("--sweep", action="store_true", help="time every point of the n / L / batch sweep instead")
     ap.add_argument("--sweep-reps", type=int, default=5)
+    ap.add_argument("--workload", choices=["step"] + sorted(ROWS), default="step",
+                    help="step: the headline hot-path step; the others time one widened row each")
     args = ap.parse_args()
-    if args.sweep:
+    if args.workload != "step":
+        row_bench(args)
+    elif args.sweep:
         sweep(args)
     elif args.impl == "reference":
         reference(args)

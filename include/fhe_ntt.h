@@ -244,6 +244,27 @@ int fhe_keyswitch_hoisted(uint64_t *out, const uint64_t *in, size_t in_stride, c
                           int modup_mode, const fhe_ntt_tables *t_qp, const void *modup,
                           uint64_t *workspace, size_t ws_bytes, void *stream);
 
+/* The two halves of fhe_keyswitch_ip / fhe_keyswitch_hoisted, for callers
+ * that reuse one decomposition across several calls (more rotations or key
+ * sets later) or schedule the halves on different streams.
+ *
+ * fhe_keyswitch_decompose: digits [batch][dnum][L+K][n] (NTT domain, basis
+ * qp) = NTT(X_j) of every digit of `in` (arguments as fhe_keyswitch_ip;
+ * `digits` is fhe_keyswitch_workspace_bytes long and must not overlap in or
+ * the tables).
+ *
+ * fhe_keyswitch_apply: with galois == NULL and R == 1,
+ *   out[b][c][l] = sum_j digits[b][j][l] * keys[j][c][l]            (keys [dnum][2][L+K][n])
+ * otherwise (host array of R odd elements in [1, 2n), 1 <= R <= 64)
+ *   out[r][b][c][l] = sum_j sigma_{galois[r]}(digits[b][j])[l] * keys[r][j][c][l]
+ * out must not overlap digits, keys or the tables. */
+int fhe_keyswitch_decompose(uint64_t *digits, const uint64_t *in, size_t in_stride, int log_n, int L, int K,
+                            int dnum, int batch, int modup_mode, const fhe_ntt_tables *t_qp,
+                            const void *modup, void *stream);
+int fhe_keyswitch_apply(uint64_t *out, const uint64_t *digits, const uint64_t *keys, const uint32_t *galois,
+                        int R, int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
+                        void *stream);
+
 /* ---- basis conversion and modraise ------------------------------------ */
 
 #define FHE_BCONV_EXACT 0    /* Garner: X in [0, Q) */

@@ -74,6 +74,10 @@ SIGNATURES = {
                                    ctypes.POINTER(NttTables), _vp, _vp, _size, _vp]),
     "fhe_keyswitch_hoisted": (_int, [_vp, _vp, _size, _vp, ctypes.POINTER(ctypes.c_uint32), _int, _int, _int, _int,
                                      _int, _int, _int, ctypes.POINTER(NttTables), _vp, _vp, _size, _vp]),
+    "fhe_keyswitch_decompose": (_int, [_vp, _vp, _size, _int, _int, _int, _int, _int, _int,
+                                       ctypes.POINTER(NttTables), _vp, _vp]),
+    "fhe_keyswitch_apply": (_int, [_vp, _vp, _vp, ctypes.POINTER(ctypes.c_uint32), _int, _int, _int, _int, _int, _int,
+                                   ctypes.POINTER(NttTables), _vp]),
     "fhe_bconv_tables_bytes": (_int, [_int, _int, ctypes.POINTER(_size)]),
     "fhe_bconv_tables_build_host": (_int, [_int, _u64p, _int, _u64p, _vp, _size]),
     "fhe_bconv": (_int, [_vp, _vp, _int, _int, _int, _int, _int, _vp, _vp]),

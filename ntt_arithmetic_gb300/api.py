@@ -337,6 +337,44 @@ def rescale(out: torch.Tensor, x: torch.Tensor, tables_q: NttTables, rs: Moddown
                    stream=stream)
 
 
+def keyswitch_decompose(digits: torch.Tensor, x: torch.Tensor, L: int, K: int, dnum: int, tables_qp: NttTables,
+                        modup: ModupTables, stream=None, in_offset: int = 0, in_stride: int = 0,
+                        batch: int | None = None, approx: bool = False) -> torch.Tensor:
+    """digits [batch, dnum, L+K, n] (NTT domain) = NTT of every extended digit
+    of x (x as in keyswitch_ip)."""
+    _residues(digits, "digits")
+    _residues(x, "x")
+    n = digits.shape[-1]
+    log_n = _log2(n)
+    batch = _ks_input(x, L, n, in_offset, in_stride, batch)
+    if tuple(digits.shape[-3:]) != (dnum, L + K, n) or digits.numel() != batch * dnum * (L + K) * n:
+        raise ValueError("digits must be [batch, dnum, L+K, n]")
+    src = ctypes.c_void_p(x.data_ptr() + 8 * in_offset)
+    N.call("fhe_keyswitch_decompose", _ptr(digits), src, in_stride, log_n, L, K, dnum, batch,
+           N.FHE_MODUP_APPROX if approx else N.FHE_MODUP_EXACT, tables_qp.ref(), _ptr(modup.blob),
+           _stream(x.device, stream))
+    return digits
+
+
+def keyswitch_apply(out: torch.Tensor, digits: torch.Tensor, keys: torch.Tensor, L: int, K: int, dnum: int,
+                    tables_qp: NttTables, galois: Sequence[int] | None = None, stream=None) -> torch.Tensor:
+    """Inner product of precomputed digits with keys; with `galois`, one
+    rotation per element, the automorphism fused into the read."""
+    for t, nm in ((out, "out"), (digits, "digits"), (keys, "keys")):
+        _residues(t, nm)
+    n = digits.shape[-1]
+    log_n = _log2(n)
+    batch = digits.numel() // (dnum * (L + K) * n)
+    R = 1 if galois is None else len(galois)
+    kshape = (dnum, 2, L + K, n) if galois is None else (R, dnum, 2, L + K, n)
+    if tuple(keys.shape) != kshape or out.numel() != R * batch * 2 * (L + K) * n:
+        raise ValueError("keys/out shapes do not match")
+    gal = None if galois is None else (ctypes.c_uint32 * max(R, 1))(*[int(k) for k in galois])
+    N.call("fhe_keyswitch_apply", _ptr(out), _ptr(digits), _ptr(keys), gal, R, log_n, L, K, dnum, batch,
+           tables_qp.ref(), _stream(digits.device, stream))
+    return out
+
+
 # ------------------------------------------------------ basis conversion ---
 
 class BconvTables:

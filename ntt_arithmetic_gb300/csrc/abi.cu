@@ -257,6 +257,63 @@ extern "C" int fhe_keyswitch_hoisted(uint64_t *out, const uint64_t *in, size_t i
                           workspace, ws_bytes, stream);
 }
 
+extern "C" int fhe_keyswitch_decompose(uint64_t *digits, const uint64_t *in, size_t in_stride, int log_n, int L,
+                                       int K, int dnum, int batch, int modup_mode, const fhe_ntt_tables *t_qp,
+                                       const void *modup, void *stream) {
+    size_t need = 0;
+    int s = fhe_keyswitch_workspace_bytes(log_n, L, K, dnum, batch, &need);
+    if (s) return s;
+    const int LK = L + K;
+    if ((s = check_shape(log_n, LK, (long)batch * dnum))) return s;
+    if ((s = check_tables(t_qp, log_n, LK))) return s;
+    if (modup_mode != FHE_MODUP_EXACT && modup_mode != FHE_MODUP_APPROX) return FHE_EINVAL;
+    if (!digits || !in || !modup || !aligned16(digits) || !aligned16(in) || !aligned16(modup)) return FHE_EINVAL;
+    const size_t item = (size_t)L << log_n;
+    if (in_stride == 0) in_stride = item;
+    if (in_stride < item || (in_stride & 1)) return FHE_EINVAL;
+    if ((s = select_device({digits, in, modup, t_qp->blob}))) return s;
+    const Span sd{digits, need}, si{in, ((size_t)(batch - 1) * in_stride + item) * 8}, tb{t_qp->blob, t_qp->bytes},
+        sm{modup, modup_layout(L, K, dnum).bytes};
+    if (overlap(sd, si) || overlap(sd, tb) || overlap(sd, sm)) return FHE_EALIAS;
+    int launched = 0, r;
+    if ((r = launch_modup(digits, in, (long)in_stride, log_n, L, K, dnum, batch, modup_mode == FHE_MODUP_APPROX, t_qp,
+                          modup, stream)) < 0)
+        return finish(-1);
+    launched += r;
+    if ((r = launch_ntt(digits, log_n, LK, (long)batch * dnum * LK, t_qp, false, stream)) < 0) return finish(-1);
+    return finish(launched + r);
+}
+
+extern "C" int fhe_keyswitch_apply(uint64_t *out, const uint64_t *digits, const uint64_t *keys, const uint32_t *galois,
+                                   int R, int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
+                                   void *stream) {
+    const int LK = L + K;
+    int s = check_shape(log_n, LK, (long)batch * dnum);
+    if (s) return s;
+    if ((s = check_tables(t_qp, log_n, LK))) return s;
+    if (dnum < 1 || dnum > LK || R < 1 || R > kMaxRotations || (!galois && R != 1)) return FHE_EINVAL;
+    if (!out || !digits || !keys || !aligned16(out) || !aligned16(digits) || !aligned16(keys)) return FHE_EINVAL;
+    GaloisSet g = {};
+    if (galois) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, galois) != cudaSuccess) cudaGetLastError();
+        else if (a.type == cudaMemoryTypeDevice) return FHE_EDEVICE;
+        const uint64_t two_n = 2ull << log_n;
+        for (int r = 0; r < R; r++) {
+            if (!(galois[r] & 1) || galois[r] >= two_n) return FHE_EINVAL;
+            g.k[r] = galois[r];
+        }
+    }
+    if ((s = select_device({out, digits, keys, t_qp->blob}))) return s;
+    const size_t plane = ((size_t)LK << log_n) * 8;
+    const Span so{out, 2 * plane * batch * R}, sd{digits, plane * dnum * batch}, sk{keys, 2 * plane * dnum * R},
+        tb{t_qp->blob, t_qp->bytes};
+    if (overlap(so, sd) || overlap(so, sk) || overlap(so, tb)) return FHE_EALIAS;
+    const int r = galois ? launch_ks_ip_aut(out, digits, keys, log_n, LK, dnum, batch, R, g, t_qp, stream)
+                         : launch_ks_ip(out, digits, keys, log_n, LK, dnum, batch, t_qp, stream);
+    return finish(r);
+}
+
 extern "C" int fhe_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int batch, int mode,
                          const void *bconv, void *stream) {
     size_t tb = 0;

@@ -169,3 +169,28 @@ def test_hoisted_arguments_and_launches(g):
     c0 = g.api.launch_count()
     g.api.keyswitch_hoisted(out[:3], x, keys[:3], [1, 5, 25], L, K, dnum, t, mt)
     assert g.api.launch_count() - c0 == 3             # ModUp, NTT of the digits, fused automorphism + IP
+
+
+def test_decompose_apply_equal_the_one_call_forms(g):
+    import torch
+    log_n, L, K, dnum, batch = 12, 8, 4, 3, 2
+    n = 1 << log_n
+    qp = g.qp_basis(log_n, L, K)
+    t = g.tables(log_n, tuple(qp))
+    mt = g.api.ModupTables(L, K, dnum, qp)
+    x = g.dev(inputs.uniform_residues((batch, L, n), qp[:L], 860, buffer=0))
+    keys = g.dev(inputs.uniform_residues((3 * dnum * 2, L + K, n), qp, 861, buffer=1)).view(3, dnum, 2, L + K, n)
+    ks = [5, 25, 2 * n - 1]
+    for approx in (False, True):
+        digits = torch.empty((batch, dnum, L + K, n), dtype=torch.uint64, device="cuda")
+        g.api.keyswitch_decompose(digits, x, L, K, dnum, t, mt, approx=approx)
+        one = torch.empty((batch, 2, L + K, n), dtype=torch.uint64, device="cuda")
+        g.api.keyswitch_apply(one, digits, keys[0], L, K, dnum, t)
+        ref = torch.empty_like(one)
+        g.api.keyswitch_ip(ref, x, keys[0], L, K, dnum, t, mt, approx=approx)
+        assert g.same_bits(one, ref)
+        rot = torch.empty((3, batch, 2, L + K, n), dtype=torch.uint64, device="cuda")
+        g.api.keyswitch_apply(rot, digits, keys, L, K, dnum, t, galois=ks)
+        ref = torch.empty_like(rot)
+        g.api.keyswitch_hoisted(ref, x, keys, ks, L, K, dnum, t, mt, approx=approx)
+        assert g.same_bits(rot, ref)
