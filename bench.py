@@ -195,12 +195,15 @@ def build_state(device, seed: int = 3):
     return st
 
 
-def run_step(st, step: int, ev=None):
-    """One pass of the hot path; `ev` (list of 7 events) brackets each call."""
+def run_step(st, step: int, ev=None, X=None, KS=None):
+    """One pass of the hot path on input X (default st["X"]) into KS
+    (default st["KS"]); `ev` (list of 7 events) brackets each call."""
     from ntt_arithmetic_gb300 import api
     k = pow(5, 1 << (step % 16), 2 * N)
     rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
-    X, Y, D = st["X"], st["Y"], st["D"]
+    X = st["X"] if X is None else X
+    KS = st["KS"] if KS is None else KS
+    Y, D = st["Y"], st["D"]
     rec(0)
     api.ntt_fwd(X, st["tq"])
     rec(1)
@@ -213,9 +216,55 @@ def run_step(st, step: int, ev=None):
     api.ntt_inv(D, st["tq"])
     rec(5)
     # relinearisation input: component d2 of each of the 4 products (batch stride 3 L n)
-    api.keyswitch_ip(st["KS"], D, st["keys"], L, K, DNUM, st["tqp"], st["modup"], st["ws"],
+    api.keyswitch_ip(KS, D, st["keys"], L, K, DNUM, st["tqp"], st["modup"], st["ws"],
                      in_offset=2 * L * N, in_stride=3 * L * N, batch=PAIRS)
     rec(6)
+
+
+def e2e_steps(st, steps: int, device) -> float:
+    """Mean ms per step end to end: every step copies its input X from pinned
+    host memory and reads its key-switch output back to pinned host memory.
+    The copies run on their own streams, double-buffered, so step i's input
+    copy and step i-1's output copy overlap step i-1's and step i's kernels
+    (a serving pipeline); events order every buffer reuse."""
+    import torch
+    # three non-default streams: the legacy default stream would serialise
+    # with the copy streams
+    comp, s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
+    if "X2" not in st:
+        st["X2"] = torch.empty_like(st["X"])
+        st["KS2"] = torch.empty_like(st["KS"])
+        st["ks_pinned2"] = torch.empty(st["KS"].shape, dtype=torch.uint64).pin_memory()
+    Xb, KSb, outb = [st["X"], st["X2"]], [st["KS"], st["KS2"]], [st["ks_pinned"], st["ks_pinned2"]]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]     # step's kernels finished with X[b] and KS[b]
+    ev_out = [torch.cuda.Event() for _ in range(2)]      # KS[b] copied out
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    start.record(comp)
+    for e in ev_done + ev_out:
+        e.record(comp)
+    for i in range(steps):
+        b = i % 2
+        s_in.wait_event(start)
+        s_in.wait_event(ev_done[b])              # X[b] no longer read by step i-2
+        with torch.cuda.stream(s_in):
+            Xb[b].copy_(st["x_pinned"], non_blocking=True)
+        ev_in[b].record(s_in)
+        comp.wait_event(ev_in[b])
+        comp.wait_event(ev_out[b])               # KS[b] of step i-2 copied out
+        with torch.cuda.stream(comp):
+            run_step(st, i, X=Xb[b], KS=KSb[b])
+        ev_done[b].record(comp)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            outb[b].copy_(KSb[b], non_blocking=True)
+        ev_out[b].record(s_out)
+    for e in ev_out:
+        comp.wait_event(e)
+    stop.record(comp)
+    torch.cuda.synchronize(device)
+    return start.elapsed_time(stop) / steps
 
 
 def ours(args):
@@ -259,19 +308,11 @@ def ours(args):
     kern = [statistics.mean(p[j] for p in per) for j in range(6)]
     ms_max = max_over_ranks(ms, device)
 
-    # end to end through the public API with host buffers: pinned H2D of the
-    # step's input, the whole step, D2H of its key-switch output
-    e2e_steps = max(1, min(args.steps, 5))
+    # end to end through the public API with host buffers: every step copies
+    # its input from pinned host memory and its key-switch output back
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        st["X"].copy_(st["x_pinned"], non_blocking=True)
-        run_step(st, i)
-        st["ks_pinned"].copy_(st["KS"], non_blocking=True)
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
+    e2e_steps(st, max(3, args.warmup), device)          # warm-up of the copy pipeline (streams, pinned buffers)
+    e2e_ms = max_over_ranks(e2e_steps(st, args.steps, device), device)
 
     clocks = clk.summary()
     hbm, hbm_kind = peaks()
@@ -306,8 +347,9 @@ def ours(args):
                      "hbm_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9, "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind},
         "clocks": clocks,
         "gpu_launches": launches,
-        "e2e": {"value": whole_job_rate(UNITS, ws, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": st["x_pinned"].numel() * 8, "d2h_bytes_per_step": st["ks_pinned"].numel() * 8},
+        "e2e": {"value": whole_job_rate(UNITS, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms, "steps": args.steps,
+                "h2d_bytes_per_step": st["x_pinned"].numel() * 8, "d2h_bytes_per_step": st["ks_pinned"].numel() * 8,
+                "pipelining": "input/output copies on their own streams, double-buffered across steps"},
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_sample_steps)
@@ -851,14 +893,14 @@ def row_bench(args):
     roof.update({"achieved": achieved, "frac": achieved / roof["peak"], "kernel_ms": kms,
                  "traffic": kernel_traffic(row.name, row.traffic_rows), "traffic_unit": "bytes/launch"})
     barrier()
-    e2e_steps = max(1, min(args.steps, 5))
+    n_e2e = max(1, min(args.steps, 5))
     f0, f1 = _events(2)
     f0.record(stream)
-    for _ in range(e2e_steps):
+    for _ in range(n_e2e):
         h2d, d2h = row.e2e_step()
     f1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / n_e2e, dev)
     line = {
         "metric": row.metric, "value": whole_job_rate(row.units_per_step, ws, ms), "unit": row.unit,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

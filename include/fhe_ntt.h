@@ -98,7 +98,8 @@ typedef struct fhe_ntt_tables {
     int32_t L;                /* number of primes covered */
     const uint64_t *q;        /* [L] moduli */
     const uint64_t *consts;   /* [L][16] per-prime constants */
-    const uint64_t *fwd;      /* [L][n][2] forward twiddles and Shoup companions */
+    const uint64_t *fwd;      /* [L][n][2] forward twiddles and Shoup companions, the value
+                                 psi^brv(k) at slot fhe_ntt_fwd_table_slot(log_n, k) */
     const uint64_t *inv;      /* [L][n][2] inverse (cyclic) twiddles and companions */
     const uint64_t *twist;    /* [L][n][2] n^-1 psi^-j and companions */
     const void *blob;         /* base of the device blob */
@@ -116,6 +117,13 @@ int fhe_ntt_tables_build_host(int log_n, int L, const uint64_t *q, void *host_bl
 
 /* Fill *out with device pointers into dev_blob (no copy, no launch). */
 int fhe_ntt_tables_bind(const void *dev_blob, size_t bytes, int log_n, int L, fhe_ntt_tables *out);
+
+/* Where the forward twiddle of index k (value psi^brv(k), 0 <= k < n) is
+ * stored in a prime's fwd table: the stages of the transform's last register
+ * pass keep their twiddles in the order that pass reads them (consecutive
+ * threads, consecutive entries); every other entry is at slot k.  For tools
+ * that read or write table blobs. */
+int fhe_ntt_fwd_table_slot(int log_n, uint32_t k, uint32_t *slot);
 
 /* ---- transforms -------------------------------------------------------- */
 

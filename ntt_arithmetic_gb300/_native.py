@@ -60,6 +60,7 @@ SIGNATURES = {
     "fhe_ntt_tables_bytes": (_int, [_int, _int, ctypes.POINTER(_size)]),
     "fhe_ntt_tables_build_host": (_int, [_int, _int, _u64p, _vp, _size]),
     "fhe_ntt_tables_bind": (_int, [_vp, _size, _int, _int, ctypes.POINTER(NttTables)]),
+    "fhe_ntt_fwd_table_slot": (_int, [_int, ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "fhe_ntt_fwd": (_int, [_vp, _int, _int, _int, ctypes.POINTER(NttTables), _vp]),
     "fhe_ntt_inv": (_int, [_vp, _int, _int, _int, ctypes.POINTER(NttTables), _vp]),
     "fhe_mul_ntt": (_int, [_vp, _vp, _vp, _int, _int, _int, ctypes.POINTER(NttTables), _vp]),

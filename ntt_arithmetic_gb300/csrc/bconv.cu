@@ -11,9 +11,10 @@
 // modulo p without the correction.  Every product is by a precomputed constant
 // (lazy Shoup); each target's sum stays below 2^56 and is reduced once.
 //
-// Layout: in [batch][S][n], out [batch][T][n].  One thread per coefficient
-// computes the digits once and then a contiguous chunk of targets (grid y), so
-// a long target chain (thousands of primes at n = 2^11) still fills the GPU.
+// Layout: in [batch][S][n], out [batch][T][n].  One thread per pair of
+// coefficients computes their digits once and then a contiguous chunk of
+// targets (grid y), so a long target chain (thousands of primes at n = 2^11)
+// still fills the GPU.
 #include <cuda_runtime.h>
 
 #include "fhe_arith.cuh"
@@ -25,6 +26,37 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Digits of one coefficient from its S source residues (in place in v).
+template <int MAXS, bool APPROX>
+__device__ __forceinline__ void bconv_digits(uint64_t (&v)[MAXS], int S, const uint64_t *__restrict__ src,
+                                             const ulonglong2 *__restrict__ garner) {
+    if constexpr (APPROX) {
+#pragma unroll
+        for (int a = 0; a < MAXS; a++) {
+            if (a < S) {
+                const uint64_t q = __ldg(src + a);
+                const ulonglong2 c = __ldg(garner + a);
+                v[a] = reduce4(shoup_lazy(v[a], c.x, c.y, q), q);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int a = 1; a < MAXS; a++) {
+            if (a < S) {
+                const uint64_t q = __ldg(src + a);
+                uint64_t u = v[a];
+#pragma unroll
+                for (int c = 0; c < a; c++) {
+                    const ulonglong2 g = __ldg(garner + a * S + c);
+                    u = shoup_lazy(u + 4 * q - v[c], g.x, g.y, q);   // v_c < 2^50 < 4 q
+                }
+                v[a] = reduce4(u, q);
+            }
+        }
+    }
+}
+
+// One thread per pair of adjacent coefficients (16-byte loads and stores).
 template <int MAXS, bool APPROX>
 __global__ void __launch_bounds__(kThreads)
 k_bconv(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n, int S, int T, int tchunk,
@@ -36,47 +68,34 @@ k_bconv(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n, 
     const long b = blockIdx.z;
     const int t0 = blockIdx.y * tchunk;
     const int t1 = t0 + tchunk < T ? t0 + tchunk : T;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-        uint64_t v[MAXS];
+    for (long i = 2 * ((long)blockIdx.x * blockDim.x + threadIdx.x); i < n; i += 2L * gridDim.x * blockDim.x) {
+        uint64_t v0[MAXS], v1[MAXS];
 #pragma unroll
-        for (int a = 0; a < MAXS; a++) v[a] = a < S ? __ldcs(in + (b * S + a) * n + i) : 0;
-        if constexpr (APPROX) {
-#pragma unroll
-            for (int a = 0; a < MAXS; a++) {
-                if (a < S) {
-                    const uint64_t q = __ldg(src + a);
-                    const ulonglong2 c = __ldg(garner + a);
-                    v[a] = reduce4(shoup_lazy(v[a], c.x, c.y, q), q);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int a = 1; a < MAXS; a++) {
-                if (a < S) {
-                    const uint64_t q = __ldg(src + a);
-                    uint64_t u = v[a];
-#pragma unroll
-                    for (int c = 0; c < a; c++) {
-                        const ulonglong2 g = __ldg(garner + a * S + c);
-                        u = shoup_lazy(u + 4 * q - v[c], g.x, g.y, q);   // v_c < 2^50 < 4 q
-                    }
-                    v[a] = reduce4(u, q);
-                }
+        for (int a = 0; a < MAXS; a++) {
+            v0[a] = v1[a] = 0;
+            if (a < S) {
+                const ulonglong2 x = __ldcs(reinterpret_cast<const ulonglong2 *>(in + (b * S + a) * n + i));
+                v0[a] = x.x;
+                v1[a] = x.y;
             }
         }
+        bconv_digits<MAXS, APPROX>(v0, S, src, garner);
+        bconv_digits<MAXS, APPROX>(v1, S, src, garner);
         uint64_t *o = out + b * T * n + i;
         for (int t = t0; t < t1; t++) {
             const ulonglong2 pc = __ldg(dst + t);   // (p, floor(2^58 / p))
             const ulonglong2 *wt = weights + (long)t * S;
-            uint64_t acc = APPROX ? 0 : v[0];      // exact: the weight of v_0 is 1
+            uint64_t acc0 = APPROX ? 0 : v0[0], acc1 = APPROX ? 0 : v1[0];   // exact: the weight of v_0 is 1
 #pragma unroll
             for (int a = APPROX ? 0 : 1; a < MAXS; a++) {
                 if (a < S) {
                     const ulonglong2 m = __ldg(wt + a);
-                    acc += shoup_lazy(v[a], m.x, m.y, pc.x);   // < 4p each: sum < 2^56
+                    acc0 += shoup_lazy(v0[a], m.x, m.y, pc.x);   // < 4p each: sum < 2^56
+                    acc1 += shoup_lazy(v1[a], m.x, m.y, pc.x);
                 }
             }
-            __stcs(o + (long)t * n, reduce_small(acc, pc.x, (uint32_t)pc.y));
+            __stcs(reinterpret_cast<ulonglong2 *>(o + (long)t * n),
+                   make_ulonglong2(reduce_small(acc0, pc.x, (uint32_t)pc.y), reduce_small(acc1, pc.x, (uint32_t)pc.y)));
         }
     }
 }
@@ -86,7 +105,7 @@ void launch_t(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int ba
               cudaStream_t st) {
     const BconvLayout lay = bconv_layout(S, T);
     const long n = 1L << log_n;
-    const long bx = (n + kThreads - 1) / kThreads;
+    const long bx = (n / 2 + kThreads - 1) / kThreads;   // one thread per coefficient pair
     // enough CTAs for 8 per SM; each chunk repeats the digit computation once
     const long want = (long)sm_count() * 8;
     long chunks = (want + bx * batch - 1) / (bx * batch);

@@ -37,6 +37,7 @@
 
 #include "fhe_arith.cuh"
 #include "fhe_internal.h"
+#include "ntt_shapes.h"
 
 namespace cg = cooperative_groups;
 
@@ -256,7 +257,11 @@ __device__ __forceinline__ void fwd_stage(uint64_t (&x)[SH::E], const Ctx &c) {
             const int base = (1 << S) + (c.r << (SH::LOGM - B - EP + I)) + ((g >> B) << I);
 #pragma unroll
             for (int jj = 0; jj < NW; jj++) {
-                const ulonglong2 w = __ldg(c.tw + base + jj);
+                // the last pass (B = 0) reads its twiddles from the (r, jj, g)
+                // order of the table (fwd_table_slot): coalesced across g
+                const int slot = B == 0 ? (1 << S) + (c.r << (SH::LOGM - EP + I)) + (jj << (SH::LOGM - EP)) + g
+                                        : base + jj;
+                const ulonglong2 w = __ldg(c.tw + slot);
 #pragma unroll
                 for (int u = 0; u < HALF; u++) {
                     const int j = jj * 2 * HALF + u;
@@ -657,41 +662,6 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
 }
 
 }  // namespace
-
-// Launch shape per log2(n): cluster size (log2 C), threads per CTA (log2 T),
-// residues per thread (log2 E, = radix of a register pass) and the minimum
-// number of resident CTAs per SM the register allocation must allow.
-#define FHE_SHAPE_1 0, 0, 1, 1
-#define FHE_SHAPE_2 0, 0, 2, 1
-#define FHE_SHAPE_3 0, 0, 3, 1
-#define FHE_SHAPE_4 0, 1, 3, 1
-#define FHE_SHAPE_5 0, 2, 3, 1
-#define FHE_SHAPE_6 0, 3, 3, 1
-#define FHE_SHAPE_7 0, 4, 3, 1
-#define FHE_SHAPE_8 0, 5, 3, 1
-#define FHE_SHAPE_9 0, 6, 3, 1
-#define FHE_SHAPE_10 0, 7, 3, 1
-#ifndef FHE_SHAPE_11
-#define FHE_SHAPE_11 0, 7, 4, 4
-#endif
-#ifndef FHE_SHAPE_12
-#define FHE_SHAPE_12 0, 8, 4, 2
-#endif
-#ifndef FHE_SHAPE_13
-#define FHE_SHAPE_13 0, 8, 5, 2
-#endif
-#ifndef FHE_SHAPE_14
-#define FHE_SHAPE_14 1, 8, 5, 2
-#endif
-#ifndef FHE_SHAPE_15
-#define FHE_SHAPE_15 2, 8, 5, 2
-#endif
-#ifndef FHE_SHAPE_16
-#define FHE_SHAPE_16 3, 8, 5, 2
-#endif
-#ifndef FHE_SHAPE_17
-#define FHE_SHAPE_17 4, 8, 5, 2
-#endif
 
 int launch_ntt(uint64_t *res, int log_n, int L, long rows, const fhe_ntt_tables *t, bool inverse, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;

@@ -1,0 +1,99 @@
+// ntt_shapes.h -- launch shape of the NTT kernels per log2(n), shared by the
+// kernels (ntt.cu) and the table builder (tables.cpp), which lays out the
+// forward twiddles of the last register pass in the order that pass reads.
+#pragma once
+
+// Launch shape per log2(n): cluster size (log2 C), threads per CTA (log2 T),
+// residues per thread (log2 E, = radix of a register pass) and the minimum
+// number of resident CTAs per SM the register allocation must allow.
+#define FHE_SHAPE_1 0, 0, 1, 1
+#define FHE_SHAPE_2 0, 0, 2, 1
+#define FHE_SHAPE_3 0, 0, 3, 1
+#define FHE_SHAPE_4 0, 1, 3, 1
+#define FHE_SHAPE_5 0, 2, 3, 1
+#define FHE_SHAPE_6 0, 3, 3, 1
+#define FHE_SHAPE_7 0, 4, 3, 1
+#define FHE_SHAPE_8 0, 5, 3, 1
+#define FHE_SHAPE_9 0, 6, 3, 1
+#define FHE_SHAPE_10 0, 7, 3, 1
+#ifndef FHE_SHAPE_11
+#define FHE_SHAPE_11 0, 7, 4, 4
+#endif
+#ifndef FHE_SHAPE_12
+#define FHE_SHAPE_12 0, 8, 4, 2
+#endif
+#ifndef FHE_SHAPE_13
+#define FHE_SHAPE_13 0, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_14
+#define FHE_SHAPE_14 1, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_15
+#define FHE_SHAPE_15 2, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_16
+#define FHE_SHAPE_16 3, 8, 5, 2
+#endif
+#ifndef FHE_SHAPE_17
+#define FHE_SHAPE_17 4, 8, 5, 2
+#endif
+
+namespace fhe {
+
+struct NttShape {
+    int logc, logt, loge, minb;
+};
+
+constexpr NttShape ntt_shape(int log_n) {
+    switch (log_n) {
+        case 1: return {FHE_SHAPE_1};
+        case 2: return {FHE_SHAPE_2};
+        case 3: return {FHE_SHAPE_3};
+        case 4: return {FHE_SHAPE_4};
+        case 5: return {FHE_SHAPE_5};
+        case 6: return {FHE_SHAPE_6};
+        case 7: return {FHE_SHAPE_7};
+        case 8: return {FHE_SHAPE_8};
+        case 9: return {FHE_SHAPE_9};
+        case 10: return {FHE_SHAPE_10};
+        case 11: return {FHE_SHAPE_11};
+        case 12: return {FHE_SHAPE_12};
+        case 13: return {FHE_SHAPE_13};
+        case 14: return {FHE_SHAPE_14};
+        case 15: return {FHE_SHAPE_15};
+        case 16: return {FHE_SHAPE_16};
+        case 17: return {FHE_SHAPE_17};
+        default: return {0, 0, 1, 1};
+    }
+}
+
+// Stages in the forward transform's last register pass (local bits [0, EP)).
+constexpr int fwd_last_pass_stages(int log_n) {
+    const NttShape s = ntt_shape(log_n);
+    const int logm = log_n - s.logc;
+    const int p = (logm + s.loge - 1) / s.loge;
+    return p == 1 ? logm : s.loge;
+}
+
+// Storage slot of forward twiddle k (the value psi^brv(k), brv over log_n
+// bits) in a prime's fwd table.  Stage s uses k in [2^s, 2^(s+1)); inside
+// the last pass's stages (s >= log_n - EP, I = s - (log_n - EP)) the offset
+// k - 2^s = (r, g, jj) -- cluster rank r, group g of 2^G, G = log_n - logc - EP,
+// twiddle jj of 2^I -- is stored as (r, jj, g), so that the threads of a warp
+// (consecutive g) read consecutive 16-byte entries.  Other stages: slot = k.
+constexpr uint32_t fwd_table_slot(int log_n, uint32_t k) {
+    if (k < 2) return k;
+    int s = 0;
+    while ((k >> (s + 1)) != 0) s++;
+    const int ep = fwd_last_pass_stages(log_n);
+    if (s < log_n - ep) return k;
+    const int i = s - (log_n - ep);
+    const int gbits = log_n - ntt_shape(log_n).logc - ep;
+    const uint32_t off = k - (1u << s);
+    const uint32_t jj = off & ((1u << i) - 1);
+    const uint32_t g = (off >> i) & ((1u << gbits) - 1);
+    const uint32_t r = off >> (i + gbits);
+    return (1u << s) + (r << (i + gbits)) + (jj << gbits) + g;
+}
+
+}  // namespace fhe

@@ -66,10 +66,14 @@ k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_
 
 // out[b][c][l][i] = sum_j ext[b][j][l][i] * keys[j][c][l][i] mod p_l.
 // One thread owns a pair of coefficients of one limb for every batch item,
-// so each key word is fetched from HBM once per call.
+// so each key word is fetched from HBM once per call.  DN > 0 (dnum <= 4):
+// the thread's keys are held in registers across the batch loop and every
+// load of a batch item is issued before its products; DN = 0: any dnum.
+template <int DN>
 __global__ void __launch_bounds__(kThreads)
-k_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, long pairs, int log_n, int LK, int dnum,
+k_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, long pairs, int log_n, int LK, int dnum_rt,
         int batch, const uint64_t *__restrict__ consts) {
+    const int dnum = DN > 0 ? DN : dnum_rt;
     const long plane = (long)LK << log_n;      // one [LK][n] block
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
@@ -78,22 +82,51 @@ k_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, long pairs, in
         const uint64_t *kc = consts + l * K_COUNT;
         const uint64_t q = __ldg(kc + K_Q), mu = __ldg(kc + K_MU12);
         const uint32_t c58 = (uint32_t)__ldg(kc + K_C58);
-        for (int bi = 0; bi < batch; bi++) {
-            uint64_t h0x = 0, l0x = 0, h0y = 0, l0y = 0, h1x = 0, l1x = 0, h1y = 0, l1y = 0;
-            for (int j = 0; j < dnum; j++) {
-                const ulonglong2 dv = __ldcs(reinterpret_cast<const ulonglong2 *>(ext + ((long)bi * dnum + j) * plane + e));
-                const ulonglong2 k0 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j) * plane + e));
-                const ulonglong2 k1 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j + 1) * plane + e));
-                mac128(h0x, l0x, dv.x, k0.x);
-                mac128(h0y, l0y, dv.y, k0.y);
-                mac128(h1x, l1x, dv.x, k1.x);
-                mac128(h1y, l1y, dv.y, k1.y);
+        if constexpr (DN > 0) {
+            ulonglong2 k0[DN], k1[DN];
+#pragma unroll
+            for (int j = 0; j < DN; j++) {
+                k0[j] = __ldcs(reinterpret_cast<const ulonglong2 *>(keys + (2L * j) * plane + e));
+                k1[j] = __ldcs(reinterpret_cast<const ulonglong2 *>(keys + (2L * j + 1) * plane + e));
             }
-            uint64_t *o = out + (long)bi * 2 * plane + e;
-            __stcs(reinterpret_cast<ulonglong2 *>(o),
-                   make_ulonglong2(barrett_reduce128(h0x, l0x, q, mu, c58), barrett_reduce128(h0y, l0y, q, mu, c58)));
-            __stcs(reinterpret_cast<ulonglong2 *>(o + plane),
-                   make_ulonglong2(barrett_reduce128(h1x, l1x, q, mu, c58), barrett_reduce128(h1y, l1y, q, mu, c58)));
+            for (int bi = 0; bi < batch; bi++) {
+                ulonglong2 dv[DN];
+#pragma unroll
+                for (int j = 0; j < DN; j++)
+                    dv[j] = __ldcs(reinterpret_cast<const ulonglong2 *>(ext + ((long)bi * DN + j) * plane + e));
+                uint64_t h0x = 0, l0x = 0, h0y = 0, l0y = 0, h1x = 0, l1x = 0, h1y = 0, l1y = 0;
+#pragma unroll
+                for (int j = 0; j < DN; j++) {
+                    mac128(h0x, l0x, dv[j].x, k0[j].x);
+                    mac128(h0y, l0y, dv[j].y, k0[j].y);
+                    mac128(h1x, l1x, dv[j].x, k1[j].x);
+                    mac128(h1y, l1y, dv[j].y, k1[j].y);
+                }
+                uint64_t *o = out + (long)bi * 2 * plane + e;
+                __stcs(reinterpret_cast<ulonglong2 *>(o), make_ulonglong2(barrett_reduce128(h0x, l0x, q, mu, c58),
+                                                                       barrett_reduce128(h0y, l0y, q, mu, c58)));
+                __stcs(reinterpret_cast<ulonglong2 *>(o + plane),
+                       make_ulonglong2(barrett_reduce128(h1x, l1x, q, mu, c58), barrett_reduce128(h1y, l1y, q, mu, c58)));
+            }
+        } else {
+            for (int bi = 0; bi < batch; bi++) {
+                uint64_t h0x = 0, l0x = 0, h0y = 0, l0y = 0, h1x = 0, l1x = 0, h1y = 0, l1y = 0;
+                for (int j = 0; j < dnum; j++) {
+                    const ulonglong2 dv =
+                        __ldcs(reinterpret_cast<const ulonglong2 *>(ext + ((long)bi * dnum + j) * plane + e));
+                    const ulonglong2 k0 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j) * plane + e));
+                    const ulonglong2 k1 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j + 1) * plane + e));
+                    mac128(h0x, l0x, dv.x, k0.x);
+                    mac128(h0y, l0y, dv.y, k0.y);
+                    mac128(h1x, l1x, dv.x, k1.x);
+                    mac128(h1y, l1y, dv.y, k1.y);
+                }
+                uint64_t *o = out + (long)bi * 2 * plane + e;
+                __stcs(reinterpret_cast<ulonglong2 *>(o), make_ulonglong2(barrett_reduce128(h0x, l0x, q, mu, c58),
+                                                                       barrett_reduce128(h0y, l0y, q, mu, c58)));
+                __stcs(reinterpret_cast<ulonglong2 *>(o + plane),
+                       make_ulonglong2(barrett_reduce128(h1x, l1x, q, mu, c58), barrett_reduce128(h1y, l1y, q, mu, c58)));
+            }
         }
     }
 }
@@ -117,8 +150,10 @@ int launch_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, int log_n, 
 int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,
                  const fhe_ntt_tables *t, void *stream) {
     const long pairs = ((long)LK << log_n) / 2;
-    k_ks_ip<<<stream_grid(pairs, kThreads, 8), kThreads, 0, (cudaStream_t)stream>>>(out, ext, keys, pairs, log_n, LK,
-                                                                                     dnum, batch, t->consts);
+    auto kern = dnum == 1 ? k_ks_ip<1> : dnum == 2 ? k_ks_ip<2> : dnum == 3 ? k_ks_ip<3> : dnum == 4 ? k_ks_ip<4>
+                                                                                                     : k_ks_ip<0>;
+    kern<<<stream_grid(pairs, kThreads, 8), kThreads, 0, (cudaStream_t)stream>>>(out, ext, keys, pairs, log_n, LK, dnum,
+                                                                                  batch, t->consts);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

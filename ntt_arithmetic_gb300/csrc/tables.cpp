@@ -8,6 +8,7 @@
 
 #include "fhe_arith.cuh"
 #include "fhe_internal.h"
+#include "ntt_shapes.h"
 
 namespace {
 
@@ -218,8 +219,9 @@ extern "C" int fhe_ntt_tables_build_host(int log_n, int L, const uint64_t *q, vo
         for (uint64_t k = 0; k < n; k++) {
             // forward (psi-merged, bit-reversed): fwd[k] = psi^brv(k), brv over log_n bits
             const uint64_t w = pw[bit_reverse((uint32_t)k, log_n)];
-            f[2 * k] = w;
-            f[2 * k + 1] = shoup(w, ql);
+            const uint32_t slot = fwd_table_slot(log_n, (uint32_t)k);
+            f[2 * slot] = w;
+            f[2 * slot + 1] = shoup(w, ql);
             // twist of the inverse: twist[j] = n^-1 psi^-j
             const uint64_t tj = mul_mod(ninv, ipw[k], ql);
             tw[2 * k] = tj;
@@ -496,4 +498,10 @@ int selftest_arith(uint64_t seed, int iters) {
 
 extern "C" int fhe_selftest_host(uint64_t seed, int iters) {
     return fhe::selftest_arith(seed, iters) == 0 ? FHE_OK : FHE_EINVAL;
+}
+
+extern "C" int fhe_ntt_fwd_table_slot(int log_n, uint32_t k, uint32_t *slot) {
+    if (!slot || log_n < 1 || log_n > kMaxLogN || k >= (1u << log_n)) return FHE_EINVAL;
+    *slot = fwd_table_slot(log_n, k);
+    return FHE_OK;
 }

@@ -102,13 +102,32 @@ def test_tables_contents(lib):
         psi = oracle.psi(q, 2 * n)
         for k in range(1, n):
             w = pow(psi, oracle.brv(k, log_n), q)
-            assert int(fwd[l, k, 0]) == w and int(fwd[l, k, 1]) == (w << 64) // q
+            slot = ctypes.c_uint32()
+            assert lib.fhe_ntt_fwd_table_slot(log_n, k, ctypes.byref(slot)) == 0
+            assert int(fwd[l, slot.value, 0]) == w and int(fwd[l, slot.value, 1]) == (w << 64) // q
             h = 1 << (k.bit_length() - 1)
             wi = pow(psi, -(k - h) * (n // h), q)
             assert int(inv[l, k, 0]) == wi and int(inv[l, k, 1]) == (wi << 64) // q
         for j in range(n):
             tj = pow(n, -1, q) * pow(psi, -j, q) % q
             assert int(twi[l, j, 0]) == tj and int(twi[l, j, 1]) == (tj << 64) // q
+
+
+@pytest.mark.parametrize("log_n", list(range(1, 18)))
+def test_fwd_table_slots_are_a_permutation_within_each_stage(lib, log_n):
+    """The stored order of the forward twiddles is a permutation of each
+    stage's block [2^s, 2^(s+1)), the identity outside the last pass."""
+    n = 1 << log_n
+    slot = ctypes.c_uint32()
+    slots = []
+    for k in range(n):
+        assert lib.fhe_ntt_fwd_table_slot(log_n, k, ctypes.byref(slot)) == 0
+        slots.append(slot.value)
+    assert sorted(slots) == list(range(n))
+    for k, s_ in enumerate(slots):
+        if k >= 2:
+            assert s_.bit_length() == k.bit_length()
+    assert lib.fhe_ntt_fwd_table_slot(log_n, n, ctypes.byref(slot)) == N.FHE_EINVAL
 
 
 def test_table_builder_rejects_bad_moduli(lib):
