@@ -51,6 +51,7 @@ SMS, SM_MAX_MHZ = 152, 2070.0
 ALU_PEAK_BFLY = SMS * BFLY_PER_CLK_SM * SM_MAX_MHZ * 1e6
 BFLY_PER_FWD = NPOLY * L * (N // 2) * LOG_N
 NTT_BYTES_PER_FWD = 16 * NPOLY * L * N     # read + write every residue once
+KS_MIN_BYTES_X4 = 8 * N * (PAIRS * (L + 2 * (L + K)) + DNUM * 2 * (L + K))   # 285.2 MB
 
 
 def peaks():
@@ -340,6 +341,9 @@ def ours(args):
         "ntt_fwd_poly_prime_per_s": NPOLY * L / fwd_s,
         "ntt_fwd_hbm_frac": NTT_BYTES_PER_FWD / fwd_s / 1e9 / hbm,
         "keyswitch_ops_per_s": PAIRS / (kern[5] * 1e-3) * ws,
+        # fully fused minimum of the step's 4 key switches: 4 inputs [24][n] + the shared keys
+        # [3][2][32][n] + 4 outputs [2][32][n], 8 B each, in the measured time, against the HBM peak
+        "keyswitch_x4_hbm_bound_frac": (KS_MIN_BYTES_X4 / (kern[5] * 1e-3) / 1e9) / hbm,
         "roofline": {"bound": "alu", "achieved": achieved_bfly / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
                      "unit": "Gbutterfly/s", "frac": achieved_bfly / ALU_PEAK_BFLY, "traffic": ntt_fwd_traffic(),
                      "traffic_unit": "bytes/launch", "algorithmic_bytes": NTT_BYTES_PER_FWD,
@@ -537,6 +541,9 @@ class RowBench:
 
     def step(self):
         raise NotImplementedError
+
+    def before_step(self):
+        """Untimed work between timed steps (an L2 flush for inputs smaller than L2)."""
 
     def probe(self):
         """(callable launching the dominant kernel once, roofline dict sans achieved/frac)."""
@@ -757,6 +764,7 @@ class ModraiseRow(RowBench):
 
 class ChainRow(RowBench):
     name = "chain2100"
+    CL = CHAIN_L
     metric = "NTT (poly x prime)/s on the 2100-prime chain, n=2^11"
     unit = "NTT (poly x prime)/s"
     workload = ("n=2^11, 2100-prime boot chain: fwd NTT of 16 polys (4 ciphertext pairs) -> tensor -> inv NTT of "
@@ -767,13 +775,13 @@ class ChainRow(RowBench):
     def setup(self, dev):
         import torch
         from ntt_arithmetic_gb300 import api, inputs
-        self.chain = api.find_primes(CHAIN_LOG_N, CHAIN_L)
+        self.chain = api.find_primes(CHAIN_LOG_N, self.CL)
         n = 1 << CHAIN_LOG_N
         self.t = api.NttTables(CHAIN_LOG_N, self.chain, dev)
-        host = inputs.uniform_residues((2, PAIRS, 2, CHAIN_L, n), self.chain, 61, buffer=0)
+        host = inputs.uniform_residues((2, PAIRS, 2, self.CL, n), self.chain, 61, buffer=0)
         self.x_pin = torch.from_numpy(host).pin_memory()
         self.X = self.x_pin.to(dev)
-        self.D = torch.empty((PAIRS, 3, CHAIN_L, n), dtype=torch.uint64, device=dev)
+        self.D = torch.empty((PAIRS, 3, self.CL, n), dtype=torch.uint64, device=dev)
         self.o_pin = torch.empty(self.D.shape, dtype=torch.uint64).pin_memory()
 
     def step(self):
@@ -785,12 +793,12 @@ class ChainRow(RowBench):
     def probe(self):
         from ntt_arithmetic_gb300 import api
         n = 1 << CHAIN_LOG_N
-        bfly = 16 * CHAIN_L * (n // 2) * CHAIN_LOG_N
+        bfly = 16 * self.CL * (n // 2) * CHAIN_LOG_N
         fn = lambda: api.ntt_fwd(self.X, self.t)
         return fn, {"bound": "alu", "work": bfly, "peak": ALU_PEAK_BFLY / 1e9, "unit": "Gbutterfly/s",
-                    "kernel": "k_ntt_fwd<11,0,7,4> (16 polys x 2100 primes)",
-                    "work_note": "16 x 2100 transforms x 1024 x 11 butterflies",
-                    "algorithmic_bytes": 16 * 16 * CHAIN_L * n}
+                    "kernel": f"k_ntt_fwd<11,0,7,4,4> (16 polys x {self.CL} primes)",
+                    "work_note": f"16 x {self.CL} transforms x 1024 x 11 butterflies",
+                    "algorithmic_bytes": 16 * 16 * self.CL * n}
 
     def e2e_step(self):
         self.X.copy_(self.x_pin, non_blocking=True)
@@ -798,15 +806,14 @@ class ChainRow(RowBench):
         self.o_pin.copy_(self.D, non_blocking=True)
         return self.x_pin.numel() * 8, self.o_pin.numel() * 8
 
-    SAMPLE_LIMBS = CHAIN_L
 
     def oracle_setup(self):
         import oracle
         from ntt_arithmetic_gb300 import inputs
-        chain = [int(v) for v in oracle.primes(2 << CHAIN_LOG_N, CHAIN_L)]
-        self.o_qs = chain[:self.SAMPLE_LIMBS]
+        chain = [int(v) for v in oracle.primes(2 << CHAIN_LOG_N, self.CL)]
+        self.o_qs = chain[:self.CL]
         self.o_ps = oracle.psis(self.o_qs, 1 << CHAIN_LOG_N)
-        self.o_x = inputs.uniform_residues((2, 1, 2, self.SAMPLE_LIMBS, 1 << CHAIN_LOG_N), self.o_qs, 61, buffer=7)
+        self.o_x = inputs.uniform_residues((2, 1, 2, self.CL, 1 << CHAIN_LOG_N), self.o_qs, 61, buffer=7)
 
     def oracle_sample(self):
         import oracle
@@ -815,11 +822,31 @@ class ChainRow(RowBench):
         X = oracle.ntt_batch(self.o_x, self.o_qs, self.o_ps, threads=threads)
         D = oracle.tensor_batch(X[0], X[1], self.o_qs)
         oracle.ntt_batch(D, self.o_qs, self.o_ps, inverse=True, threads=threads)
-        return (time.perf_counter() - t0, 7 * self.SAMPLE_LIMBS,
-                f"1 of the 4 ciphertext pairs on all {self.SAMPLE_LIMBS} primes, {threads} threads")
+        return (time.perf_counter() - t0, 7 * self.CL,
+                f"1 of the 4 ciphertext pairs on all {self.CL} primes, {threads} threads")
 
 
-ROWS = {r.name: r for r in (ModdownRow, HoistedRow, ModraiseRow, ChainRow)}
+class LayerRow(ChainRow):
+    name = "layer112"
+    CL = 112
+    metric = "NTT (poly x prime)/s on the 112-prime layer chain, n=2^11"
+    workload = ("n=2^11, 112-prime layer chain (4 token positions x 2 components = 4 ciphertext pairs, 3.5 MiB per "
+                "ciphertext): fwd NTT of 16 polys -> tensor -> inv NTT of the 12 product polys")
+    units_per_step = 28 * 112
+    traffic_rows = 16 * 112
+    l2 = ("inputs 29 MB (< L2): a 256 MB write flushes L2 before every step, outside the timed region (each step "
+          "is bracketed by its own events and the step times are summed)")
+
+    def setup(self, dev):
+        import torch
+        super().setup(dev)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def before_step(self):
+        self.flush.zero_()
+
+
+ROWS = {r.name: r for r in (ModdownRow, HoistedRow, ModraiseRow, ChainRow, LayerRow)}
 
 
 def row_bench(args):
@@ -869,19 +896,21 @@ def row_bench(args):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
+        row.before_step()
         row.step()
     barrier()
     launches0 = api.launch_count()
-    e0, e1 = _events(2)
+    evs = _events(2 * args.steps)
     with ClockSampler(local) as clk:
         barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            row.before_step()
+            evs[2 * i].record(stream)
             row.step()
-        e1.record(stream)
+            evs[2 * i + 1].record(stream)
         barrier()
     launches = api.launch_count() - launches0
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    ms = max_over_ranks(sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)) / args.steps, dev)
     fn, roof = row.probe()
     kms = _time_calls(fn, max(3, args.steps))
     achieved = roof.pop("work") / (kms * 1e-3) / 1e9
