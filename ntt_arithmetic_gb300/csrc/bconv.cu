@@ -8,8 +8,9 @@
 // Exact: Garner's mixed-radix digits v_a of X in [0, Q), Q = q_0 ... q_{S-1},
 // then X mod p = sum_a v_a (q_0 ... q_{a-1}) mod p.  Approximate: the CRT sum
 // sum_a [x_a (Q / q_a)^-1]_{q_a} (Q / q_a) = X + e Q with 0 <= e < S, reduced
-// modulo p without the correction.  Every product is by a precomputed constant
-// (lazy Shoup); each target's sum stays below 2^56 and is reduced once.
+// modulo p without the correction.  Garner's recursion uses lazy Shoup
+// products; each target's sum is an exact multiply-accumulate of 25-bit
+// halves (mac25) with one Barrett reduction.
 //
 // Layout: in [batch][S][n], out [batch][T][n].  One thread per pair of
 // coefficients computes their digits once and then a contiguous chunk of
@@ -82,20 +83,35 @@ k_bconv(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n, 
         bconv_digits<MAXS, APPROX>(v0, S, src, garner);
         bconv_digits<MAXS, APPROX>(v1, S, src, garner);
         uint64_t *o = out + b * T * n + i;
+        Split25 s0[MAXS], s1[MAXS];
+#pragma unroll
+        for (int a = 0; a < MAXS; a++) {
+            s0[a] = split25(v0[a]);
+            s1[a] = split25(v1[a]);
+        }
         for (int t = t0; t < t1; t++) {
-            const ulonglong2 pc = __ldg(dst + t);   // (p, floor(2^58 / p))
+            const ulonglong2 pc = __ldg(dst + 2 * t);       // (p, floor(2^58 / p))
+            if (!APPROX && S == 1) {   // one source prime (modraise from one limb): X = x_0 < 2^50
+                __stcs(reinterpret_cast<ulonglong2 *>(o + (long)t * n),
+                       make_ulonglong2(reduce_small(v0[0], pc.x, (uint32_t)pc.y), reduce_small(v1[0], pc.x, (uint32_t)pc.y)));
+                continue;
+            }
+            const uint64_t mu12 = __ldg(reinterpret_cast<const uint64_t *>(dst + 2 * t + 1));
             const ulonglong2 *wt = weights + (long)t * S;
-            uint64_t acc0 = APPROX ? 0 : v0[0], acc1 = APPROX ? 0 : v1[0];   // exact: the weight of v_0 is 1
+            Mac25 acc0, acc1;
 #pragma unroll
             for (int a = APPROX ? 0 : 1; a < MAXS; a++) {
                 if (a < S) {
-                    const ulonglong2 m = __ldg(wt + a);
-                    acc0 += shoup_lazy(v0[a], m.x, m.y, pc.x);   // < 4p each: sum < 2^56
-                    acc1 += shoup_lazy(v1[a], m.x, m.y, pc.x);
+                    const ulonglong2 w = __ldg(wt + a);
+                    const Split25 m = split25_entry(w.x, w.y);
+                    mac25(acc0, s0[a], m);
+                    mac25(acc1, s1[a], m);
                 }
             }
+            // exact: the weight of v_0 is 1
             __stcs(reinterpret_cast<ulonglong2 *>(o + (long)t * n),
-                   make_ulonglong2(reduce_small(acc0, pc.x, (uint32_t)pc.y), reduce_small(acc1, pc.x, (uint32_t)pc.y)));
+                   make_ulonglong2(mac25_reduce(acc0, APPROX ? 0 : v0[0], pc.x, mu12, (uint32_t)pc.y),
+                                   mac25_reduce(acc1, APPROX ? 0 : v1[0], pc.x, mu12, (uint32_t)pc.y)));
         }
     }
 }

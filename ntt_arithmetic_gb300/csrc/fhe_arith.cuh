@@ -136,6 +136,61 @@ FHE_HD void mac128(uint64_t &hi, uint64_t &lo, uint64_t a, uint64_t b) {
     hi += ph + (lo < pl ? 1 : 0);
 }
 
+// Exact sums of products sum_a v_a m_a for v_a, m_a < 2^50 and at most 16
+// terms, reduced once: the sums of basis extensions (ModUp, ModDown, basis
+// conversion), where every product is by a different constant (stored
+// pre-split in the tables).  Each factor
+// is split into 25-bit halves, v = v1 2^25 + v0, and the three column sums
+// s0 = sum v0 m0, s1 = sum v1 m1, s01 = sum (v0 + v1)(m0 + m1) are kept in
+// 64-bit words (Karatsuba: the middle column is s01 - s0 - s1).  Every
+// product is one 32x32 -> 64 multiply-add and no high half is needed, against
+// two high and three wide products for a Shoup product.  Bounds: s0, s1 <
+// 16 2^50 = 2^54, s01 < 16 2^52 = 2^56.
+struct Split25 {
+    uint32_t lo, hi, sum;   // v0, v1, v0 + v1
+};
+FHE_HD Split25 split25(uint64_t v) {
+    const uint32_t lo = (uint32_t)v & 0x1FFFFFFu, hi = (uint32_t)(v >> 25);
+    return {lo, hi, lo + hi};
+}
+// A constant factor m < 2^50 stored split, as the two words of a table entry:
+// word 0 = m0 | m1 << 32, word 1 = m0 + m1.
+FHE_HD void split25_store(uint64_t m, uint64_t *entry) {
+    const Split25 s = split25(m);
+    entry[0] = (uint64_t)s.lo | (uint64_t)s.hi << 32;
+    entry[1] = s.sum;
+}
+FHE_HD Split25 split25_entry(uint64_t w0, uint64_t w1) { return {(uint32_t)w0, (uint32_t)(w0 >> 32), (uint32_t)w1}; }
+struct Mac25 {
+    uint64_t s0 = 0, s1 = 0, s01 = 0;
+};
+FHE_HD void mac25(Mac25 &acc, const Split25 &v, const Split25 &m) {
+#if defined(__CUDA_ARCH__)
+    asm("mad.wide.u32 %0, %3, %4, %0;\n\t"
+        "mad.wide.u32 %1, %5, %6, %1;\n\t"
+        "mad.wide.u32 %2, %7, %8, %2;"
+        : "+l"(acc.s0), "+l"(acc.s1), "+l"(acc.s01)
+        : "r"(v.lo), "r"(m.lo), "r"(v.hi), "r"(m.hi), "r"(v.sum), "r"(m.sum));
+#else
+    acc.s0 += (uint64_t)v.lo * m.lo;
+    acc.s1 += (uint64_t)v.hi * m.hi;
+    acc.s01 += (uint64_t)v.sum * m.sum;
+#endif
+}
+// (sum + extra) mod q with X = s1 2^50 + (s01 - s0 - s1) 2^25 + s0 + extra
+// < 2^105 (extra < 2^60), through barrett_reduce128.
+FHE_HD uint64_t mac25_reduce(const Mac25 &acc, uint64_t extra, uint64_t q, uint64_t mu12, uint32_t c58) {
+    const uint64_t mid = acc.s01 - acc.s0 - acc.s1;
+    uint64_t lo = acc.s0 + extra, hi = 0;
+    uint64_t t = mid << 25;
+    lo += t;
+    hi += (mid >> 39) + (lo < t ? 1 : 0);
+    t = acc.s1 << 50;
+    lo += t;
+    hi += (acc.s1 >> 14) + (lo < t ? 1 : 0);
+    return barrett_reduce128(hi, lo, q, mu12, c58);
+}
+
 // Forward (Cooley-Tukey) butterfly with the psi-merged twiddle w (Roy et
 // al./Poppelmann et al. merged negacyclic NTT) and Harvey's lazy additive
 // bound: if X, Y < B then X', Y' < B + 4q.  No comparison at all.

@@ -26,9 +26,9 @@ struct ModupLayout {
     int alpha;
     size_t off_digits;   // [dnum] ModupDigit
     size_t off_garner;   // [dnum][alpha][alpha] pairs: d_b^-1 mod d_a (b < a)       (exact)
-    size_t off_mr;       // [dnum][L+K][alpha] pairs: prod_{b<a} d_b mod qp_l         (exact)
+    size_t off_mr;       // [dnum][L+K][alpha] split factors: prod_{b<a} d_b mod qp_l (exact)
     size_t off_qinv;     // [dnum][alpha] pairs: (D_j / d_a)^-1 mod d_a                (approximate)
-    size_t off_qhat;     // [dnum][L+K][alpha] pairs: (D_j / d_a) mod qp_l             (approximate)
+    size_t off_qhat;     // [dnum][L+K][alpha] split factors: (D_j / d_a) mod qp_l     (approximate)
     size_t bytes;
 };
 ModupLayout modup_layout(int L, int K, int dnum);
@@ -37,7 +37,7 @@ bool modup_shape_ok(int L, int K, int dnum);
 // ModDown constants for Q = (q_0..q_{L-1}), P = (p_0..p_{K-1}).
 struct ModdownLayout {
     size_t off_garner;   // [K][K] pairs: p_b^-1 mod p_a (b < a)
-    size_t off_mr;       // [L][K] pairs: prod_{b<a} p_b mod q_l
+    size_t off_mr;       // [L][K] split factors: prod_{b<a} p_b mod q_l
     size_t off_hp;       // [K] words: (P-1)/2 mod p_k
     size_t off_hq;       // [L] words: (P-1)/2 mod q_l
     size_t off_pinv;     // [L] pairs: P^-1 mod q_l
@@ -49,14 +49,16 @@ ModdownLayout moddown_layout(int L, int K);
 constexpr int kMaxBconvSrc = 16;
 struct BconvLayout {
     size_t off_src;      // [S] words: source primes
-    size_t off_dst;      // [T][2] words: target prime, floor(2^58 / prime)
+    size_t off_dst;      // [T][4] words: target prime, floor(2^58 / prime), floor(2^100 / prime) << 12, 0
     size_t off_garner;   // [S][S] pairs: q_b^-1 mod q_a (b < a)                      (exact)
-    size_t off_mr;       // [T][S] pairs: prod_{b<a} q_b mod p_t                      (exact)
+    size_t off_mr;       // [T][S] split factors: prod_{b<a} q_b mod p_t              (exact)
     size_t off_qinv;     // [S] pairs: (Q / q_a)^-1 mod q_a                           (approximate)
-    size_t off_qhat;     // [T][S] pairs: (Q / q_a) mod p_t                           (approximate)
+    size_t off_qhat;     // [T][S] split factors: (Q / q_a) mod p_t                   (approximate)
     size_t bytes;
 };
 BconvLayout bconv_layout(int S, int T);
+
+// "split factors" are 16-byte entries written by split25_store (fhe_arith.cuh).
 
 // Galois elements of one hoisted key switch.
 constexpr int kMaxRotations = 64;

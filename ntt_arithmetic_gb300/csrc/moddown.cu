@@ -9,7 +9,8 @@
 // With c = (X + h) mod P, floor((X + h) / P) = (X + h - c) / P, so per
 // coefficient:
 //   1. the P residues of X + h are converted exactly to c mod q_l by Garner's
-//      mixed radix (the same construction as the key-switch ModUp) and
+//      mixed radix (the same construction as the key-switch ModUp; the radix
+//      sum is an exact multiply-accumulate reduced once) and
 //      d_l = c - h mod q_l is written (coefficient domain);
 //   2. out_l = (x_l - d_l) P^-1 mod q_l.
 // In the coefficient domain both steps run in one pass (one read of every
@@ -80,18 +81,21 @@ k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long 
                 v[a] = reduce4(u, p);
             }
         }
+        Split25 vs[MAXK];
+#pragma unroll
+        for (int a = 0; a < MAXK; a++) vs[a] = split25(v[a]);
         for (int l = 0; l < L; l++) {
             const uint64_t *kc = consts_q + (long)l * K_COUNT;
             const uint64_t q = __ldg(kc + K_Q);
-            uint64_t acc = v[0];
+            Mac25 acc;   // sum_{a >= 1} v_a (p_0 ... p_{a-1}); the weight of v_0 is 1
 #pragma unroll
             for (int a = 1; a < MAXK; a++) {
                 if (a < K) {
                     const ulonglong2 m = __ldg(mr + l * K + a);
-                    acc += shoup_lazy(v[a], m.x, m.y, q);   // < 2^50 + 15 * 4q < 2^56
+                    mac25(acc, vs[a], split25_entry(m.x, m.y));
                 }
             }
-            uint64_t c = reduce_small(acc, q, (uint32_t)__ldg(kc + K_C58));
+            uint64_t c = mac25_reduce(acc, v[0], q, __ldg(kc + K_MU12), (uint32_t)__ldg(kc + K_C58));
             if (nearest) {
                 const uint64_t h = __ldg(hq + l);
                 c = c >= h ? c - h : c + q - h;

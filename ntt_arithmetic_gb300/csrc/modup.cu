@@ -9,13 +9,14 @@
 // extension" of FHElium's CUDA layer ("Eager, Compile, and native
 // execution", section "CUDA execution") and the "Garner extension" of the
 // kestrel-llm chain (overview, section 4.2).  All constants are fixed per
-// basis, so every product is a lazy Shoup product; the extension sums stay
-// below 2^56 and are reduced once.
+// basis: Garner's recursion uses lazy Shoup products.
 //
 // The approximate variant replaces Garner's recursion by the CRT sum
 //   X + e D = sum_a [x_a (D / d_a)^-1]_{d_a} (D / d_a),   0 <= e < alpha,
 // reduced modulo each target prime without correcting e D: alpha products
 // for the brackets, then alpha multiply-accumulates per target.
+// The extension sums are exact multiply-accumulates of 25-bit halves with one
+// Barrett reduction per target (mac25 in fhe_arith.cuh).
 #include <cuda_runtime.h>
 
 #include "fhe_arith.cuh"
@@ -75,19 +76,23 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
 #pragma unroll
         for (int a = 0; a < MAXA; a++)
             if (a < cnt) __stcs(dst + (long)(lo + a) * n, x[a]);   // limbs of the digit are copies
+        Split25 vs[MAXA];
+#pragma unroll
+        for (int a = 0; a < MAXA; a++) vs[a] = split25(v[a]);
         for (int l = 0; l < LK; l++) {
             if (l >= lo && l < lo + cnt) continue;
             const uint64_t *kc = consts + (long)l * K_COUNT;
-            const uint64_t p = __ldg(kc + K_Q);
-            uint64_t acc = APPROX ? 0 : v[0];   // exact: the weight of v_0 is 1
+            Mac25 acc;
 #pragma unroll
             for (int a = APPROX ? 0 : 1; a < MAXA; a++) {
                 if (a < cnt) {
                     const ulonglong2 m = __ldg(mj + l * alpha + a);
-                    acc += shoup_lazy(v[a], m.x, m.y, p);   // < 4p each: sum < 2^56
+                    mac25(acc, vs[a], split25_entry(m.x, m.y));
                 }
             }
-            __stcs(dst + (long)l * n, reduce_small(acc, p, (uint32_t)__ldg(kc + K_C58)));
+            // exact: the weight of v_0 is 1
+            __stcs(dst + (long)l * n, mac25_reduce(acc, APPROX ? 0 : v[0], __ldg(kc + K_Q), __ldg(kc + K_MU12),
+                                                   (uint32_t)__ldg(kc + K_C58)));
         }
     }
 }

@@ -118,7 +118,7 @@ BconvLayout bconv_layout(int S, int T) {
     BconvLayout s;
     s.off_src = 0;
     s.off_dst = align256((size_t)S * 8);
-    s.off_garner = align256(s.off_dst + (size_t)T * 16);
+    s.off_garner = align256(s.off_dst + (size_t)T * 32);
     s.off_mr = align256(s.off_garner + (size_t)S * S * 16);
     s.off_qinv = align256(s.off_mr + (size_t)T * S * 16);
     s.off_qhat = align256(s.off_qinv + (size_t)S * 16);
@@ -312,8 +312,7 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
             const uint64_t p = qp[l];
             uint64_t prod = 1 % p;
             for (int i = 0; i < hi - lo; i++) {
-                mj[(l * alpha + i) * 2] = prod;
-                mj[(l * alpha + i) * 2 + 1] = shoup(prod, p);
+                split25_store(prod, mj + (l * alpha + i) * 2);
                 prod = mul_mod(prod, qp[lo + i] % p, p);
             }
         }
@@ -333,8 +332,7 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
                 uint64_t hp = 1 % p;
                 for (int b = 0; b < hi - lo; b++)
                     if (b != a) hp = mul_mod(hp, qp[lo + b] % p, p);
-                qh[(l * alpha + a) * 2] = hp;
-                qh[(l * alpha + a) * 2 + 1] = shoup(hp, p);
+                split25_store(hp, qh + (l * alpha + a) * 2);
             }
         }
     }
@@ -387,18 +385,17 @@ extern "C" int fhe_bconv_tables_build_host(int S, const uint64_t *src, int T, co
     }
     for (int t = 0; t < T; t++) {
         const uint64_t p = dst[t];
-        dp[t * 2] = p;
-        dp[t * 2 + 1] = (1ull << 58) / p;
+        dp[t * 4] = p;
+        dp[t * 4 + 1] = (1ull << 58) / p;
+        dp[t * 4 + 2] = (uint64_t)(((u128)1 << 100) / p) << 12;
         uint64_t prod = 1 % p;
         for (int a = 0; a < S; a++) {
-            mr[((size_t)t * S + a) * 2] = prod;
-            mr[((size_t)t * S + a) * 2 + 1] = shoup(prod, p);
+            split25_store(prod, mr + ((size_t)t * S + a) * 2);
             prod = mul_mod(prod, src[a] % p, p);
             uint64_t hp = 1 % p;
             for (int b = 0; b < S; b++)
                 if (b != a) hp = mul_mod(hp, src[b] % p, p);
-            qh[((size_t)t * S + a) * 2] = hp;
-            qh[((size_t)t * S + a) * 2 + 1] = shoup(hp, p);
+            split25_store(hp, qh + ((size_t)t * S + a) * 2);
         }
     }
     return FHE_OK;
@@ -443,8 +440,7 @@ extern "C" int fhe_moddown_tables_build_host(int L, int K, const uint64_t *qp, v
         const uint64_t q = qp[l];
         uint64_t prod = 1 % q;
         for (int a = 0; a < K; a++) {
-            mr[(l * K + a) * 2] = prod;
-            mr[(l * K + a) * 2 + 1] = shoup(prod, q);
+            split25_store(prod, mr + (l * K + a) * 2);
             prod = mul_mod(prod, P[a] % q, q);
         }
         // prod = P mod q
@@ -489,6 +485,18 @@ int selftest_arith(uint64_t seed, int iters) {
             for (int k = 0; k < 1 + it % 24; k++) mac128(h, l, next() % q, next() % q);
             const u128 T = ((u128)h << 64) | l;
             if (barrett_reduce128(h, l, q, mu12, c58) != (uint64_t)(T % q)) return 13;
+            // sums of up to 16 products of reduced values, with an extra term
+            Mac25 acc;
+            u128 ref_sum = 0;
+            const int terms = 1 + it % 16;
+            for (int k = 0; k < terms; k++) {
+                uint64_t v = next() % q, m = next() % q;
+                if (it % 5 == 0) { v = q - 1; m = q - 1; }
+                mac25(acc, split25(v), split25(m));
+                ref_sum += (u128)v * m;
+            }
+            const uint64_t extra = it % 3 == 0 ? next() % q : 0;
+            if (mac25_reduce(acc, extra, q, mu12, c58) != (uint64_t)((ref_sum + extra) % q)) return 14;
         }
     }
     return 0;
