@@ -59,7 +59,7 @@ __device__ __forceinline__ void bconv_digits(uint64_t (&v)[MAXS], int S, const u
 
 // One thread per pair of adjacent coefficients (16-byte loads and stores).
 template <int MAXS, bool APPROX>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 k_bconv(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n, int S, int T, int tchunk,
         const uint64_t *__restrict__ src, const ulonglong2 *__restrict__ dst, const ulonglong2 *__restrict__ garner,
         const ulonglong2 *__restrict__ weights) {
