@@ -46,7 +46,9 @@ k_copy_limbs(uint64_t *__restrict__ ws, const uint64_t *__restrict__ in, long pa
 // src[b * src_item + k * n + i] (k < K).  FUSED (coefficient domain): instead
 // of d, write out[b][l][i] = (x_l - d_l) P^-1 mod q_l directly, reading x_l
 // from src - L n (the Q limbs of the same batch item).
-template <int MAXK, bool FUSED>
+// STAGED (L <= kMaxBasis): the radix weights and the Q primes' reduction
+// constants are staged in shared memory and read as broadcasts.
+template <int MAXK, bool FUSED, bool STAGED>
 __global__ void __launch_bounds__(kThreads)
 k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long src_item, int log_n, int L, int K,
                int batch, int nearest, const ulonglong2 *__restrict__ garner, const ulonglong2 *__restrict__ mr,
@@ -55,6 +57,21 @@ k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long 
     const long n = 1L << log_n;
     const long total = n * batch;
     const long stride = (long)gridDim.x * blockDim.x;
+    __shared__ ulonglong2 s_mr[STAGED ? kMaxBasis * MAXK : 1];
+    __shared__ ulonglong2 s_qm[STAGED ? kMaxBasis : 1];     // (q, floor(2^100 / q) << 12)
+    __shared__ uint32_t s_c58[STAGED ? kMaxBasis : 1];
+    if constexpr (STAGED) {
+        for (int e = threadIdx.x; e < L * MAXK; e += blockDim.x) {
+            const int l = e / MAXK, a = e - l * MAXK;
+            s_mr[e] = a < K ? __ldg(mr + l * K + a) : make_ulonglong2(0, 0);
+        }
+        for (int l = threadIdx.x; l < L; l += blockDim.x) {
+            const uint64_t *kc = consts_q + (long)l * K_COUNT;
+            s_qm[l] = make_ulonglong2(__ldg(kc + K_Q), __ldg(kc + K_MU12));
+            s_c58[l] = (uint32_t)__ldg(kc + K_C58);
+        }
+        __syncthreads();
+    }
     for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
         const long b = e >> log_n, i = e & (n - 1);
         uint64_t v[MAXK];
@@ -86,16 +103,17 @@ k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long 
         for (int a = 0; a < MAXK; a++) vs[a] = split25(v[a]);
         for (int l = 0; l < L; l++) {
             const uint64_t *kc = consts_q + (long)l * K_COUNT;
-            const uint64_t q = __ldg(kc + K_Q);
+            const ulonglong2 qm = STAGED ? s_qm[l] : make_ulonglong2(__ldg(kc + K_Q), __ldg(kc + K_MU12));
+            const uint64_t q = qm.x;
             Mac25 acc;   // sum_{a >= 1} v_a (p_0 ... p_{a-1}); the weight of v_0 is 1
 #pragma unroll
             for (int a = 1; a < MAXK; a++) {
                 if (a < K) {
-                    const ulonglong2 m = __ldg(mr + l * K + a);
+                    const ulonglong2 m = STAGED ? s_mr[l * MAXK + a] : __ldg(mr + l * K + a);
                     mac25(acc, vs[a], split25_entry(m.x, m.y));
                 }
             }
-            uint64_t c = mac25_reduce(acc, v[0], q, __ldg(kc + K_MU12), (uint32_t)__ldg(kc + K_C58));
+            uint64_t c = mac25_reduce(acc, v[0], q, qm.y, STAGED ? s_c58[l] : (uint32_t)__ldg(kc + K_C58));
             if (nearest) {
                 const uint64_t h = __ldg(hq + l);
                 c = c >= h ? c - h : c + q - h;
@@ -137,7 +155,9 @@ void launch_conv(uint64_t *d, const uint64_t *src, long src_item, int log_n, int
                  bool fused, const ModdownLayout &lay, const char *md, const fhe_ntt_tables *t_qp, cudaStream_t st) {
     const long total = (long)batch << log_n;
     const unsigned grid = stream_grid(total, kThreads, 8);
-    auto kern = fused ? k_moddown_conv<MAXK, true> : k_moddown_conv<MAXK, false>;
+    const bool staged = L <= kMaxBasis;
+    auto kern = fused ? (staged ? k_moddown_conv<MAXK, true, true> : k_moddown_conv<MAXK, true, false>)
+                      : (staged ? k_moddown_conv<MAXK, false, true> : k_moddown_conv<MAXK, false, false>);
     kern<<<grid, kThreads, 0, st>>>(d, src, src_item, log_n, L, K, batch, nearest ? 1 : 0,
                                     (const ulonglong2 *)(md + lay.off_garner), (const ulonglong2 *)(md + lay.off_mr),
                                     (const uint64_t *)(md + lay.off_hp), (const uint64_t *)(md + lay.off_hq),

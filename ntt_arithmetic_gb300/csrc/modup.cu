@@ -16,7 +16,9 @@
 // reduced modulo each target prime without correcting e D: alpha products
 // for the brackets, then alpha multiply-accumulates per target.
 // The extension sums are exact multiply-accumulates of 25-bit halves with one
-// Barrett reduction per target (mac25 in fhe_arith.cuh).
+// Barrett reduction per target (mac25 in fhe_arith.cuh).  Each CTA stages its
+// digit's extension weights and the targets' reduction constants in shared
+// memory, so the inner loop reads them as broadcasts.
 #include <cuda_runtime.h>
 
 #include "fhe_arith.cuh"
@@ -39,7 +41,23 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
     const int j = blockIdx.y, bi = blockIdx.z;
     const int lo = dg[j].lo, cnt = dg[j].count;
     const ulonglong2 *gj = garner + (long)j * alpha * (APPROX ? 1 : alpha);
-    const ulonglong2 *mj = mr + (long)j * LK * alpha;
+    // this digit's extension weights and the targets' constants, staged in shared memory
+    __shared__ ulonglong2 s_mr[kMaxBasis * MAXA];
+    __shared__ ulonglong2 s_qm[kMaxBasis];     // (q, floor(2^100 / q) << 12)
+    __shared__ uint32_t s_c58[kMaxBasis];
+    {
+        const ulonglong2 *src_mr = mr + (long)j * LK * alpha;
+        for (int e = threadIdx.x; e < LK * MAXA; e += blockDim.x) {
+            const int l = e / MAXA, a = e - l * MAXA;
+            s_mr[e] = a < alpha ? __ldg(src_mr + l * alpha + a) : make_ulonglong2(0, 0);
+        }
+        for (int l = threadIdx.x; l < LK; l += blockDim.x) {
+            const uint64_t *kc = consts + (long)l * K_COUNT;
+            s_qm[l] = make_ulonglong2(__ldg(kc + K_Q), __ldg(kc + K_MU12));
+            s_c58[l] = (uint32_t)__ldg(kc + K_C58);
+        }
+        __syncthreads();
+    }
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
         uint64_t x[MAXA], v[MAXA];
         const uint64_t *src = in + (long)bi * in_stride + (long)lo * n + i;
@@ -81,18 +99,17 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
         for (int a = 0; a < MAXA; a++) vs[a] = split25(v[a]);
         for (int l = 0; l < LK; l++) {
             if (l >= lo && l < lo + cnt) continue;
-            const uint64_t *kc = consts + (long)l * K_COUNT;
             Mac25 acc;
 #pragma unroll
             for (int a = APPROX ? 0 : 1; a < MAXA; a++) {
                 if (a < cnt) {
-                    const ulonglong2 m = __ldg(mj + l * alpha + a);
+                    const ulonglong2 m = s_mr[l * MAXA + a];
                     mac25(acc, vs[a], split25_entry(m.x, m.y));
                 }
             }
+            const ulonglong2 qm = s_qm[l];
             // exact: the weight of v_0 is 1
-            __stcs(dst + (long)l * n, mac25_reduce(acc, APPROX ? 0 : v[0], __ldg(kc + K_Q), __ldg(kc + K_MU12),
-                                                   (uint32_t)__ldg(kc + K_C58)));
+            __stcs(dst + (long)l * n, mac25_reduce(acc, APPROX ? 0 : v[0], qm.x, qm.y, s_c58[l]));
         }
     }
 }
