@@ -70,6 +70,7 @@ uint64_t fhe_launch_count(void);
  * per prime (seeded by `seed`).  Needs no GPU.  FHE_OK when all agree. */
 int fhe_selftest_host(uint64_t seed, int iters);
 
+
 /* ---- primes and roots -------------------------------------------------- */
 
 /* The `count` largest primes q < below (below = 0 means 2^bits) with
@@ -140,6 +141,21 @@ int fhe_ntt_fwd(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables
 /* In-place exact inverse of fhe_ntt_fwd, including the 1/n factor:
  * bit-reversed evaluations in, natural-order coefficients out. */
 int fhe_ntt_inv(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream);
+
+/* Measurement aid with no counterpart on the pages: the throughput ceiling of
+ * the NTT butterfly on this GPU.  Each of the `ctas` CTAs of 256 threads keeps
+ * 32 residues per thread in registers and runs `iters` rounds of five radix-2
+ * stages (80 lazy Cooley-Tukey butterflies per thread per round, the
+ * arithmetic of fhe_ntt_fwd) with twiddles read coalesced from prime 0 of
+ * `t`, then writes one word per thread to out[ctas * 256] (device memory,
+ * caller-owned, 16-byte aligned): the XOR of its 32 residues reduced into
+ * [0, q_0), a checksum of the butterfly network (residue i of global thread g
+ * starts at (977 g + 131 i) mod q_0; round r uses, for stage s and twiddle j,
+ * entry 32 (32 (r mod 2) + 2^s + j) + (g mod 32) of prime 0's forward table).
+ * Butterflies per call: ctas * 256 * iters * 80.  Needs t->log_n >= 11;
+ * 1 <= ctas <= 1048576, 1 <= iters <= 128 (the lazy bound of the residues),
+ * else FHE_EINVAL.  One launch on `stream`, no host sync. */
+int fhe_butterfly_probe(uint64_t *out, int ctas, int iters, const fhe_ntt_tables *t, void *stream);
 
 /* ---- NTT-domain kernels ------------------------------------------------ */
 

@@ -92,6 +92,7 @@ SIGNATURES = {
     "fhe_keyswitch_ip_noalloc": (_int, [_vp, _vp, _size, _vp, _int, _int, _int, _int, _int,
                                         ctypes.POINTER(NttTables), _vp, _vp]),
     "fhe_keyswitch_noalloc_max_bytes": (_size, []),
+    "fhe_butterfly_probe": (_int, [_vp, _int, _int, ctypes.POINTER(NttTables), _vp]),
 }
 
 _lib = None

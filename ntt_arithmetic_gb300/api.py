@@ -65,6 +65,18 @@ def launch_count() -> int:
     return int(N.lib().fhe_launch_count())
 
 
+def butterfly_probe(out: torch.Tensor, iters: int, tables: "NttTables", stream=None) -> int:
+    """Launch the butterfly throughput probe (fhe_butterfly_probe) with one
+    CTA of 256 threads per 256 words of `out`; returns the number of
+    butterflies the launch performs."""
+    _residues(out, "out")
+    if out.numel() % 256:
+        raise ValueError("out must hold a multiple of 256 words")
+    ctas = out.numel() // 256
+    N.call("fhe_butterfly_probe", _ptr(out), ctas, int(iters), tables.ref(), _stream(out.device, stream))
+    return ctas * 256 * int(iters) * 80
+
+
 # ---------------------------------------------------------------- tables ---
 
 class NttTables:

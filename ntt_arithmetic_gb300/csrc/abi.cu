@@ -104,6 +104,17 @@ extern "C" const char *fhe_status_str(int s) {
 
 extern "C" uint64_t fhe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+extern "C" int fhe_butterfly_probe(uint64_t *out, int ctas, int iters, const fhe_ntt_tables *t, void *stream) {
+    if (!out || !aligned16(out) || ctas < 1 || ctas > (1 << 20) || iters < 1 || iters > 128) return FHE_EINVAL;
+    if (!t || t->log_n < 11) return FHE_EINVAL;
+    int s = check_tables(t, t->log_n, 1);
+    if (s) return s;
+    if ((s = select_device({out, t->blob}))) return s;
+    const Span o{out, (size_t)ctas * 256 * 8}, tb{t->blob, t->bytes};
+    if (overlap(o, tb)) return FHE_EALIAS;
+    return finish(launch_bfly_probe(out, ctas, iters, t, stream));
+}
+
 static int ntt_call(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream, bool inverse) {
     int s = check_shape(log_n, L, batch);
     if (s) return s;

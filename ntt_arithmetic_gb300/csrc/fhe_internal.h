@@ -89,6 +89,8 @@ int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int l
 int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, int batch, bool ntt_domain,
                    bool nearest, const fhe_ntt_tables *t_qp, const void *md, uint64_t *ws, void *stream);
 
+int launch_bfly_probe(uint64_t *out, int ctas, int iters, const fhe_ntt_tables *t, void *stream);
+
 // Tables view shifted to limbs [first, first + count) of t (no copy).
 fhe_ntt_tables tables_slice(const fhe_ntt_tables *t, int first, int count);
 

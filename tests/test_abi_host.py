@@ -186,3 +186,15 @@ def test_modup_table_shapes(lib):
     assert lib.fhe_modup_tables_bytes(7, 3, 3, ctypes.byref(nb)) == 0        # ragged digits 3,3,1
     assert lib.fhe_modup_tables_bytes(40, 8, 2, ctypes.byref(nb)) == N.FHE_EINVAL   # alpha = 20 > 16
     assert lib.fhe_modup_tables_bytes(4, 1, 3, ctypes.byref(nb)) == N.FHE_EINVAL    # digit 2 would be empty
+
+
+def test_butterfly_probe_validates_on_the_host(lib):
+    t = N.NttTables()
+    fake = ctypes.c_void_p(1 << 20)            # never dereferenced: validation fails first
+    assert lib.fhe_butterfly_probe(None, 1, 1, ctypes.byref(t), None) == N.FHE_EINVAL
+    assert lib.fhe_butterfly_probe(fake, 0, 1, ctypes.byref(t), None) == N.FHE_EINVAL
+    assert lib.fhe_butterfly_probe(fake, 1, 0, ctypes.byref(t), None) == N.FHE_EINVAL
+    assert lib.fhe_butterfly_probe(fake, 1, 129, ctypes.byref(t), None) == N.FHE_EINVAL
+    assert lib.fhe_butterfly_probe(fake, 1, 1, None, None) == N.FHE_EINVAL
+    t.log_n = 10                                # the probe reads 2048 table entries
+    assert lib.fhe_butterfly_probe(fake, 1, 1, ctypes.byref(t), None) == N.FHE_EINVAL
