@@ -162,3 +162,24 @@ def test_moddown_launch_count(g):
     c2 = g.api.launch_count()
     assert c1 - c0 == 1
     assert c2 - c1 == 5
+
+
+@pytest.mark.parametrize("domain", ["coeff", "ntt"])
+def test_moddown_long_chain(g, domain):
+    """More than 64 Q primes: the conversion reads its weights from global memory
+    instead of staging them in shared memory (n = 2^11, 150 + 2 primes, and a
+    rescale of a 130-prime chain)."""
+    import torch
+    log_n, n = 11, 1 << 11
+    qp = g.qp_basis(log_n, 150, 2)
+    x = inputs.uniform_residues((2, 152, n), qp, 740, buffer=1)
+    for nearest in (True, False):
+        got = _run(g, x, 150, 2, qp, domain, nearest)
+        assert np.array_equal(got, _want(x, qp, 150, 2, domain, nearest)), nearest
+    q = list(g.primes(log_n, 130))
+    t = g.tables(log_n, tuple(q))
+    rs = g.api.ModdownTables(129, 1, q)
+    x = inputs.uniform_residues((2, 130, n), q, 741, buffer=1)
+    out = torch.empty((2, 129, n), dtype=torch.uint64, device="cuda")
+    g.api.rescale(out, g.dev(x), t, rs, domain=domain, nearest=True)
+    assert np.array_equal(g.host(out), _want(x, q, 129, 1, domain, True))
