@@ -61,7 +61,7 @@ k_aut_coeff(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, long pa
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
         const long e = 2 * i;
         const long row = e >> log_n;
-        const uint64_t q = __ldg(consts + (row % L) * K_COUNT + K_Q);
+        const uint64_t q = __ldg(consts + ((uint32_t)row % (uint32_t)L) * K_COUNT + K_Q);   // rows < 2^30
         const uint64_t *src = in + (row << log_n);
         uint64_t v[2];
 #pragma unroll

@@ -22,7 +22,7 @@ k_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, long pairs, int log_n
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
         const long e = 2 * i;
-        const int l = (int)((e >> log_n) % L);
+        const int l = (int)((uint32_t)(e >> log_n) % (uint32_t)L);
         const uint64_t q = __ldg(consts + l * K_COUNT + K_Q), mu = __ldg(consts + l * K_COUNT + K_MU12);
         const ulonglong2 va = __ldcs(reinterpret_cast<const ulonglong2 *>(a + e));
         const ulonglong2 vb = __ldcs(reinterpret_cast<const ulonglong2 *>(b + e));
@@ -38,9 +38,9 @@ k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
         const long e = 2 * i;                  // flat index over [batch][L][n]
-        const long row = e >> log_n;
-        const long bi = row / L;
-        const int l = (int)(row - bi * L);
+        const uint32_t row = (uint32_t)(e >> log_n);   // rows < 2^30
+        const uint32_t bi = row / (uint32_t)L;
+        const int l = (int)(row - bi * (uint32_t)L);
         const long in_off = e + bi * plane;    // [batch][2][L][n]
         const long out_off = e + 2 * bi * plane;  // [batch][3][L][n]
         const uint64_t *kc = consts + l * K_COUNT;
