@@ -423,9 +423,13 @@ def cpu_baseline(steps: int):
     for i in range(steps):
         oracle_step(s, i, threads)
     dt = (time.perf_counter() - t0) / steps
+    t0 = time.perf_counter()
+    oracle_step(s, 0, 1)                      # the same sample on one core, once
+    dt1 = time.perf_counter() - t0
     return {"value": SAMPLE_UNITS / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"1 of the 4 ciphertext pairs of the step ({SAMPLE_UNITS} transforms + its automorph, "
-                      f"mul, tensor and 1 key switch), {steps} step(s), {dt:.2f} s/step, {threads} threads"}
+                      f"mul, tensor and 1 key switch), {steps} step(s), {dt:.2f} s/step, {threads} threads",
+            "single_thread": {"value": SAMPLE_UNITS / dt1, "unit": UNIT, "cores": 1, "s_per_step": dt1}}
 
 
 def reference(args):
