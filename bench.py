@@ -172,6 +172,88 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
+class NvmlClockPoller:
+    """SM clock, clock-event reasons and power read through NVML (read-only
+    queries, no setting is changed) every `period` seconds by a thread, for
+    exactly the span between start() and stop(): the timed region itself,
+    which is too short for nvidia-smi's 100 ms sampling.  `reader` replaces
+    NVML (tests); it returns (sm_mhz, max_sm_mhz, reason_bits, power_mw)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device=None, period: float = 0.002, reader=None):
+        import threading
+        self.period, self.samples, self._stop = period, [], threading.Event()
+        self._thread = None
+        self.reader = reader or self._nvml_reader(device)
+
+    @staticmethod
+    def _nvml_reader(device):
+        import ctypes
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                return None
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:   # NVML_CLOCK_SM
+                return None
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            return None
+
+        def read():
+            clk, rs, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+            nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+            reasons_fn(h, ctypes.byref(rs))
+            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+            return clk.value, mx.value, rs.value, mw.value
+        return read
+
+    def start(self):
+        import threading
+        if self.reader is None:
+            return self
+
+        def loop():
+            while not self._stop.is_set():
+                self.samples.append(self.reader())
+                time.sleep(self.period)
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+        return self
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self.samples.append(self.reader())   # at least one sample at the end of the region
+
+    def summary(self):
+        if not self.samples:
+            return None
+        sm = [c for c, _, _, _ in self.samples]
+        bits = 0
+        for _, _, r, _ in self.samples:
+            bits |= r
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(m for _, m, _, _ in self.samples),
+                "sm_min_mhz": min(sm), "reasons": sorted(n for b, n in self.REASONS.items() if bits & b),
+                "samples": len(self.samples), "power_w_max": max(p for _, _, _, p in self.samples) / 1000.0,
+                "source": f"NVML every {self.period * 1e3:g} ms inside the timed region"}
+
+
+def clock_record(poller, sampler):
+    """The NVML record of the timed region when NVML was readable, else nvidia-smi's."""
+    rec = poller.summary() if poller is not None else None
+    return rec if rec is not None else sampler.summary()
+
+
 def build_state(device, seed: int = 3):
     import torch
     from ntt_arithmetic_gb300 import api, inputs
@@ -320,11 +402,13 @@ def ours(args):
     launches0 = api.launch_count()
     with ClockSampler(local) as clk:
         barrier()
+        poll = NvmlClockPoller(device).start()
         start.record(stream)
         for i in range(args.steps):
             run_step(st, args.warmup + i, evs[i])
         stop.record(stream)
         barrier()
+        poll.stop()
     launches = api.launch_count() - launches0
     ms = start.elapsed_time(stop) / args.steps
     per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)]
@@ -337,7 +421,7 @@ def ours(args):
     e2e_steps(st, max(3, args.warmup), device)          # warm-up of the copy pipeline (streams, pinned buffers)
     e2e_ms = max_over_ranks(e2e_steps(st, args.steps, device), device)
 
-    clocks = clk.summary()
+    clocks = clock_record(poll, clk)
     hbm, hbm_kind = peaks()
     fwd_s = kern[0] * 1e-3
     achieved_bfly = BFLY_PER_FWD / fwd_s
@@ -932,12 +1016,14 @@ def row_bench(args):
     evs = _events(2 * args.steps)
     with ClockSampler(local) as clk:
         barrier()
+        poll = NvmlClockPoller(dev).start()
         for i in range(args.steps):
             row.before_step()
             evs[2 * i].record(stream)
             row.step()
             evs[2 * i + 1].record(stream)
         barrier()
+        poll.stop()
     launches = api.launch_count() - launches0
     ms = max_over_ranks(sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)) / args.steps, dev)
     fn, roof = row.probe()
@@ -965,7 +1051,7 @@ def row_bench(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "u64",
         "data": "synthetic: seeded uniform residues in [0, q) (SplitMix64 counter generator)",
         "config": dict(row.config(), parallelism=f"replicas x{ws}"),
-        "roofline": roof, "clocks": clk.summary(), "gpu_launches": launches,
+        "roofline": roof, "clocks": clock_record(poll, clk), "gpu_launches": launches,
         "e2e": {"value": whole_job_rate(row.units_per_step, ws, e2e_ms), "unit": row.unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
     }
