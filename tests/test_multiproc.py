@@ -67,7 +67,8 @@ def test_gloo_world2_max_over_ranks_and_shards():
     assert line["max_ms"] == 15.0
     assert abs(line["rate"] - 1056 * 2 / 15e-3) < 1e-6
     assert line["distinct_shards"]
-    assert outs[1].strip() == ""
+    # rank 1 prints nothing of its own (some gloo builds log their connections)
+    assert not [ln for ln in outs[1].splitlines() if ln.strip() and not ln.startswith("[Gloo]")]
 
 
 def test_reference_arm_prints_only_on_rank0():
