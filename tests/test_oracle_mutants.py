@@ -7,7 +7,10 @@ bit reversal, a '+' for the negacyclic '-', a lost automorphism sign, a
 Garner radix error, a non-minimal root, a missing 1/n, swapped key
 components, a wrong tensor cross term, a wrong prime step, a dropped
 Miller-Rabin round, two ModDown rounding mistakes, two approximate basis
-conversion mistakes and two hoisted key-switch mistakes.
+conversion mistakes, two hoisted key-switch mistakes, an inverse twist by
+the forward root, a cyclic transform by psi instead of psi^2, a wrong
+extension radix, a ModDown by P instead of P^-1, a digit width rounded down
+and an NTT-domain automorphism composed in the wrong order.
 """
 import os
 import shutil
@@ -67,6 +70,27 @@ MUTANTS = {
     "hoisted_automorphism_in_wrong_domain": (
         "oracle_automorph_batch(ext, rot, log_n, LK, batch * dnum, qp, psi_qp, ks[r], 1, threads);",
         "oracle_automorph_batch(ext, rot, log_n, LK, batch * dnum, qp, psi_qp, ks[r], 0, threads);"),
+    "intt_twist_uses_forward_root": (
+        "for (uint64_t j = 0; j < n; j++) { a[j] = mulmod(a[j], pw, q); pw = mulmod(pw, psi_inv, q); }",
+        "for (uint64_t j = 0; j < n; j++) { a[j] = mulmod(a[j], pw, q); pw = mulmod(pw, psi, q); }"),
+    "ntt_cyclic_root_not_squared": (
+        "cyclic_dft(a, log_n, q, mulmod(psi, psi, q));",
+        "cyclic_dft(a, log_n, q, psi);"),
+    "extension_radix_wrong": (
+        "        acc = addmod(acc, mulmod(v[i] % p, radix, p), p);\n        radix = mulmod(radix, d[i] % p, p);",
+        "        acc = addmod(acc, mulmod(v[i] % p, radix, p), p);\n        radix = mulmod(radix, d[i] % p, p);"
+        " if (i == 0) radix = addmod(radix, 1, p);"),
+    "moddown_multiplies_by_P": (
+        "out[l] = mulmod(num, invmod(Pm, q), q);",
+        "out[l] = mulmod(num, Pm, q);"),
+    "digit_width_rounded_down": (
+        "    int alpha = (L + dnum - 1) / dnum;\n    *lo = j * alpha;",
+        "    int alpha = L / dnum;\n    *lo = j * alpha;"),
+    "automorph_ntt_domain_composed_backwards": (
+        "    oracle_intt(tmp, log_n, q, psi);\n    oracle_automorph_coeff(tmp, out, log_n, q, k);\n"
+        "    oracle_ntt(out, log_n, q, psi);",
+        "    oracle_ntt(tmp, log_n, q, psi);\n    oracle_automorph_coeff(tmp, out, log_n, q, k);\n"
+        "    oracle_intt(out, log_n, q, psi);"),
     "miller_rabin_one_round": (
         "    for (int i = 0; i < 12; i++) {\n        uint64_t x = powmod(small[i], d, n);",
         "    for (int i = 0; i < 1; i++) {\n        uint64_t x = powmod(small[i], d, n);"),
