@@ -20,3 +20,24 @@ def test_e2e_pipeline_matches_plain_steps():
         bench.run_step(st, i)
         torch.cuda.synchronize()
         assert np.array_equal(st["KS"].cpu().numpy(), got[i]), i
+
+
+def test_pr1_row_step_is_the_negacyclic_product():
+    """One step of the bench's n=2048 / 4-prime row (forward NTT of a and b,
+    pointwise product, inverse NTT) leaves the schoolbook negacyclic product
+    a*b in its output, prime by prime."""
+    import torch
+    import gpu_util  # noqa: F401  (builds the library)
+    import bench
+    import oracle
+    from ntt_arithmetic_gb300 import inputs
+    row = bench.Pr1Row()
+    row.setup(torch.device("cuda", 0))
+    row.step()
+    torch.cuda.synchronize()
+    got = row.P.cpu().numpy()
+    n = 1 << row.LOG_N
+    for l, q in enumerate(row.q):
+        a = inputs.uniform_residues((1, row.L, n), row.q, 1, buffer=0)[0, l]
+        b = inputs.uniform_residues((1, row.L, n), row.q, 1, buffer=1)[0, l]
+        assert np.array_equal(got[l], oracle.negacyclic_mul(a, b, int(q))), l
