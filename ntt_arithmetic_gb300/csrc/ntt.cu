@@ -1,17 +1,23 @@
 // ntt.cu -- batched negacyclic NTT / INTT over RNS primes on sm_103a.
 //
-// One (polynomial, prime) row of n = 2^LOGN residues is transformed by a
-// thread-block cluster of C = 2^LOGC CTAs (C = 1 for n <= 2^13).  Each CTA
-// owns M = n / C residues in shared memory: the "compact grouped" /
-// "fixed-radix shared-memory" execution FHElium describes for its CUDA NTT
-// families ("Eager, Compile, and native execution", table "Native operator
-// families"), here built on Blackwell thread-block clusters.
+// One (polynomial, prime) row of n = 2^LOGN residues is cut into C = 2^LOGC
+// blocks of M = n / C residues (C = 1 for n <= 2^13), one CTA per block,
+// which holds its block in registers and shared memory: the "compact
+// grouped" / "fixed-radix shared-memory" execution FHElium describes for its
+// CUDA NTT families ("Eager, Compile, and native execution", table "Native
+// operator families").  The first LOGC forward stages (the last LOGC inverse
+// stages) mix the blocks: either the C CTAs form a Blackwell thread-block
+// cluster and exchange through L2, or -- the forward's "split" shapes
+// (ntt_shapes.h) -- a column kernel runs those stages over the whole row in
+// one HBM pass and the C block CTAs then run independently.
 //
 // Forward (natural -> bit-reversed, psi-merged Cooley-Tukey):
 //   stage s (s = 0 .. LOGN-1) pairs positions p and p + n/2^(s+1) inside blocks
 //   of n/2^s and multiplies by psi^brv(2^s + block) (table fwd[2^s + block]).
 //   * cross stages s < LOGC: the C elements {j1 M + j2 : j1 < C} of a column
-//     j2 live in C different CTAs; each thread loads whole columns from HBM,
+//     j2 belong to C different blocks.  Split shapes: k_ntt_fwd_cols gives
+//     each column to a few threads of one CTA and stores the stages' lazy
+//     results back in place.  Cluster shapes: each thread loads whole columns from HBM,
 //     applies the LOGC stages in registers and hands element j1 to CTA j1,
 //     either through the row's own positions in L2 (global stores, one
 //     cluster barrier with release/acquire semantics, L1-bypassing loads;
@@ -74,10 +80,6 @@ struct Shape {
     static constexpr int P = (LOGM + LOGE - 1) / LOGE;     // local passes
     static constexpr int EREM = LOGM - (P - 1) * LOGE;     // stages in the odd-sized pass
     static_assert(LOGM == LOGT + LOGE, "M = T * E");
-    static_assert(LOGC <= LOGE, "a thread holds at least one whole column");
-    // cross phase: each thread owns COLS columns of C residues, moved in
-    // groups of W adjacent columns (16-byte accesses when W = 2)
-    static constexpr int COLS = E / C, W = COLS % 2 == 0 ? 2 : 1, NG = COLS / W;
     // Staged twiddles (shared memory, after the data block), copied there
     // asynchronously at kernel start so that their latency overlaps the data
     // load instead of stalling the first butterflies of each stage.
@@ -97,6 +99,14 @@ struct Shape {
     static constexpr int ILOG = LOGM < 2 * LOGE ? LOGM : 2 * LOGE;
     static constexpr int INV_TW = 1 << ILOG;
     static constexpr int smem_words(bool inverse) { return M + 2 * (inverse ? INV_TW : FWD_TW); }
+};
+
+// Cross phase of a cluster shape: each thread owns COLS whole columns of C
+// residues, moved in groups of W adjacent columns (16-byte accesses when W = 2).
+template <class SH>
+struct Cols {
+    static_assert(SH::LOGC <= SH::LOGE, "a thread holds at least one whole column");
+    static constexpr int COLS = SH::E / SH::C, W = COLS % 2 == 0 ? 2 : 1, NG = COLS / W;
 };
 
 struct Ctx {
@@ -232,14 +242,14 @@ __device__ __forceinline__ void block_store_coalesced(const uint64_t *sm, uint64
 
 template <class SH>
 __device__ __forceinline__ void col_put_cg(const uint64_t (&x)[SH::E], int cg, int j1, uint64_t *p) {
-    if constexpr (SH::W == 2)
+    if constexpr (Cols<SH>::W == 2)
         __stcg(reinterpret_cast<ulonglong2 *>(p), make_ulonglong2(x[(2 * cg) * SH::C + j1], x[(2 * cg + 1) * SH::C + j1]));
     else
         __stcg(p, x[cg * SH::C + j1]);
 }
 template <class SH>
 __device__ __forceinline__ void col_get_cg(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
-    if constexpr (SH::W == 2) {
+    if constexpr (Cols<SH>::W == 2) {
         const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2 *>(p));
         x[(2 * cg) * SH::C + j1] = v.x;
         x[(2 * cg + 1) * SH::C + j1] = v.y;
@@ -341,13 +351,13 @@ __device__ __forceinline__ void cross_fwd(uint64_t (&x)[SH::E], const Ctx &c) {
 // First column j2 of the thread's column group cg (W adjacent columns).
 template <class SH>
 __device__ __forceinline__ int col_j2(int cg, int t, int r) {
-    return r * (SH::M / SH::C) + SH::W * (cg * SH::T + t);
+    return r * (SH::M / SH::C) + Cols<SH>::W * (cg * SH::T + t);
 }
 
 // Column-group access: residues (j1, j2 .. j2 + W - 1) <-> x[(W cg + h) C + j1].
 template <class SH>
 __device__ __forceinline__ void col_get(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
-    if constexpr (SH::W == 2) {
+    if constexpr (Cols<SH>::W == 2) {
         const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(p);
         x[(2 * cg) * SH::C + j1] = v.x;
         x[(2 * cg + 1) * SH::C + j1] = v.y;
@@ -357,7 +367,7 @@ __device__ __forceinline__ void col_get(uint64_t (&x)[SH::E], int cg, int j1, co
 }
 template <class SH>
 __device__ __forceinline__ void col_get_cs(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
-    if constexpr (SH::W == 2) {
+    if constexpr (Cols<SH>::W == 2) {
         const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(p));
         x[(2 * cg) * SH::C + j1] = v.x;
         x[(2 * cg + 1) * SH::C + j1] = v.y;
@@ -367,7 +377,7 @@ __device__ __forceinline__ void col_get_cs(uint64_t (&x)[SH::E], int cg, int j1,
 }
 template <class SH>
 __device__ __forceinline__ void col_put(const uint64_t (&x)[SH::E], int cg, int j1, uint64_t *p) {
-    if constexpr (SH::W == 2)
+    if constexpr (Cols<SH>::W == 2)
         *reinterpret_cast<ulonglong2 *>(p) = make_ulonglong2(x[(2 * cg) * SH::C + j1], x[(2 * cg + 1) * SH::C + j1]);
     else
         *p = x[cg * SH::C + j1];
@@ -455,7 +465,7 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
         constexpr int C = SH::C;
         if constexpr (!FHE_XCHG_L2) cluster_arrive_relaxed();
 #pragma unroll
-        for (int cg = 0; cg < SH::NG; cg++) {
+        for (int cg = 0; cg < Cols<SH>::NG; cg++) {
             const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
             for (int j1 = 0; j1 < C; j1++) col_get_cs<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
@@ -465,7 +475,7 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
         cross_fwd<SH, 0>(x, c);
         if constexpr (FHE_XCHG_L2) {
 #pragma unroll
-            for (int cg = 0; cg < SH::NG; cg++) {
+            for (int cg = 0; cg < Cols<SH>::NG; cg++) {
                 const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
                 for (int j1 = 0; j1 < C; j1++) col_put_cg<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
@@ -480,7 +490,7 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
             for (int j1 = 0; j1 < C; j1++) {
                 uint64_t *dst = cl.map_shared_rank(sm, (unsigned)j1);
 #pragma unroll
-                for (int cg = 0; cg < SH::NG; cg++) col_put<SH>(x, cg, j1, dst + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
+                for (int cg = 0; cg < Cols<SH>::NG; cg++) col_put<SH>(x, cg, j1, dst + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
             }
             cluster_arrive();
             cluster_wait();
@@ -492,6 +502,97 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
         __syncthreads();   // the staged twiddles are visible to every thread
     }
     fwd_passes<SH, 0>(x, sm, data + (long)c.r * SH::M, c);
+}
+
+// ------------------------------------------------------- split forward --
+//
+// The cross stages of a split shape as a kernel of their own.  The TPC =
+// 2^LOGTPC threads of a column j2 hold its C residues j1 M + j2 (stride M,
+// coalesced across the CTA's COLS adjacent columns), first as j1 = g + TPC i
+// for the stages of span >= TPC, then -- after one shared-memory exchange --
+// as j1 = VPT g + i for the spans below TPC.  Every twiddle depends on j1
+// only (fwd[2^s + (j1 >> (LOGC - s))], warp-uniform).  The outputs are
+// stored in place unreduced (< (4 LOGC + 1) q), the block kernel's input.
+template <int LOGN, int LOGC, int LOGTPC>
+__global__ void __launch_bounds__(256)
+k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+               const uint64_t *__restrict__ consts) {
+    constexpr int C = 1 << LOGC, M = 1 << (LOGN - LOGC);
+    constexpr int TPC = 1 << LOGTPC, LOGVPT = LOGC - LOGTPC, VPT = 1 << LOGVPT;
+    constexpr int COLS = 256 / TPC, CPR = M / COLS;   // columns per CTA, CTAs per row
+    static_assert(LOGTPC <= LOGVPT, "the spans below TPC lie inside one thread's run of VPT residues");
+    static_assert(M % COLS == 0, "whole CTAs per row");
+    __shared__ uint64_t tile[C][COLS];
+    // rows limb-major, as row_of: the CTAs running together share a prime
+    const long rowi = (long)blockIdx.x / CPR;
+    const int part = (int)(blockIdx.x - rowi * CPR);
+    const int l = (int)(rowi / batch);
+    const long row = (rowi - (long)l * batch) * L + l;
+    const int cl = threadIdx.x % COLS, g = threadIdx.x / COLS;
+    uint64_t *p = res + (row << LOGN) + part * COLS + cl;
+    const uint64_t q = __ldg(consts + (long)l * K_COUNT + K_Q);
+    const ulonglong2 *w = tw + ((long)l << LOGN);
+    uint64_t x[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; i++) x[i] = __ldcs(p + (long)(g + TPC * i) * M);
+#pragma unroll
+    for (int S = 0; S < LOGVPT; S++) {
+        const int HI = VPT >> (S + 1);   // span C / 2^(S+1) = TPC HI in j1
+#pragma unroll
+        for (int i = 0; i < VPT; i++) {
+            if (i & HI) continue;
+            const ulonglong2 wt = __ldg(w + (1 << S) + ((g + TPC * i) >> (LOGC - S)));
+            ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+        }
+    }
+    if constexpr (LOGTPC > 0) {
+#pragma unroll
+        for (int i = 0; i < VPT; i++) tile[g + TPC * i][cl] = x[i];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < VPT; i++) x[i] = tile[VPT * g + i][cl];
+#pragma unroll
+        for (int S = LOGVPT; S < LOGC; S++) {
+            const int HI = 1 << (LOGC - 1 - S);   // span < TPC <= VPT
+#pragma unroll
+            for (int i = 0; i < VPT; i++) {
+                if (i & HI) continue;
+                const ulonglong2 wt = __ldg(w + (1 << S) + ((VPT * g + i) >> (LOGC - S)));
+                ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; i++) __stcs(p + (long)(LOGTPC > 0 ? VPT * g + i : g + TPC * i) * M, x[i]);
+}
+
+// The local stages of a split shape: CTA r of a row transforms block r
+// (residues [r M, (r + 1) M)) on its own, with the same passes, twiddle
+// staging and coalesced store as a cluster CTA after its exchange.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+__global__ void __launch_bounds__(1 << LOGT, MINB)
+k_ntt_fwd_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+              const uint64_t *__restrict__ consts) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    extern __shared__ __align__(16) uint64_t sm[];
+    Ctx c;
+    c.t = threadIdx.x;
+    c.r = (int)(blockIdx.x & (SH::C - 1));
+    int l;
+    const long row = row_of<LOGC>(L, batch, l);
+    uint64_t *blk = res + row * SH::N + (long)c.r * SH::M;
+    c.tw = tw + (long)l * SH::N;
+    c.kc = consts + (long)l * K_COUNT;
+    c.q = c.kc[K_Q];
+    ulonglong2 *etw = reinterpret_cast<ulonglong2 *>(sm + SH::M);
+    c.etw = etw;
+    etw_issue_pass<SH, 0>(etw, c.tw, c.r, c.t);   // the local passes' shared twiddles (no cross stages here)
+    cp_async_commit();
+    uint64_t x[SH::E];
+    global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, blk, c.t);
+    cp_async_wait_all();
+    __syncthreads();   // the staged twiddles are visible to every thread
+    fwd_passes<SH, 0>(x, sm, blk, c);
 }
 
 // ---------------------------------------------------------------- inverse --
@@ -568,15 +669,15 @@ __device__ __forceinline__ void cross_inv(uint64_t (&x)[SH::E], const Ctx &c) {
     if constexpr (S < SH::LOGC) {
         constexpr int C = SH::C, H = 1 << S;
 #pragma unroll
-        for (int cg = 0; cg < SH::NG; cg++) {
+        for (int cg = 0; cg < Cols<SH>::NG; cg++) {
             const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
             for (int jlo = 0; jlo < H; jlo++) {
                 const ulonglong2 *tw = c.tw + (long)SH::M * (H + jlo) + j2;
 #pragma unroll
-                for (int h = 0; h < SH::W; h++) {
+                for (int h = 0; h < Cols<SH>::W; h++) {
                     const ulonglong2 w = __ldg(tw + h);
-                    const int col = SH::W * cg + h;
+                    const int col = Cols<SH>::W * cg + h;
 #pragma unroll
                     for (int jhi = 0; jhi < C / (2 * H); jhi++) {
                         const int j1 = jhi * 2 * H + jlo;
@@ -630,7 +731,7 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
             cluster_arrive();   // release: this block is in L2
             cluster_wait();     // acquire: every block is
 #pragma unroll
-            for (int cg = 0; cg < SH::NG; cg++) {
+            for (int cg = 0; cg < Cols<SH>::NG; cg++) {
                 const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
                 for (int j1 = 0; j1 < C; j1++) col_get_cg<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
@@ -644,22 +745,22 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
             for (int j1 = 0; j1 < C; j1++) {
                 const uint64_t *src = cl.map_shared_rank(sm, (unsigned)j1);
 #pragma unroll
-                for (int cg = 0; cg < SH::NG; cg++) col_get<SH>(x, cg, j1, src + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
+                for (int cg = 0; cg < Cols<SH>::NG; cg++) col_get<SH>(x, cg, j1, src + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
             }
         }
         cross_inv<SH, 0>(x, c);
 #pragma unroll
-        for (int cg = 0; cg < SH::NG; cg++) {
+        for (int cg = 0; cg < Cols<SH>::NG; cg++) {
             const int j2 = col_j2<SH>(cg, c.t, c.r);
 #pragma unroll
             for (int j1 = 0; j1 < C; j1++) {
                 const long p = (long)j1 * SH::M + j2;
 #pragma unroll
-                for (int h = 0; h < SH::W; h++) {
-                    const int col = SH::W * cg + h;
+                for (int h = 0; h < Cols<SH>::W; h++) {
+                    const int col = Cols<SH>::W * cg + h;
                     x[col * C + j1] = twist(x[col * C + j1], __ldg(tws + p + h), c.q);
                 }
-                if constexpr (SH::W == 2)
+                if constexpr (Cols<SH>::W == 2)
                     __stcs(reinterpret_cast<ulonglong2 *>(data + p), make_ulonglong2(x[(2 * cg) * C + j1], x[(2 * cg + 1) * C + j1]));
                 else
                     __stcs(data + p, x[cg * C + j1]);
@@ -709,12 +810,13 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
 
 // ---------------------------------------------------------------- launch --
 
-template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
-int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool inverse, cudaStream_t st) {
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, bool INVERSE>
+int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
-    void (*kern)(uint64_t *, int, int, const ulonglong2 *, const uint64_t *, const ulonglong2 *) =
-        inverse ? k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB> : k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
-    const size_t smem = (size_t)SH::smem_words(inverse) * sizeof(uint64_t);
+    void (*kern)(uint64_t *, int, int, const ulonglong2 *, const uint64_t *, const ulonglong2 *);
+    if constexpr (INVERSE) kern = k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB>;
+    else kern = k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
+    const size_t smem = (size_t)SH::smem_words(INVERSE) * sizeof(uint64_t);
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
@@ -738,11 +840,43 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
     attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
     cfg.attrs = attr;
     cfg.numAttrs = SH::C > 1 ? 2 : 0;
-    const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(inverse ? t->inv : t->fwd);
+    const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(INVERSE ? t->inv : t->fwd);
     const ulonglong2 *twist_tab = reinterpret_cast<const ulonglong2 *>(t->twist);
     if (rows % L) return -1;
     if (cudaLaunchKernelEx(&cfg, kern, res, L, (int)(rows / L), tw, t->consts, twist_tab) != cudaSuccess) return -1;
     return 1;
+}
+
+// Split forward: the column kernel (first LOGC stages), then one CTA per block.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+int launch_split_fwd(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    constexpr int LOGTPC = LOGC / 2;                  // threads per column
+    constexpr int CPR = SH::M / (256 >> LOGTPC);      // column-kernel CTAs per row
+    if (rows % L) return -1;
+    const int batch = (int)(rows / L);
+    const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(t->fwd);
+    k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)(rows * CPR), 256, 0, st>>>(res, L, batch, tw, t->consts);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    auto kern = k_ntt_fwd_blk<LOGN, LOGC, LOGT, LOGE, MINB>;
+    const size_t smem = (size_t)SH::smem_words(false) * sizeof(uint64_t);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, L, batch, tw, t->consts);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    return 2;
+}
+
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT>
+int launch_fwd(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
+    if constexpr (SPLIT) return launch_split_fwd<LOGN, LOGC, LOGT, LOGE, MINB>(res, L, rows, t, st);
+    else return launch_shape<LOGN, LOGC, LOGT, LOGE, MINB, false>(res, L, rows, t, st);
+}
+
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+int launch_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
+    return launch_shape<LOGN, LOGC, LOGT, LOGE, MINB, true>(res, L, rows, t, st);
 }
 
 }  // namespace
@@ -750,23 +884,40 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, bool 
 int launch_ntt(uint64_t *res, int log_n, int L, long rows, const fhe_ntt_tables *t, bool inverse, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     switch (log_n) {
-        case 1: return launch_shape<1, FHE_SHAPE_1>(res, L, rows, t, inverse, st);
-        case 2: return launch_shape<2, FHE_SHAPE_2>(res, L, rows, t, inverse, st);
-        case 3: return launch_shape<3, FHE_SHAPE_3>(res, L, rows, t, inverse, st);
-        case 4: return launch_shape<4, FHE_SHAPE_4>(res, L, rows, t, inverse, st);
-        case 5: return launch_shape<5, FHE_SHAPE_5>(res, L, rows, t, inverse, st);
-        case 6: return launch_shape<6, FHE_SHAPE_6>(res, L, rows, t, inverse, st);
-        case 7: return launch_shape<7, FHE_SHAPE_7>(res, L, rows, t, inverse, st);
-        case 8: return launch_shape<8, FHE_SHAPE_8>(res, L, rows, t, inverse, st);
-        case 9: return launch_shape<9, FHE_SHAPE_9>(res, L, rows, t, inverse, st);
-        case 10: return launch_shape<10, FHE_SHAPE_10>(res, L, rows, t, inverse, st);
-        case 11: return launch_shape<11, FHE_SHAPE_11>(res, L, rows, t, inverse, st);
-        case 12: return launch_shape<12, FHE_SHAPE_12>(res, L, rows, t, inverse, st);
-        case 13: return launch_shape<13, FHE_SHAPE_13>(res, L, rows, t, inverse, st);
-        case 14: return launch_shape<14, FHE_SHAPE_14>(res, L, rows, t, inverse, st);
-        case 15: return launch_shape<15, FHE_SHAPE_15>(res, L, rows, t, inverse, st);
-        case 16: return launch_shape<16, FHE_SHAPE_16>(res, L, rows, t, inverse, st);
-        case 17: return launch_shape<17, FHE_SHAPE_17>(res, L, rows, t, inverse, st);
+        case 1: return inverse ? launch_inv<1, FHE_INV_SHAPE_1>(res, L, rows, t, st)
+                          : launch_fwd<1, FHE_SHAPE_1>(res, L, rows, t, st);
+        case 2: return inverse ? launch_inv<2, FHE_INV_SHAPE_2>(res, L, rows, t, st)
+                          : launch_fwd<2, FHE_SHAPE_2>(res, L, rows, t, st);
+        case 3: return inverse ? launch_inv<3, FHE_INV_SHAPE_3>(res, L, rows, t, st)
+                          : launch_fwd<3, FHE_SHAPE_3>(res, L, rows, t, st);
+        case 4: return inverse ? launch_inv<4, FHE_INV_SHAPE_4>(res, L, rows, t, st)
+                          : launch_fwd<4, FHE_SHAPE_4>(res, L, rows, t, st);
+        case 5: return inverse ? launch_inv<5, FHE_INV_SHAPE_5>(res, L, rows, t, st)
+                          : launch_fwd<5, FHE_SHAPE_5>(res, L, rows, t, st);
+        case 6: return inverse ? launch_inv<6, FHE_INV_SHAPE_6>(res, L, rows, t, st)
+                          : launch_fwd<6, FHE_SHAPE_6>(res, L, rows, t, st);
+        case 7: return inverse ? launch_inv<7, FHE_INV_SHAPE_7>(res, L, rows, t, st)
+                          : launch_fwd<7, FHE_SHAPE_7>(res, L, rows, t, st);
+        case 8: return inverse ? launch_inv<8, FHE_INV_SHAPE_8>(res, L, rows, t, st)
+                          : launch_fwd<8, FHE_SHAPE_8>(res, L, rows, t, st);
+        case 9: return inverse ? launch_inv<9, FHE_INV_SHAPE_9>(res, L, rows, t, st)
+                          : launch_fwd<9, FHE_SHAPE_9>(res, L, rows, t, st);
+        case 10: return inverse ? launch_inv<10, FHE_INV_SHAPE_10>(res, L, rows, t, st)
+                          : launch_fwd<10, FHE_SHAPE_10>(res, L, rows, t, st);
+        case 11: return inverse ? launch_inv<11, FHE_INV_SHAPE_11>(res, L, rows, t, st)
+                          : launch_fwd<11, FHE_SHAPE_11>(res, L, rows, t, st);
+        case 12: return inverse ? launch_inv<12, FHE_INV_SHAPE_12>(res, L, rows, t, st)
+                          : launch_fwd<12, FHE_SHAPE_12>(res, L, rows, t, st);
+        case 13: return inverse ? launch_inv<13, FHE_INV_SHAPE_13>(res, L, rows, t, st)
+                          : launch_fwd<13, FHE_SHAPE_13>(res, L, rows, t, st);
+        case 14: return inverse ? launch_inv<14, FHE_INV_SHAPE_14>(res, L, rows, t, st)
+                          : launch_fwd<14, FHE_SHAPE_14>(res, L, rows, t, st);
+        case 15: return inverse ? launch_inv<15, FHE_INV_SHAPE_15>(res, L, rows, t, st)
+                          : launch_fwd<15, FHE_SHAPE_15>(res, L, rows, t, st);
+        case 16: return inverse ? launch_inv<16, FHE_INV_SHAPE_16>(res, L, rows, t, st)
+                          : launch_fwd<16, FHE_SHAPE_16>(res, L, rows, t, st);
+        case 17: return inverse ? launch_inv<17, FHE_INV_SHAPE_17>(res, L, rows, t, st)
+                          : launch_fwd<17, FHE_SHAPE_17>(res, L, rows, t, st);
         default: return -1;
     }
 }
