@@ -7,9 +7,10 @@
 // CUDA NTT families ("Eager, Compile, and native execution", table "Native
 // operator families").  The first LOGC forward stages (the last LOGC inverse
 // stages) mix the blocks: either the C CTAs form a Blackwell thread-block
-// cluster and exchange through L2, or -- the forward's "split" shapes
-// (ntt_shapes.h) -- a column kernel runs those stages over the whole row in
-// one HBM pass and the C block CTAs then run independently.
+// cluster and exchange through L2, or -- the "split" shapes (ntt_shapes.h) --
+// a column kernel runs those stages over the whole row in one HBM pass, and
+// the C block CTAs run independently before it (inverse) or after it
+// (forward).
 //
 // Forward (natural -> bit-reversed, psi-merged Cooley-Tukey):
 //   stage s (s = 0 .. LOGN-1) pairs positions p and p + n/2^(s+1) inside blocks
@@ -28,7 +29,9 @@
 //     memory round trip and one __syncthreads between passes.
 // Inverse (bit-reversed -> natural): cyclic Cooley-Tukey (decimation in time)
 //   with omega^-1 = psi^-2 followed by the twist n^-1 psi^-j; local passes
-//   first (spans 1, 2, 4, ...), cross stages last -- the mirror image.
+//   first (spans 1, 2, 4, ...), cross stages last -- the mirror image.  Split
+//   shapes: k_ntt_inv_blk runs the local passes and stores each block back
+//   unreduced, then k_ntt_inv_cols runs the cross stages and the twist.
 //
 // Twiddles: those that every thread of a CTA (or a warp) shares -- the
 // forward's cross stages and all of its local passes but the last, the
@@ -695,7 +698,9 @@ __device__ __forceinline__ uint64_t twist(uint64_t x, ulonglong2 t, uint64_t q) 
     return reduce4(shoup_lazy(x, t.x, t.y, q), q);
 }
 
-template <class SH, int PI>
+// BLK: a split shape's block kernel -- the local passes only; the block is
+// stored back in place unreduced for the column kernel (k_ntt_inv_cols).
+template <class SH, int PI, bool BLK = false>
 __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, uint64_t *data,
                                            const ulonglong2 *tws, const Ctx &c) {
     constexpr int LOGE = SH::LOGE;
@@ -707,7 +712,9 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         __syncthreads();
         constexpr int EP2 = PI + 1 == SH::P - 1 ? SH::EREM : LOGE;
         smem_load<SH, B + LOGE, EP2>(x, sm, c.t);
-        inv_passes<SH, PI + 1>(x, sm, blk, data, tws, c);
+        inv_passes<SH, PI + 1, BLK>(x, sm, blk, data, tws, c);
+    } else if constexpr (BLK) {
+        global_store<SH, B, EP>(x, blk, c.t);   // pass B holds bits >= B: coalesced
     } else if constexpr (SH::C == 1) {
         constexpr int G = SH::E >> EP, EPN = 1 << EP;
 #pragma unroll
@@ -808,6 +815,105 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
     inv_passes<SH, 0>(x, sm, blk, data, twist_tab + (long)l * SH::N, c);   // indexed by global position
 }
 
+// ------------------------------------------------------- split inverse --
+//
+// The local stages of a split shape: CTA r of a row runs spans 1 .. M/2 on
+// block r alone (the same passes and staged twiddles as a cluster CTA before
+// its exchange) and stores the block in place, unreduced.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+__global__ void __launch_bounds__(1 << LOGT, MINB)
+k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+              const uint64_t *__restrict__ consts) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    static_assert(SH::E >= 2, "the block is loaded through shared memory");
+    extern __shared__ __align__(16) uint64_t sm[];
+    Ctx c;
+    c.t = threadIdx.x;
+    c.r = (int)(blockIdx.x & (SH::C - 1));
+    int l;
+    const long row = row_of<LOGC>(L, batch, l);
+    uint64_t *blk = res + row * SH::N + (long)c.r * SH::M;
+    c.tw = tw + (long)l * SH::N;
+    c.kc = consts + (long)l * K_COUNT;
+    c.q = c.kc[K_Q];
+    ulonglong2 *etw = reinterpret_cast<ulonglong2 *>(sm + SH::M);
+    c.etw = etw;
+    for (int u = 1 + c.t; u < SH::INV_TW; u += SH::T) cp_async16(etw + u, c.tw + u);
+    cp_async_commit();
+    uint64_t x[SH::E];
+    block_load_coalesced<SH>(sm, blk, c.t);
+    cp_async_wait_all();
+    __syncthreads();   // the block and the staged twiddles are visible to every thread
+    smem_load<SH, 0, SH::P == 1 ? SH::EREM : LOGE>(x, sm, c.t);
+    inv_passes<SH, 0, true>(x, sm, blk, nullptr, nullptr, c);
+}
+
+// The cross stages of a split inverse and the twist, over whole columns.
+// The TPC = 2^LOGTPC threads of column j2 hold its C residues j1 M + j2, first
+// as j1 = VPT g + i for the spans below VPT, then -- after one shared-memory
+// exchange -- as j1 = g + TPC i for the spans >= VPT.  The span-M 2^S stage
+// pairs j1 and j1 + 2^S and multiplies by inv[M (2^S + (j1 mod 2^S)) + j2]
+// (coalesced across the CTA's COLS adjacent columns); then every residue is
+// multiplied by n^-1 psi^-p (p = j1 M + j2), reduced into [0, q) and stored.
+template <int LOGN, int LOGC, int LOGTPC>
+__global__ void __launch_bounds__(256)
+k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+               const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__ twist_tab) {
+    constexpr int C = 1 << LOGC, M = 1 << (LOGN - LOGC);
+    constexpr int TPC = 1 << LOGTPC, LOGVPT = LOGC - LOGTPC, VPT = 1 << LOGVPT;
+    constexpr int COLS = 256 / TPC, CPR = M / COLS;   // columns per CTA, CTAs per row
+    static_assert(LOGTPC <= LOGVPT, "the spans >= VPT are whole multiples of TPC");
+    static_assert(M % COLS == 0, "whole CTAs per row");
+    __shared__ uint64_t tile[C][COLS];
+    // rows limb-major, as row_of: the CTAs running together share a prime
+    const long rowi = (long)blockIdx.x / CPR;
+    const int part = (int)(blockIdx.x - rowi * CPR);
+    const int l = (int)(rowi / batch);
+    const long row = (rowi - (long)l * batch) * L + l;
+    const int cl = threadIdx.x % COLS, g = threadIdx.x / COLS;
+    const int j2 = part * COLS + cl;
+    uint64_t *p = res + (row << LOGN) + j2;
+    const uint64_t q = __ldg(consts + (long)l * K_COUNT + K_Q);
+    const ulonglong2 *w = tw + ((long)l << LOGN) + j2;
+    const ulonglong2 *tt = twist_tab + ((long)l << LOGN) + j2;
+    uint64_t x[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; i++) x[i] = __ldcs(p + (long)(VPT * g + i) * M);
+#pragma unroll
+    for (int S = 0; S < LOGVPT; S++) {
+        const int H = 1 << S;   // j1 = VPT g + i, VPT g a multiple of 2^(S+1)
+#pragma unroll
+        for (int i = 0; i < VPT; i++) {
+            if (i & H) continue;
+            const ulonglong2 wt = __ldg(w + (long)((1 << S) + (i & (H - 1))) * M);
+            ct_bfly(x[i], x[i + H], wt.x, wt.y, q);
+        }
+    }
+    if constexpr (LOGTPC > 0) {
+#pragma unroll
+        for (int i = 0; i < VPT; i++) tile[VPT * g + i][cl] = x[i];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < VPT; i++) x[i] = tile[g + TPC * i][cl];
+#pragma unroll
+        for (int S = LOGVPT; S < LOGC; S++) {
+            const int HI = 1 << (S - LOGTPC);   // span 2^S = TPC HI in j1 = g + TPC i
+#pragma unroll
+            for (int i = 0; i < VPT; i++) {
+                if (i & HI) continue;
+                const int j1 = g + TPC * i;
+                const ulonglong2 wt = __ldg(w + (long)((1 << S) + (j1 & ((1 << S) - 1))) * M);
+                ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const long off = (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M;
+        __stcs(p + off, twist(x[i], __ldg(tt + off), q));
+    }
+}
+
 // ---------------------------------------------------------------- launch --
 
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, bool INVERSE>
@@ -874,9 +980,32 @@ int launch_fwd(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStr
     else return launch_shape<LOGN, LOGC, LOGT, LOGE, MINB, false>(res, L, rows, t, st);
 }
 
+// Split inverse: one CTA per block (the local stages), then the column kernel.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+int launch_split_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    constexpr int LOGTPC = LOGC / 2;                  // threads per column
+    constexpr int CPR = SH::M / (256 >> LOGTPC);      // column-kernel CTAs per row
+    if (rows % L) return -1;
+    const int batch = (int)(rows / L);
+    const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(t->inv);
+    auto kern = k_ntt_inv_blk<LOGN, LOGC, LOGT, LOGE, MINB>;
+    const size_t smem = (size_t)SH::smem_words(true) * sizeof(uint64_t);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, L, batch, tw, t->consts);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    k_ntt_inv_cols<LOGN, LOGC, LOGTPC><<<(unsigned)(rows * CPR), 256, 0, st>>>(
+        res, L, batch, tw, t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    return 2;
+}
+
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT>
 int launch_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
-    return launch_shape<LOGN, LOGC, LOGT, LOGE, MINB, true>(res, L, rows, t, st);
+    if constexpr (SPLIT) return launch_split_inv<LOGN, LOGC, LOGT, LOGE, MINB>(res, L, rows, t, st);
+    else return launch_shape<LOGN, LOGC, LOGT, LOGE, MINB, true>(res, L, rows, t, st);
 }
 
 }  // namespace

@@ -11,7 +11,9 @@
 //   1 -- split: a column kernel runs the first log2 C stages over the whole
 //        row, then C independent CTAs run the remaining stages on one block
 //        each (no cluster; measured 8 % faster at n = 2^16, 20 % at 2^17).
-// The inverse shapes (FHE_INV_SHAPE_n, the first four fields) are clusters.
+// The inverse shapes (FHE_INV_SHAPE_n) have the same five fields; a split
+// inverse runs the block CTAs first (the local stages) and the column kernel
+// last (the last log2 C stages and the twist n^-1 psi^-j).
 #define FHE_SHAPE_1 0, 0, 1, 1, 0
 #define FHE_SHAPE_2 0, 0, 2, 1, 0
 #define FHE_SHAPE_3 0, 0, 3, 1, 0
@@ -44,24 +46,35 @@
 #define FHE_SHAPE_17 6, 7, 4, 4, 1
 #endif
 
-// Inverse shapes: the cluster shapes for n >= 2^14, the forward ones below.
-#define FHE_INV_SHAPE_1 0, 0, 1, 1
-#define FHE_INV_SHAPE_2 0, 0, 2, 1
-#define FHE_INV_SHAPE_3 0, 0, 3, 1
-#define FHE_INV_SHAPE_4 0, 1, 3, 1
-#define FHE_INV_SHAPE_5 0, 2, 3, 1
-#define FHE_INV_SHAPE_6 0, 3, 3, 1
-#define FHE_INV_SHAPE_7 0, 4, 3, 1
-#define FHE_INV_SHAPE_8 0, 5, 3, 1
-#define FHE_INV_SHAPE_9 0, 6, 3, 1
-#define FHE_INV_SHAPE_10 0, 7, 3, 1
-#define FHE_INV_SHAPE_11 0, 7, 4, 4
-#define FHE_INV_SHAPE_12 0, 8, 4, 2
-#define FHE_INV_SHAPE_13 0, 8, 5, 2
-#define FHE_INV_SHAPE_14 1, 8, 5, 2
-#define FHE_INV_SHAPE_15 2, 8, 5, 2
-#define FHE_INV_SHAPE_16 3, 8, 5, 2
-#define FHE_INV_SHAPE_17 4, 8, 5, 2
+// Inverse shapes: split for n = 2^16 and 2^17 (measured on 201 MB of
+// residues: 247 against 263 us at 2^16, 259 against 338 us at 2^17), clusters
+// of 2^LOGC CTAs for 2^14 (229 against 234 us split) and 2^15, one CTA per
+// row below.
+#define FHE_INV_SHAPE_1 0, 0, 1, 1, 0
+#define FHE_INV_SHAPE_2 0, 0, 2, 1, 0
+#define FHE_INV_SHAPE_3 0, 0, 3, 1, 0
+#define FHE_INV_SHAPE_4 0, 1, 3, 1, 0
+#define FHE_INV_SHAPE_5 0, 2, 3, 1, 0
+#define FHE_INV_SHAPE_6 0, 3, 3, 1, 0
+#define FHE_INV_SHAPE_7 0, 4, 3, 1, 0
+#define FHE_INV_SHAPE_8 0, 5, 3, 1, 0
+#define FHE_INV_SHAPE_9 0, 6, 3, 1, 0
+#define FHE_INV_SHAPE_10 0, 7, 3, 1, 0
+#define FHE_INV_SHAPE_11 0, 7, 4, 4, 0
+#define FHE_INV_SHAPE_12 0, 8, 4, 2, 0
+#define FHE_INV_SHAPE_13 0, 8, 5, 2, 0
+#ifndef FHE_INV_SHAPE_14
+#define FHE_INV_SHAPE_14 1, 8, 5, 2, 0
+#endif
+#ifndef FHE_INV_SHAPE_15
+#define FHE_INV_SHAPE_15 2, 8, 5, 2, 0
+#endif
+#ifndef FHE_INV_SHAPE_16
+#define FHE_INV_SHAPE_16 5, 7, 4, 4, 1
+#endif
+#ifndef FHE_INV_SHAPE_17
+#define FHE_INV_SHAPE_17 6, 7, 4, 4, 1
+#endif
 
 namespace fhe {
 
