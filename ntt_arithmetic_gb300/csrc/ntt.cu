@@ -509,7 +509,9 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
 
 // ------------------------------------------------------- split forward --
 //
-// The cross stages of a split shape as a kernel of their own.  The TPC =
+// The cross stages of a split shape as a kernel of their own.  CTA (l, chunk,
+// part) owns COLS adjacent columns j2 of prime l for up to `chunk` consecutive
+// batch items, and loads item b + 1 while it transforms item b.  The TPC =
 // 2^LOGTPC threads of a column j2 hold its C residues j1 M + j2 (stride M,
 // coalesced across the CTA's COLS adjacent columns), first as j1 = g + TPC i
 // for the stages of span >= TPC, then -- after one shared-memory exchange --
@@ -517,8 +519,8 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
 // only (fwd[2^s + (j1 >> (LOGC - s))], warp-uniform).  The outputs are
 // stored in place unreduced (< (4 LOGC + 1) q), the block kernel's input.
 template <int LOGN, int LOGC, int LOGTPC>
-__global__ void __launch_bounds__(256)
-k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+__global__ void __launch_bounds__(256, 4)
+k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ulonglong2 *__restrict__ tw,
                const uint64_t *__restrict__ consts) {
     constexpr int C = 1 << LOGC, M = 1 << (LOGN - LOGC);
     constexpr int TPC = 1 << LOGTPC, LOGVPT = LOGC - LOGTPC, VPT = 1 << LOGVPT;
@@ -526,47 +528,59 @@ k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *_
     static_assert(LOGTPC <= LOGVPT, "the spans below TPC lie inside one thread's run of VPT residues");
     static_assert(M % COLS == 0, "whole CTAs per row");
     __shared__ uint64_t tile[C][COLS];
-    // rows limb-major, as row_of: the CTAs running together share a prime
-    const long rowi = (long)blockIdx.x / CPR;
-    const int part = (int)(blockIdx.x - rowi * CPR);
-    const int l = (int)(rowi / batch);
-    const long row = (rowi - (long)l * batch) * L + l;
+    // limb-major (as row_of): the CTAs running together share a prime
+    const int part = (int)(blockIdx.x % CPR);
+    const int nch = (batch + chunk - 1) / chunk;
+    const int rest = (int)(blockIdx.x / CPR);
+    const int l = rest / nch, b0 = (rest - l * nch) * chunk;
+    const int b1 = min(batch, b0 + chunk);
     const int cl = threadIdx.x % COLS, g = threadIdx.x / COLS;
-    uint64_t *p = res + (row << LOGN) + part * COLS + cl;
     const uint64_t q = __ldg(consts + (long)l * K_COUNT + K_Q);
     const ulonglong2 *w = tw + ((long)l << LOGN);
-    uint64_t x[VPT];
+    const long rstride = (long)L << LOGN;   // between consecutive batch items of one prime
+    uint64_t *p = res + ((long)b0 * L + l) * ((long)1 << LOGN) + part * COLS + cl;
+    uint64_t xn[VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; i++) x[i] = __ldcs(p + (long)(g + TPC * i) * M);
+    for (int i = 0; i < VPT; i++) xn[i] = __ldcs(p + (long)(g + TPC * i) * M);
+    for (int b = b0; b < b1; b++, p += rstride) {
+        uint64_t x[VPT];
 #pragma unroll
-    for (int S = 0; S < LOGVPT; S++) {
-        const int HI = VPT >> (S + 1);   // span C / 2^(S+1) = TPC HI in j1
+        for (int i = 0; i < VPT; i++) x[i] = xn[i];
+        if (b + 1 < b1) {
 #pragma unroll
-        for (int i = 0; i < VPT; i++) {
-            if (i & HI) continue;
-            const ulonglong2 wt = __ldg(w + (1 << S) + ((g + TPC * i) >> (LOGC - S)));
-            ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+            for (int i = 0; i < VPT; i++) xn[i] = __ldcs(p + rstride + (long)(g + TPC * i) * M);
         }
-    }
-    if constexpr (LOGTPC > 0) {
 #pragma unroll
-        for (int i = 0; i < VPT; i++) tile[g + TPC * i][cl] = x[i];
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < VPT; i++) x[i] = tile[VPT * g + i][cl];
-#pragma unroll
-        for (int S = LOGVPT; S < LOGC; S++) {
-            const int HI = 1 << (LOGC - 1 - S);   // span < TPC <= VPT
+        for (int S = 0; S < LOGVPT; S++) {
+            const int HI = VPT >> (S + 1);   // span C / 2^(S+1) = TPC HI in j1
 #pragma unroll
             for (int i = 0; i < VPT; i++) {
                 if (i & HI) continue;
-                const ulonglong2 wt = __ldg(w + (1 << S) + ((VPT * g + i) >> (LOGC - S)));
+                const ulonglong2 wt = __ldg(w + (1 << S) + ((g + TPC * i) >> (LOGC - S)));
                 ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
             }
         }
-    }
+        if constexpr (LOGTPC > 0) {
+            __syncthreads();   // the previous item's tile reads are done
 #pragma unroll
-    for (int i = 0; i < VPT; i++) __stcs(p + (long)(LOGTPC > 0 ? VPT * g + i : g + TPC * i) * M, x[i]);
+            for (int i = 0; i < VPT; i++) tile[g + TPC * i][cl] = x[i];
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < VPT; i++) x[i] = tile[VPT * g + i][cl];
+#pragma unroll
+            for (int S = LOGVPT; S < LOGC; S++) {
+                const int HI = 1 << (LOGC - 1 - S);   // span < TPC <= VPT
+#pragma unroll
+                for (int i = 0; i < VPT; i++) {
+                    if (i & HI) continue;
+                    const ulonglong2 wt = __ldg(w + (1 << S) + ((VPT * g + i) >> (LOGC - S)));
+                    ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; i++) __stcs(p + (long)(LOGTPC > 0 ? VPT * g + i : g + TPC * i) * M, x[i]);
+    }
 }
 
 // The local stages of a split shape: CTA r of a row transforms block r
@@ -849,68 +863,83 @@ k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__
 }
 
 // The cross stages of a split inverse and the twist, over whole columns.
-// The TPC = 2^LOGTPC threads of column j2 hold its C residues j1 M + j2, first
-// as j1 = VPT g + i for the spans below VPT, then -- after one shared-memory
-// exchange -- as j1 = g + TPC i for the spans >= VPT.  The span-M 2^S stage
-// pairs j1 and j1 + 2^S and multiplies by inv[M (2^S + (j1 mod 2^S)) + j2]
-// (coalesced across the CTA's COLS adjacent columns); then every residue is
-// multiplied by n^-1 psi^-p (p = j1 M + j2), reduced into [0, q) and stored.
+// CTA (l, chunk, part) owns COLS adjacent columns j2 of prime l and runs them
+// for up to `chunk` consecutive batch items.  The TPC = 2^LOGTPC threads of
+// column j2 hold its C residues j1 M + j2, first as j1 = VPT g + i for the
+// spans below VPT, then -- after one shared-memory exchange -- as
+// j1 = g + TPC i for the spans >= VPT.  The span-M 2^S stage pairs j1 and
+// j1 + 2^S and multiplies by inv[M (2^S + (j1 mod 2^S)) + j2]: those C - 1
+// twiddles of each column depend on the column, not on the batch item, so the
+// CTA copies them into shared memory once (cp.async, overlapping the first
+// item's loads) and every item reads them there.  Last, every residue is
+// multiplied by n^-1 psi^-p (p = j1 M + j2, loaded with the item's residues),
+// reduced into [0, q) and stored.
 template <int LOGN, int LOGC, int LOGTPC>
 __global__ void __launch_bounds__(256)
-k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ulonglong2 *__restrict__ tw,
                const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__ twist_tab) {
     constexpr int C = 1 << LOGC, M = 1 << (LOGN - LOGC);
     constexpr int TPC = 1 << LOGTPC, LOGVPT = LOGC - LOGTPC, VPT = 1 << LOGVPT;
     constexpr int COLS = 256 / TPC, CPR = M / COLS;   // columns per CTA, CTAs per row
     static_assert(LOGTPC <= LOGVPT, "the spans >= VPT are whole multiples of TPC");
     static_assert(M % COLS == 0, "whole CTAs per row");
+    __shared__ __align__(16) ulonglong2 stw[C - 1][COLS];   // twiddle 2^S + jlo of column cl at [2^S + jlo - 1][cl]
     __shared__ uint64_t tile[C][COLS];
-    // rows limb-major, as row_of: the CTAs running together share a prime
-    const long rowi = (long)blockIdx.x / CPR;
-    const int part = (int)(blockIdx.x - rowi * CPR);
-    const int l = (int)(rowi / batch);
-    const long row = (rowi - (long)l * batch) * L + l;
+    // limb-major (as row_of): the CTAs running together share a prime
+    const int part = (int)(blockIdx.x % CPR);
+    const int nch = (batch + chunk - 1) / chunk;
+    const int rest = (int)(blockIdx.x / CPR);
+    const int l = rest / nch, b0 = (rest - l * nch) * chunk;
+    const int b1 = min(batch, b0 + chunk);
     const int cl = threadIdx.x % COLS, g = threadIdx.x / COLS;
     const int j2 = part * COLS + cl;
-    uint64_t *p = res + (row << LOGN) + j2;
+    const ulonglong2 *wl = tw + ((long)l << LOGN) + part * COLS;
+    for (int u = threadIdx.x; u < (C - 1) * COLS; u += 256)
+        cp_async16(&stw[u / COLS][u % COLS], wl + (long)(u / COLS + 1) * M + u % COLS);
+    cp_async_commit();
     const uint64_t q = __ldg(consts + (long)l * K_COUNT + K_Q);
-    const ulonglong2 *w = tw + ((long)l << LOGN) + j2;
     const ulonglong2 *tt = twist_tab + ((long)l << LOGN) + j2;
-    uint64_t x[VPT];
+    for (int b = b0; b < b1; b++) {
+        uint64_t *p = res + ((long)b * L + l) * ((long)1 << LOGN) + j2;
+        uint64_t x[VPT];
+        ulonglong2 tv[VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; i++) x[i] = __ldcs(p + (long)(VPT * g + i) * M);
+        for (int i = 0; i < VPT; i++) x[i] = __ldcs(p + (long)(VPT * g + i) * M);
 #pragma unroll
-    for (int S = 0; S < LOGVPT; S++) {
-        const int H = 1 << S;   // j1 = VPT g + i, VPT g a multiple of 2^(S+1)
+        for (int i = 0; i < VPT; i++) tv[i] = __ldg(tt + (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M);
+        cp_async_wait_all();
+        __syncthreads();   // the staged twiddles are visible; the previous item's tile reads are done
 #pragma unroll
-        for (int i = 0; i < VPT; i++) {
-            if (i & H) continue;
-            const ulonglong2 wt = __ldg(w + (long)((1 << S) + (i & (H - 1))) * M);
-            ct_bfly(x[i], x[i + H], wt.x, wt.y, q);
-        }
-    }
-    if constexpr (LOGTPC > 0) {
-#pragma unroll
-        for (int i = 0; i < VPT; i++) tile[VPT * g + i][cl] = x[i];
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < VPT; i++) x[i] = tile[g + TPC * i][cl];
-#pragma unroll
-        for (int S = LOGVPT; S < LOGC; S++) {
-            const int HI = 1 << (S - LOGTPC);   // span 2^S = TPC HI in j1 = g + TPC i
+        for (int S = 0; S < LOGVPT; S++) {
+            const int H = 1 << S;   // j1 = VPT g + i, VPT g a multiple of 2^(S+1)
 #pragma unroll
             for (int i = 0; i < VPT; i++) {
-                if (i & HI) continue;
-                const int j1 = g + TPC * i;
-                const ulonglong2 wt = __ldg(w + (long)((1 << S) + (j1 & ((1 << S) - 1))) * M);
-                ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+                if (i & H) continue;
+                const ulonglong2 wt = stw[(1 << S) + (i & (H - 1)) - 1][cl];
+                ct_bfly(x[i], x[i + H], wt.x, wt.y, q);
             }
         }
-    }
+        if constexpr (LOGTPC > 0) {
 #pragma unroll
-    for (int i = 0; i < VPT; i++) {
-        const long off = (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M;
-        __stcs(p + off, twist(x[i], __ldg(tt + off), q));
+            for (int i = 0; i < VPT; i++) tile[VPT * g + i][cl] = x[i];
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < VPT; i++) x[i] = tile[g + TPC * i][cl];
+#pragma unroll
+            for (int S = LOGVPT; S < LOGC; S++) {
+                const int HI = 1 << (S - LOGTPC);   // span 2^S = TPC HI in j1 = g + TPC i
+#pragma unroll
+                for (int i = 0; i < VPT; i++) {
+                    if (i & HI) continue;
+                    const int j1 = g + TPC * i;
+                    const ulonglong2 wt = stw[(1 << S) + (j1 & ((1 << S) - 1)) - 1][cl];
+                    ct_bfly(x[i], x[i + HI], wt.x, wt.y, q);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; i++)
+            __stcs(p + (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M, twist(x[i], tv[i], q));
     }
 }
 
@@ -962,7 +991,12 @@ int launch_split_fwd(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, c
     if (rows % L) return -1;
     const int batch = (int)(rows / L);
     const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(t->fwd);
-    k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)(rows * CPR), 256, 0, st>>>(res, L, batch, tw, t->consts);
+    // batch items per column CTA: up to 4, balanced (each CTA loads item
+    // b + 1 while it transforms item b)
+    const int nch = (batch + 3) / 4, chunk = (batch + nch - 1) / nch;
+    const int nchunks = (batch + chunk - 1) / chunk;
+    k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)L * nchunks * CPR), 256, 0, st>>>(res, L, batch, chunk,
+                                                                                            tw, t->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
     auto kern = k_ntt_fwd_blk<LOGN, LOGC, LOGT, LOGE, MINB>;
     const size_t smem = (size_t)SH::smem_words(false) * sizeof(uint64_t);
@@ -996,8 +1030,12 @@ int launch_split_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, c
         return -1;
     kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, L, batch, tw, t->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    k_ntt_inv_cols<LOGN, LOGC, LOGTPC><<<(unsigned)(rows * CPR), 256, 0, st>>>(
-        res, L, batch, tw, t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
+    // batch items per column CTA: up to 4, balanced, so the staged twiddles
+    // serve several items and the grid still spans several waves
+    const int nch = (batch + 3) / 4, chunk = (batch + nch - 1) / nch;
+    const int nchunks = (batch + chunk - 1) / chunk;
+    k_ntt_inv_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)L * nchunks * CPR), 256, 0, st>>>(
+        res, L, batch, chunk, tw, t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
     if (cudaGetLastError() != cudaSuccess) return -1;
     return 2;
 }
