@@ -454,8 +454,9 @@ def ours(args):
         "roofline": {"bound": "alu", "achieved": achieved_bfly / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
                      "unit": "Gbutterfly/s", "frac": achieved_bfly / ALU_PEAK_BFLY, "traffic": ntt_fwd_traffic(),
                      "traffic_unit": "bytes/launch", "algorithmic_bytes": NTT_BYTES_PER_FWD,
-                     "kernel": "forward NTT call = k_ntt_fwd_cols<16,5,2> (first 5 stages, strided columns) + "
-                               "k_ntt_fwd_blk<16,5,7,4,4> (last 11 stages, one CTA per 2048-block); n=2^16, 384 rows",
+                     "kernel": "forward NTT call = k_ntt_fwd_cols<16,6,3> (first 6 stages, strided columns) + "
+                               "k_ntt_fwd_blk<16,6,6,4,8> (last 10 stages, one CTA per 1024-residue block); "
+                               "n=2^16, 384 rows; traffic = both launches",
                      "measured_butterfly_ceiling": ceiling / 1e9, "frac_of_measured_ceiling": achieved_bfly / ceiling,
                      "ceiling_note": "fhe_butterfly_probe: the same butterfly register-resident, no memory traffic",
                      "hbm_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9, "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind},

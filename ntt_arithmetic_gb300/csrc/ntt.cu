@@ -561,7 +561,7 @@ k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
             }
         }
         if constexpr (LOGTPC > 0) {
-            __syncthreads();   // the previous item's tile reads are done
+            if (b > b0) __syncthreads();   // the previous item's tile reads are done
 #pragma unroll
             for (int i = 0; i < VPT; i++) tile[g + TPC * i][cl] = x[i];
             __syncthreads();

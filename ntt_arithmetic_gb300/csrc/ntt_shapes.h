@@ -11,6 +11,12 @@
 //   1 -- split: a column kernel runs the first log2 C stages over the whole
 //        row, then C independent CTAs run the remaining stages on one block
 //        each (no cluster; measured 8 % faster at n = 2^16, 20 % at 2^17).
+//        At n = 2^16 blocks of 1024 residues (C = 64, 64 threads, 8 CTAs per
+//        SM) beat blocks of 2048 (C = 32, 128 threads, 4 CTAs): 245 against
+//        250 us forward, 234 against 237 us inverse on 384 rows; blocks of
+//        4096 (256 threads) or 8 residues per thread were 8 % slower.  The
+//        same 1024-residue blocks at n = 2^14 (C = 16): 249 against 257 us
+//        with C = 8 (201 MB of residues).
 // The inverse shapes (FHE_INV_SHAPE_n) have the same five fields; a split
 // inverse runs the block CTAs first (the local stages) and the column kernel
 // last (the last log2 C stages and the twist n^-1 psi^-j).
@@ -34,13 +40,13 @@
 #define FHE_SHAPE_13 0, 8, 5, 2, 0
 #endif
 #ifndef FHE_SHAPE_14
-#define FHE_SHAPE_14 3, 7, 4, 4, 1
+#define FHE_SHAPE_14 4, 6, 4, 8, 1
 #endif
 #ifndef FHE_SHAPE_15
 #define FHE_SHAPE_15 2, 8, 5, 2, 0
 #endif
 #ifndef FHE_SHAPE_16
-#define FHE_SHAPE_16 5, 7, 4, 4, 1
+#define FHE_SHAPE_16 6, 6, 4, 8, 1
 #endif
 #ifndef FHE_SHAPE_17
 #define FHE_SHAPE_17 6, 7, 4, 4, 1
@@ -70,7 +76,7 @@
 #define FHE_INV_SHAPE_15 2, 8, 5, 2, 0
 #endif
 #ifndef FHE_INV_SHAPE_16
-#define FHE_INV_SHAPE_16 5, 7, 4, 4, 1
+#define FHE_INV_SHAPE_16 6, 6, 4, 8, 1
 #endif
 #ifndef FHE_INV_SHAPE_17
 #define FHE_INV_SHAPE_17 6, 7, 4, 4, 1
