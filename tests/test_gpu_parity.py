@@ -49,6 +49,27 @@ def test_ntt_fwd_inv_every_size(g, log_n):
     assert np.array_equal(g.host(d2), oracle.ntt_batch(y, qs, ps, inverse=True))
 
 
+@pytest.mark.parametrize("log_n", [14, 16, 17])
+@pytest.mark.parametrize("batch", [5, 7])
+def test_split_ntt_ragged_batch_chunks(g, log_n, batch):
+    """The split shapes' column kernels run up to 4 batch items of one prime
+    per CTA (5 -> 3 + 2, 7 -> 4 + 3): every row of both chunks, forward and
+    inverse, against the oracle."""
+    n = 1 << log_n
+    L = 3
+    qs = g.primes(log_n, L)
+    t = g.tables(log_n, qs)
+    ps = oracle.psis(qs, n)
+    x = inputs.uniform_residues((batch, L, n), qs, 300 + log_n + batch)
+    d = g.dev(x)
+    g.api.ntt_fwd(d, t)
+    assert np.array_equal(g.host(d), oracle.ntt_batch(x, qs, ps))
+    y = inputs.uniform_residues((batch, L, n), qs, 400 + log_n + batch)
+    d2 = g.dev(y)
+    g.api.ntt_inv(d2, t)
+    assert np.array_equal(g.host(d2), oracle.ntt_batch(y, qs, ps, inverse=True))
+
+
 def test_pr1_reference_schoolbook(g):
     """PR1 workload: n=2048, the 4 largest q < 2^50 with q = 1 mod 4096, one
     polynomial pair: NTT, pointwise product, INTT == the O(n^2) negacyclic
