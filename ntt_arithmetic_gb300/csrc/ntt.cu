@@ -5,39 +5,35 @@
 // which holds its block in registers and shared memory: the "compact
 // grouped" / "fixed-radix shared-memory" execution FHElium describes for its
 // CUDA NTT families ("Eager, Compile, and native execution", table "Native
-// operator families").  The first LOGC forward stages (the last LOGC inverse
-// stages) mix the blocks: either the C CTAs form a Blackwell thread-block
-// cluster and exchange through L2, or -- the "split" shapes (ntt_shapes.h) --
-// a column kernel runs those stages over the whole row in one HBM pass, and
-// the C block CTAs run independently before it (inverse) or after it
-// (forward).
+// operator families").  For n >= 2^14 (the "split" shapes of ntt_shapes.h)
+// the first LOGC forward stages (the last LOGC inverse stages), which mix
+// the blocks, run in a column kernel over the whole row in one HBM pass, and
+// the C block CTAs run independently after it (forward) or before it
+// (inverse): a two-kernel decomposition.
 //
 // Forward (natural -> bit-reversed, psi-merged Cooley-Tukey):
 //   stage s (s = 0 .. LOGN-1) pairs positions p and p + n/2^(s+1) inside blocks
 //   of n/2^s and multiplies by psi^brv(2^s + block) (table fwd[2^s + block]).
 //   * cross stages s < LOGC: the C elements {j1 M + j2 : j1 < C} of a column
-//     j2 belong to C different blocks.  Split shapes: k_ntt_fwd_cols gives
-//     each column to a few threads of one CTA and stores the stages' lazy
-//     results back in place.  Cluster shapes: each thread loads whole columns from HBM,
-//     applies the LOGC stages in registers and hands element j1 to CTA j1,
-//     either through the row's own positions in L2 (global stores, one
-//     cluster barrier with release/acquire semantics, L1-bypassing loads;
-//     the default, measured faster on GB300 than remote shared-memory
-//     stores) or through distributed shared memory;
+//     j2 belong to C different blocks.  k_ntt_fwd_cols gives each column to a
+//     few threads of one CTA and stores the stages' lazy results back in place;
 //   * local stages s >= LOGC run in passes of up to LOGE stages: a thread
 //     holds 2^LOGE residues (radix-2^LOGE in registers), with one shared-
-//     memory round trip and one __syncthreads between passes.
+//     memory round trip and one __syncthreads between passes (k_ntt_fwd for
+//     C = 1, k_ntt_fwd_blk per block for C > 1).
 // Inverse (bit-reversed -> natural): cyclic Cooley-Tukey (decimation in time)
 //   with omega^-1 = psi^-2 followed by the twist n^-1 psi^-j; local passes
-//   first (spans 1, 2, 4, ...), cross stages last -- the mirror image.  Split
-//   shapes: k_ntt_inv_blk runs the local passes and stores each block back
-//   unreduced, then k_ntt_inv_cols runs the cross stages and the twist.
+//   first (spans 1, 2, 4, ...), cross stages last -- the mirror image.  C = 1:
+//   k_ntt_inv; C > 1: k_ntt_inv_blk runs the local passes and stores each
+//   block back unreduced, then k_ntt_inv_cols runs the cross stages and the
+//   twist.
 //
 // Twiddles: those that every thread of a CTA (or a warp) shares -- the
-// forward's cross stages and all of its local passes but the last, the
-// inverse's first two local passes -- are copied into shared memory with
-// cp.async at kernel start, overlapping the data load; the per-thread
-// twiddles of the remaining stages are read from the table coalesced.
+// forward's local passes but the last, the inverse's first two local passes,
+// the inverse column kernel's per-column twiddles -- are copied into shared
+// memory with cp.async at kernel start, overlapping the data load; the
+// per-thread twiddles of the remaining stages are read from the table
+// coalesced.
 //
 // Arithmetic: lazy Shoup butterflies (fhe_arith.cuh).  Values grow by < 4q
 // per stage with no comparisons (forward: < 69 q after 17 stages; inverse:
@@ -47,22 +43,11 @@
 // Shared-memory index swizzle: index p is stored at p ^ (((p >> LOGE) & 7) << 1),
 // which makes every pass's accesses bank-conflict-free (two wavefronts per
 // 64-bit warp access) and keeps 16-byte pairs (2k, 2k+1) adjacent.
-#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "fhe_arith.cuh"
 #include "fhe_internal.h"
 #include "ntt_shapes.h"
-
-namespace cg = cooperative_groups;
-
-// Cross-CTA exchange of the cluster NTT: 0 = distributed shared memory
-// (remote stores / loads), 1 = through the row's own HBM positions, which
-// are L2-resident at these sizes (global stores, a cluster barrier with
-// release/acquire semantics, then L1-bypassing loads).
-#ifndef FHE_XCHG_L2
-#define FHE_XCHG_L2 1
-#endif
 
 namespace fhe {
 namespace {
@@ -86,17 +71,16 @@ struct Shape {
     // Staged twiddles (shared memory, after the data block), copied there
     // asynchronously at kernel start so that their latency overlaps the data
     // load instead of stalling the first butterflies of each stage.
-    // Forward: the cross stages and every local pass but the last, laid out
-    // [cross: C - 1][pass 0][pass 1]..., stage I of pass PI holding the CTA's
-    // 2^(LOGM - B - EP + I) consecutive table entries (the last pass reads
-    // the table directly, coalesced).
+    // Forward: every local pass but the last, laid out [pass 0][pass 1]...,
+    // stage I of pass PI holding the CTA's 2^(LOGM - B - EP + I) consecutive
+    // table entries (the last pass reads the table directly, coalesced).
     __host__ __device__ static constexpr int pass_b(int pi) { return (P - 1 - pi) * LOGE; }
     __host__ __device__ static constexpr int pass_ep(int pi) { return pi == 0 ? EREM : LOGE; }
     __host__ __device__ static constexpr int pass_cnt(int pi) {
         return (1 << (LOGM - pass_b(pi) - pass_ep(pi))) * ((1 << pass_ep(pi)) - 1);
     }
-    __host__ __device__ static constexpr int seg_off(int pi) { return pi == 0 ? C - 1 : seg_off(pi - 1) + pass_cnt(pi - 1); }
-    static constexpr int FWD_TW = P >= 2 ? seg_off(P - 1) : C - 1;
+    __host__ __device__ static constexpr int seg_off(int pi) { return pi == 0 ? 0 : seg_off(pi - 1) + pass_cnt(pi - 1); }
+    static constexpr int FWD_TW = P >= 2 ? seg_off(P - 1) : 0;
     // Inverse: table entries [1, 2^ILOG) -- every twiddle of the first two
     // local passes, which depend on the position inside the block only.
     static constexpr int ILOG = LOGM < 2 * LOGE ? LOGM : 2 * LOGE;
@@ -104,35 +88,17 @@ struct Shape {
     static constexpr int smem_words(bool inverse) { return M + 2 * (inverse ? INV_TW : FWD_TW); }
 };
 
-// Cross phase of a cluster shape: each thread owns COLS whole columns of C
-// residues, moved in groups of W adjacent columns (16-byte accesses when W = 2).
-template <class SH>
-struct Cols {
-    static_assert(SH::LOGC <= SH::LOGE, "a thread holds at least one whole column");
-    static constexpr int COLS = SH::E / SH::C, W = COLS % 2 == 0 ? 2 : 1, NG = COLS / W;
-};
-
 struct Ctx {
     const ulonglong2 *tw;   // this prime's twiddle pairs (w, floor(w 2^64 / q))
     const uint64_t *kc;     // this prime's constants
     uint64_t q;
     int t;                  // thread index
-    int r;                  // rank in the cluster
+    int r;                  // block index within the row
     const ulonglong2 *etw;  // staged twiddles (shared memory)
 };
 
 template <int LOGE>
 __device__ __forceinline__ int swz(int p) { return p ^ (((p >> LOGE) & 7) << 1); }
-
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
 
 // Position inside the CTA's block of the j-th residue of group g in a pass
 // covering local bit positions [B, B + EP).
@@ -243,34 +209,6 @@ __device__ __forceinline__ void block_store_coalesced(const uint64_t *sm, uint64
     }
 }
 
-template <class SH>
-__device__ __forceinline__ void col_put_cg(const uint64_t (&x)[SH::E], int cg, int j1, uint64_t *p) {
-    if constexpr (Cols<SH>::W == 2)
-        __stcg(reinterpret_cast<ulonglong2 *>(p), make_ulonglong2(x[(2 * cg) * SH::C + j1], x[(2 * cg + 1) * SH::C + j1]));
-    else
-        __stcg(p, x[cg * SH::C + j1]);
-}
-template <class SH>
-__device__ __forceinline__ void col_get_cg(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
-    if constexpr (Cols<SH>::W == 2) {
-        const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2 *>(p));
-        x[(2 * cg) * SH::C + j1] = v.x;
-        x[(2 * cg + 1) * SH::C + j1] = v.y;
-    } else {
-        x[cg * SH::C + j1] = __ldcg(p);
-    }
-}
-template <class SH, int B, int EP>
-__device__ __forceinline__ void global_load_cg(uint64_t (&x)[SH::E], const uint64_t *blk, int t) {
-    constexpr int G = SH::E >> EP, EPN = 1 << EP;
-#pragma unroll
-    for (int k = 0; k < G; k++) {
-        const int g = t + SH::T * k;
-#pragma unroll
-        for (int j = 0; j < EPN; j++) x[k * EPN + j] = __ldcg(blk + pass_pos<B, EP>(g, j));
-    }
-}
-
 // ---------------------------------------------------------------- forward --
 
 // Local stage I of a pass over bits [B, B+EP): global stage s = LOGN-B-EP+I,
@@ -335,57 +273,6 @@ __device__ __forceinline__ void fwd_compute(uint64_t (&x)[SH::E], const Ctx &c) 
     }
 }
 
-// Cross-CTA stages (s < LOGC) on columns: x[col * C + j1].
-template <class SH, int S>
-__device__ __forceinline__ void cross_fwd(uint64_t (&x)[SH::E], const Ctx &c) {
-    if constexpr (S < SH::LOGC) {
-        constexpr int C = SH::C, COLS = SH::E / C, H = C >> (S + 1);
-#pragma unroll
-        for (int j1 = 0; j1 < C; j1++) {
-            if (j1 & H) continue;
-            const ulonglong2 w = c.etw[(1 << S) + (j1 >> (SH::LOGC - S)) - 1];
-#pragma unroll
-            for (int col = 0; col < COLS; col++) ct_bfly(x[col * C + j1], x[col * C + j1 + H], w.x, w.y, c.q);
-        }
-        cross_fwd<SH, S + 1>(x, c);
-    }
-}
-
-// First column j2 of the thread's column group cg (W adjacent columns).
-template <class SH>
-__device__ __forceinline__ int col_j2(int cg, int t, int r) {
-    return r * (SH::M / SH::C) + Cols<SH>::W * (cg * SH::T + t);
-}
-
-// Column-group access: residues (j1, j2 .. j2 + W - 1) <-> x[(W cg + h) C + j1].
-template <class SH>
-__device__ __forceinline__ void col_get(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
-    if constexpr (Cols<SH>::W == 2) {
-        const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(p);
-        x[(2 * cg) * SH::C + j1] = v.x;
-        x[(2 * cg + 1) * SH::C + j1] = v.y;
-    } else {
-        x[cg * SH::C + j1] = *p;
-    }
-}
-template <class SH>
-__device__ __forceinline__ void col_get_cs(uint64_t (&x)[SH::E], int cg, int j1, const uint64_t *p) {
-    if constexpr (Cols<SH>::W == 2) {
-        const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(p));
-        x[(2 * cg) * SH::C + j1] = v.x;
-        x[(2 * cg + 1) * SH::C + j1] = v.y;
-    } else {
-        x[cg * SH::C + j1] = __ldcs(p);
-    }
-}
-template <class SH>
-__device__ __forceinline__ void col_put(const uint64_t (&x)[SH::E], int cg, int j1, uint64_t *p) {
-    if constexpr (Cols<SH>::W == 2)
-        *reinterpret_cast<ulonglong2 *>(p) = make_ulonglong2(x[(2 * cg) * SH::C + j1], x[(2 * cg + 1) * SH::C + j1]);
-    else
-        *p = x[cg * SH::C + j1];
-}
-
 template <class SH, int PI>
 __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, const Ctx &c) {
     constexpr int LOGE = SH::LOGE;
@@ -412,8 +299,8 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
     }
 }
 
-// Row (batch item b, limb l) of this CTA's cluster.  Clusters are numbered
-// limb-major (all batch items of limb 0, then of limb 1, ...), so the CTAs
+// Row (batch item b, limb l) of this CTA's group of C blocks.  Rows are
+// numbered limb-major (all batch items of limb 0, then of limb 1, ...), so the CTAs
 // resident at one time share a few primes' twiddle tables and a table is
 // fetched from DRAM about once per launch however long the chain is.
 template <int LOGC>
@@ -438,22 +325,17 @@ __device__ __forceinline__ void etw_issue_pass(ulonglong2 *etw, const ulonglong2
     }
 }
 
-template <class SH>
-__device__ __forceinline__ void etw_issue(ulonglong2 *etw, const ulonglong2 *tw, int r, int t) {
-    for (int u = t; u < SH::C - 1; u += SH::T) cp_async16(etw + u, tw + 1 + u);
-    etw_issue_pass<SH, 0>(etw, tw, r, t);
-    cp_async_commit();
-}
-
+// One CTA per row (C = 1): every stage is local.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
-          const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__) {
+          const uint64_t *__restrict__ consts) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    static_assert(SH::C == 1, "a row of more than one block takes the split kernels");
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
     c.t = threadIdx.x;
-    c.r = SH::C > 1 ? (int)(blockIdx.x & (SH::C - 1)) : 0;
+    c.r = 0;
     int l;
     const long row = row_of<LOGC>(L, batch, l);
     uint64_t *data = res + row * SH::N;
@@ -462,49 +344,13 @@ k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
     c.q = c.kc[K_Q];
     ulonglong2 *etw = reinterpret_cast<ulonglong2 *>(sm + SH::M);
     c.etw = etw;
-    etw_issue<SH>(etw, c.tw, c.r, c.t);
+    etw_issue_pass<SH, 0>(etw, c.tw, c.r, c.t);
+    cp_async_commit();
     uint64_t x[SH::E];
-    if constexpr (SH::C > 1) {
-        constexpr int C = SH::C;
-        if constexpr (!FHE_XCHG_L2) cluster_arrive_relaxed();
-#pragma unroll
-        for (int cg = 0; cg < Cols<SH>::NG; cg++) {
-            const int j2 = col_j2<SH>(cg, c.t, c.r);
-#pragma unroll
-            for (int j1 = 0; j1 < C; j1++) col_get_cs<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
-        }
-        cp_async_wait_all();
-        __syncthreads();   // the staged twiddles are visible to every thread
-        cross_fwd<SH, 0>(x, c);
-        if constexpr (FHE_XCHG_L2) {
-#pragma unroll
-            for (int cg = 0; cg < Cols<SH>::NG; cg++) {
-                const int j2 = col_j2<SH>(cg, c.t, c.r);
-#pragma unroll
-                for (int j1 = 0; j1 < C; j1++) col_put_cg<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
-            }
-            cluster_arrive();   // release: this CTA's columns are in L2
-            cluster_wait();     // acquire: every CTA's columns are
-            global_load_cg<SH, (SH::P - 1) * LOGE, SH::EREM>(x, data + (long)c.r * SH::M, c.t);
-        } else {
-            cluster_wait();   // every CTA of the cluster has started: DSMEM is live
-            cg::cluster_group cl = cg::this_cluster();
-#pragma unroll
-            for (int j1 = 0; j1 < C; j1++) {
-                uint64_t *dst = cl.map_shared_rank(sm, (unsigned)j1);
-#pragma unroll
-                for (int cg = 0; cg < Cols<SH>::NG; cg++) col_put<SH>(x, cg, j1, dst + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
-            }
-            cluster_arrive();
-            cluster_wait();
-            smem_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, sm, c.t);
-        }
-    } else {
-        global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, data, c.t);
-        cp_async_wait_all();
-        __syncthreads();   // the staged twiddles are visible to every thread
-    }
-    fwd_passes<SH, 0>(x, sm, data + (long)c.r * SH::M, c);
+    global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, data, c.t);
+    cp_async_wait_all();
+    __syncthreads();   // the staged twiddles are visible to every thread
+    fwd_passes<SH, 0>(x, sm, data, c);
 }
 
 // ------------------------------------------------------- split forward --
@@ -585,7 +431,7 @@ k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
 
 // The local stages of a split shape: CTA r of a row transforms block r
 // (residues [r M, (r + 1) M)) on its own, with the same passes, twiddle
-// staging and coalesced store as a cluster CTA after its exchange.
+// staging and coalesced store as the one-CTA kernel.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
@@ -679,34 +525,6 @@ __device__ __forceinline__ void inv_compute(uint64_t (&x)[SH::E], const Ctx &c) 
     }
 }
 
-// Cross-CTA stages: span M 2^S, pairs (j1, j1 + 2^S) of every column,
-// twiddle inv[M (2^S + (j1 mod 2^S)) + j2].
-template <class SH, int S>
-__device__ __forceinline__ void cross_inv(uint64_t (&x)[SH::E], const Ctx &c) {
-    if constexpr (S < SH::LOGC) {
-        constexpr int C = SH::C, H = 1 << S;
-#pragma unroll
-        for (int cg = 0; cg < Cols<SH>::NG; cg++) {
-            const int j2 = col_j2<SH>(cg, c.t, c.r);
-#pragma unroll
-            for (int jlo = 0; jlo < H; jlo++) {
-                const ulonglong2 *tw = c.tw + (long)SH::M * (H + jlo) + j2;
-#pragma unroll
-                for (int h = 0; h < Cols<SH>::W; h++) {
-                    const ulonglong2 w = __ldg(tw + h);
-                    const int col = Cols<SH>::W * cg + h;
-#pragma unroll
-                    for (int jhi = 0; jhi < C / (2 * H); jhi++) {
-                        const int j1 = jhi * 2 * H + jlo;
-                        ct_bfly(x[col * C + j1], x[col * C + j1 + H], w.x, w.y, c.q);
-                    }
-                }
-            }
-        }
-        cross_inv<SH, S + 1>(x, c);
-    }
-}
-
 // x <- x * n^-1 psi^-p mod q, fully reduced (x < 2^57 on entry)
 __device__ __forceinline__ uint64_t twist(uint64_t x, ulonglong2 t, uint64_t q) {
     return reduce4(shoup_lazy(x, t.x, t.y, q), q);
@@ -715,8 +533,8 @@ __device__ __forceinline__ uint64_t twist(uint64_t x, ulonglong2 t, uint64_t q) 
 // BLK: a split shape's block kernel -- the local passes only; the block is
 // stored back in place unreduced for the column kernel (k_ntt_inv_cols).
 template <class SH, int PI, bool BLK = false>
-__device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, uint64_t *data,
-                                           const ulonglong2 *tws, const Ctx &c) {
+__device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, const ulonglong2 *tws,
+                                           const Ctx &c) {
     constexpr int LOGE = SH::LOGE;
     constexpr int B = PI * LOGE;
     constexpr int EP = PI == SH::P - 1 ? SH::EREM : LOGE;
@@ -726,10 +544,11 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         __syncthreads();
         constexpr int EP2 = PI + 1 == SH::P - 1 ? SH::EREM : LOGE;
         smem_load<SH, B + LOGE, EP2>(x, sm, c.t);
-        inv_passes<SH, PI + 1, BLK>(x, sm, blk, data, tws, c);
+        inv_passes<SH, PI + 1, BLK>(x, sm, blk, tws, c);
     } else if constexpr (BLK) {
         global_store<SH, B, EP>(x, blk, c.t);   // pass B holds bits >= B: coalesced
-    } else if constexpr (SH::C == 1) {
+    } else {
+        static_assert(SH::C == 1, "a row of more than one block takes the split kernels");
         constexpr int G = SH::E >> EP, EPN = 1 << EP;
 #pragma unroll
         for (int k = 0; k < G; k++) {
@@ -738,71 +557,20 @@ __device__ __forceinline__ void inv_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
             for (int j = 0; j < EPN; j++) x[k * EPN + j] = twist(x[k * EPN + j], __ldg(tws + pass_pos<B, EP>(g, j)), c.q);
         }
         global_store<SH, B, EP>(x, blk, c.t);
-    } else {
-        constexpr int C = SH::C;
-        if constexpr (FHE_XCHG_L2) {
-            // this CTA's block of the row, in place; pass B holds bits >= B: coalesced
-            constexpr int G = SH::E >> EP, EPN = 1 << EP;
-#pragma unroll
-            for (int k = 0; k < G; k++) {
-                const int g = c.t + SH::T * k;
-#pragma unroll
-                for (int j = 0; j < EPN; j++) __stcg(blk + pass_pos<B, EP>(g, j), x[k * EPN + j]);
-            }
-            cluster_arrive();   // release: this block is in L2
-            cluster_wait();     // acquire: every block is
-#pragma unroll
-            for (int cg = 0; cg < Cols<SH>::NG; cg++) {
-                const int j2 = col_j2<SH>(cg, c.t, c.r);
-#pragma unroll
-                for (int j1 = 0; j1 < C; j1++) col_get_cg<SH>(x, cg, j1, data + (long)j1 * SH::M + j2);
-            }
-        } else {
-            smem_store<SH, B, EP>(x, sm, c.t);
-            cluster_arrive();
-            cluster_wait();
-            cg::cluster_group cl = cg::this_cluster();
-#pragma unroll
-            for (int j1 = 0; j1 < C; j1++) {
-                const uint64_t *src = cl.map_shared_rank(sm, (unsigned)j1);
-#pragma unroll
-                for (int cg = 0; cg < Cols<SH>::NG; cg++) col_get<SH>(x, cg, j1, src + swz<LOGE>(col_j2<SH>(cg, c.t, c.r)));
-            }
-        }
-        cross_inv<SH, 0>(x, c);
-#pragma unroll
-        for (int cg = 0; cg < Cols<SH>::NG; cg++) {
-            const int j2 = col_j2<SH>(cg, c.t, c.r);
-#pragma unroll
-            for (int j1 = 0; j1 < C; j1++) {
-                const long p = (long)j1 * SH::M + j2;
-#pragma unroll
-                for (int h = 0; h < Cols<SH>::W; h++) {
-                    const int col = Cols<SH>::W * cg + h;
-                    x[col * C + j1] = twist(x[col * C + j1], __ldg(tws + p + h), c.q);
-                }
-                if constexpr (Cols<SH>::W == 2)
-                    __stcs(reinterpret_cast<ulonglong2 *>(data + p), make_ulonglong2(x[(2 * cg) * C + j1], x[(2 * cg + 1) * C + j1]));
-                else
-                    __stcs(data + p, x[cg * C + j1]);
-            }
-        }
-        if constexpr (!FHE_XCHG_L2) {
-            cluster_arrive();   // keep this CTA's shared memory alive until every peer has read it
-            cluster_wait();
-        }
     }
 }
 
+// One CTA per row (C = 1): every stage is local, then the twist.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
           const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__ twist_tab) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    static_assert(SH::C == 1, "a row of more than one block takes the split kernels");
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
     c.t = threadIdx.x;
-    c.r = SH::C > 1 ? (int)(blockIdx.x & (SH::C - 1)) : 0;
+    c.r = 0;
     int l;
     const long row = row_of<LOGC>(L, batch, l);
     uint64_t *data = res + row * SH::N;
@@ -814,26 +582,25 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
     for (int u = 1 + c.t; u < SH::INV_TW; u += SH::T) cp_async16(etw + u, c.tw + u);
     cp_async_commit();
     uint64_t x[SH::E];
-    uint64_t *blk = data + (long)c.r * SH::M;
     constexpr int EP0 = SH::P == 1 ? SH::EREM : LOGE;
     if constexpr (SH::E >= 2) {
-        block_load_coalesced<SH>(sm, blk, c.t);
+        block_load_coalesced<SH>(sm, data, c.t);
         cp_async_wait_all();
         __syncthreads();   // the block and the staged twiddles are visible to every thread
         smem_load<SH, 0, EP0>(x, sm, c.t);
     } else {
-        global_load<SH, 0, EP0>(x, blk, c.t);
+        global_load<SH, 0, EP0>(x, data, c.t);
         cp_async_wait_all();
         __syncthreads();
     }
-    inv_passes<SH, 0>(x, sm, blk, data, twist_tab + (long)l * SH::N, c);   // indexed by global position
+    inv_passes<SH, 0>(x, sm, data, twist_tab + (long)l * SH::N, c);
 }
 
 // ------------------------------------------------------- split inverse --
 //
 // The local stages of a split shape: CTA r of a row runs spans 1 .. M/2 on
-// block r alone (the same passes and staged twiddles as a cluster CTA before
-// its exchange) and stores the block in place, unreduced.
+// block r alone (the same passes and staged twiddles as the one-CTA kernel)
+// and stores the block in place, unreduced.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
@@ -859,7 +626,7 @@ k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__
     cp_async_wait_all();
     __syncthreads();   // the block and the staged twiddles are visible to every thread
     smem_load<SH, 0, SH::P == 1 ? SH::EREM : LOGE>(x, sm, c.t);
-    inv_passes<SH, 0, true>(x, sm, blk, nullptr, nullptr, c);
+    inv_passes<SH, 0, true>(x, sm, blk, nullptr, c);
 }
 
 // The cross stages of a split inverse and the twist, over whole columns.
@@ -945,41 +712,30 @@ k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
 
 // ---------------------------------------------------------------- launch --
 
+// One CTA per row (C = 1).
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, bool INVERSE>
 int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
-    void (*kern)(uint64_t *, int, int, const ulonglong2 *, const uint64_t *, const ulonglong2 *);
-    if constexpr (INVERSE) kern = k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB>;
-    else kern = k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
-    const size_t smem = (size_t)SH::smem_words(INVERSE) * sizeof(uint64_t);
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return -1;
-    }
-    if (SH::C > 8) {   // clusters of 16 CTAs are a non-portable size
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return -1;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows * SH::C));
-    cfg.blockDim = dim3(SH::T);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = SH::C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    // let the hardware balance a cluster's CTAs over the SMs (measured 6 %
-    // faster for the clusters of 16 at n = 2^17, neutral for clusters of 8)
-    attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
-    attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
-    cfg.attrs = attr;
-    cfg.numAttrs = SH::C > 1 ? 2 : 0;
-    const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(INVERSE ? t->inv : t->fwd);
-    const ulonglong2 *twist_tab = reinterpret_cast<const ulonglong2 *>(t->twist);
+    static_assert(SH::C == 1, "a row of more than one block takes the split kernels");
     if (rows % L) return -1;
-    if (cudaLaunchKernelEx(&cfg, kern, res, L, (int)(rows / L), tw, t->consts, twist_tab) != cudaSuccess) return -1;
-    return 1;
+    const int batch = (int)(rows / L);
+    const size_t smem = (size_t)SH::smem_words(INVERSE) * sizeof(uint64_t);
+    if constexpr (INVERSE) {
+        auto kern = k_ntt_inv<LOGN, LOGC, LOGT, LOGE, MINB>;
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        kern<<<(unsigned)rows, SH::T, smem, st>>>(res, L, batch, reinterpret_cast<const ulonglong2 *>(t->inv),
+                                                  t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
+    } else {
+        auto kern = k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        kern<<<(unsigned)rows, SH::T, smem, st>>>(res, L, batch, reinterpret_cast<const ulonglong2 *>(t->fwd),
+                                                  t->consts);
+    }
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
 // Split forward: the column kernel (first LOGC stages), then one CTA per block.

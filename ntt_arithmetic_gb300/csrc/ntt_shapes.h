@@ -6,17 +6,20 @@
 // Forward launch shape per log2(n): the number of blocks a row is cut into
 // (log2 C), threads per CTA (log2 T), residues per thread (log2 E, = radix of
 // a register pass), the minimum number of resident CTAs per SM the register
-// allocation must allow, and how the C blocks of a row meet:
-//   0 -- one thread-block cluster of C CTAs (C = 1: one CTA per row);
+// allocation must allow, and the kernel structure:
+//   0 -- one CTA per row (log2 C = 0), every stage in one kernel;
 //   1 -- split: a column kernel runs the first log2 C stages over the whole
 //        row, then C independent CTAs run the remaining stages on one block
-//        each (no cluster; measured 8 % faster at n = 2^16, 20 % at 2^17).
-//        At n = 2^16 blocks of 1024 residues (C = 64, 64 threads, 8 CTAs per
-//        SM) beat blocks of 2048 (C = 32, 128 threads, 4 CTAs): 245 against
-//        250 us forward, 234 against 237 us inverse on 384 rows; blocks of
-//        4096 (256 threads) or 8 residues per thread were 8 % slower.  The
-//        same 1024-residue blocks at n = 2^14 (C = 16): 249 against 257 us
-//        with C = 8 (201 MB of residues).
+//        each.
+// Measured on GB300 (201 MB of residues): the split beat a thread-block
+// cluster of C CTAs per row exchanging through L2 by 8 % at n = 2^16 and 20 %
+// at 2^17.  Blocks of 1024 residues (64 threads x 16, 8 CTAs per SM) beat
+// blocks of 2048 at n = 2^16 (245 against 250 us forward, 234 against 237 us
+// inverse on 384 rows), at 2^15 (248 against 253 / 230 against 234 us) and at
+// 2^14 (249 against 257 us forward); blocks of 4096 (256 threads) or 8
+// residues per thread were 8 % slower.  At 2^17 blocks of 1024 would need 127
+// staged twiddle rows per inverse column CTA (65 KB), so it keeps blocks of
+// 2048.
 // The inverse shapes (FHE_INV_SHAPE_n) have the same five fields; a split
 // inverse runs the block CTAs first (the local stages) and the column kernel
 // last (the last log2 C stages and the twist n^-1 psi^-j).
@@ -43,7 +46,7 @@
 #define FHE_SHAPE_14 4, 6, 4, 8, 1
 #endif
 #ifndef FHE_SHAPE_15
-#define FHE_SHAPE_15 2, 8, 5, 2, 0
+#define FHE_SHAPE_15 5, 6, 4, 8, 1
 #endif
 #ifndef FHE_SHAPE_16
 #define FHE_SHAPE_16 6, 6, 4, 8, 1
@@ -52,10 +55,9 @@
 #define FHE_SHAPE_17 6, 7, 4, 4, 1
 #endif
 
-// Inverse shapes: split for n = 2^16 and 2^17 (measured on 201 MB of
-// residues: 247 against 263 us at 2^16, 259 against 338 us at 2^17), clusters
-// of 2^LOGC CTAs for 2^14 (229 against 234 us split) and 2^15, one CTA per
-// row below.
+// Inverse shapes: split from n = 2^14 (measured against cluster shapes: 247
+// against 263 us at 2^16, 259 against 338 us at 2^17, 227 against 229 us at
+// 2^14, 230 against 234 us at 2^15), one CTA per row below.
 #define FHE_INV_SHAPE_1 0, 0, 1, 1, 0
 #define FHE_INV_SHAPE_2 0, 0, 2, 1, 0
 #define FHE_INV_SHAPE_3 0, 0, 3, 1, 0
@@ -70,10 +72,10 @@
 #define FHE_INV_SHAPE_12 0, 8, 4, 2, 0
 #define FHE_INV_SHAPE_13 0, 8, 5, 2, 0
 #ifndef FHE_INV_SHAPE_14
-#define FHE_INV_SHAPE_14 1, 8, 5, 2, 0
+#define FHE_INV_SHAPE_14 4, 6, 4, 8, 1
 #endif
 #ifndef FHE_INV_SHAPE_15
-#define FHE_INV_SHAPE_15 2, 8, 5, 2, 0
+#define FHE_INV_SHAPE_15 5, 6, 4, 8, 1
 #endif
 #ifndef FHE_INV_SHAPE_16
 #define FHE_INV_SHAPE_16 6, 6, 4, 8, 1
