@@ -135,11 +135,15 @@ int fhe_ntt_fwd_table_slot(int log_n, uint32_t k, uint32_t *slot);
  * under every CKKS multiplication, relinearisation and rotation in the
  * kestrel-llm chain (lpnh.cn news 2512365, section 3, vllm_ntt.c) and
  * FHElium's "power-of-two-radix NTT" family ("Eager, Compile, and native
- * execution", table "Native operator families"). */
+ * execution", table "Native operator families").  Launches on `stream`, no
+ * host sync: one kernel for n <= 2^13, two for n >= 2^14 (a kernel over
+ * strided columns for the first stages, then one over contiguous blocks). */
 int fhe_ntt_fwd(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream);
 
 /* In-place exact inverse of fhe_ntt_fwd, including the 1/n factor:
- * bit-reversed evaluations in, natural-order coefficients out. */
+ * bit-reversed evaluations in, natural-order coefficients out.  Launches as
+ * fhe_ntt_fwd does, in the mirror order for n >= 2^14 (blocks, then
+ * columns). */
 int fhe_ntt_inv(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables *t, void *stream);
 
 /* Measurement aid with no counterpart on the pages: the throughput ceiling of
