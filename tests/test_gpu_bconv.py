@@ -117,7 +117,7 @@ def _hoisted_case(g, log_n, L, K, dnum, batch, ks, approx, seed):
 
 
 @pytest.mark.parametrize("log_n,L,K,dnum,batch,R", [(12, 8, 4, 2, 2, 4), (11, 24, 2, 24, 1, 3), (6, 3, 2, 3, 2, 64),
-                                                    (1, 2, 1, 2, 2, 2), (13, 10, 3, 4, 3, 5)])
+                                                    (1, 2, 1, 2, 2, 2), (13, 10, 3, 4, 3, 5), (10, 4, 2, 1, 2, 3)])
 @pytest.mark.parametrize("approx", [False, True])
 def test_hoisted_vs_oracle(g, log_n, L, K, dnum, batch, R, approx):
     two_n = 2 << log_n
