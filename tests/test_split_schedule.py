@@ -1,19 +1,22 @@
-"""Host-side check of the split NTT's column-kernel schedules (no GPU).
+"""Host-side check of the split NTT's kernel schedules (no GPU).
 
-For every split shape in csrc/ntt_shapes.h (n >= 2^14), the forward column
-kernel's stages -- which thread slot holds which column element, in which
-order the stages run, the shared-memory exchange between the two thread
-layouts and the twiddle index of every butterfly -- are replayed here in
-exact modular arithmetic over all columns at once, at the production n; the
-remaining (block-local) stages are applied by their textbook definition.
-The result must equal the oracle's NTT.  The inverse is checked the same
-way: textbook block-local stages, then the inverse column kernel's schedule
-and its twist, against the oracle's INTT.
-
-This pins the index arithmetic that the GPU parity tests exercise only
-through the compiled kernels: a wrong twiddle index or a stage run on the
-wrong layout fails here without a GPU.
+For every split shape in csrc/ntt_shapes.h (n >= 2^14) the forward and the
+inverse are replayed here at the production n, in exact modular arithmetic,
+following the kernels' own index arithmetic:
+- the column kernels: which thread slot holds which column element, the
+  order of the stages, the shared-memory exchange between the two thread
+  layouts and the twiddle index of every butterfly;
+- the block kernels: the register passes (the positions a thread holds in
+  each pass), the stages inside a pass, the twiddles staged in shared memory
+  and the last pass's reads from the permuted table slots.
+The twiddles come from the table blob that the library's host builder writes
+(fhe_ntt_tables_build_host), so the replay also checks the table layout the
+kernels rely on.  The results must equal the oracle's NTT and INTT.  A
+wrong twiddle index, a stage on the wrong layout or a mismatch between the
+table's slot order and the last pass's reads fails here without a GPU; the
+shorter replays by textbook definition stay as a second reference.
 """
+import ctypes
 import os
 import random
 import re
@@ -22,19 +25,22 @@ import numpy as np
 import pytest
 
 import oracle
+from ntt_arithmetic_gb300 import _native as N
+from ntt_arithmetic_gb300 import build as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SHAPES_H = os.path.join(ROOT, "ntt_arithmetic_gb300", "csrc", "ntt_shapes.h")
 
 
-def split_shapes(prefix: str):
-    """(log_n, log_c) of every split shape named FHE_<prefix>SHAPE_<n>."""
+def split_shapes(prefix: str, full: bool = False):
+    """(log_n, log_c) -- with full=True (log_n, log_c, log_t, log_e) -- of every
+    split shape named FHE_<prefix>SHAPE_<n>."""
     text = open(SHAPES_H).read()
     out = []
     for m in re.finditer(r"#define FHE_%sSHAPE_(\d+) (\d+), (\d+), (\d+), (\d+), (\d+)" % prefix, text):
-        log_n, logc, split = int(m.group(1)), int(m.group(2)), int(m.group(6))
+        log_n, logc, logt, loge, split = (int(m.group(i)) for i in (1, 2, 3, 4, 6))
         if split:
-            out.append((log_n, logc))
+            out.append((log_n, logc, logt, loge) if full else (log_n, logc))
     return sorted(set(out))
 
 
@@ -201,6 +207,138 @@ def test_inverse_column_schedule(log_n, logc):
     y = np.array([rng.randrange(q) for _ in range(n)], dtype=np.uint64)
     inv, twist = inv_tables(q, psi, log_n)
     row = inv_local(np.array([int(v) for v in y], dtype=object), q, inv, log_n, logc)
+    out = np.concatenate(inv_columns(col(row, log_n, logc), q, inv, twist, log_n, logc))
+    want = oracle.intt(y, q, psi)
+    assert [int(v) for v in out] == [int(v) for v in want]
+
+
+# ------------------------------------------------- block kernels, library tables --
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.lib()
+
+
+def library_tables(lib, log_n: int, q: int):
+    """The forward table by slot, the inverse table and the twist table (values only) of
+    the blob the library builds on the host for one prime."""
+    n = 1 << log_n
+    nb = ctypes.c_size_t()
+    assert lib.fhe_ntt_tables_bytes(log_n, 1, ctypes.byref(nb)) == 0
+    blob = np.zeros(nb.value, dtype=np.uint8)
+    arr = (ctypes.c_uint64 * 1)(q)
+    assert lib.fhe_ntt_tables_build_host(log_n, 1, arr, blob.ctypes.data_as(ctypes.c_void_p), nb.value) == 0
+    t = N.NttTables()
+    base = blob.ctypes.data
+    assert lib.fhe_ntt_tables_bind(ctypes.c_void_p(base), nb.value, log_n, 1, ctypes.byref(t)) == 0
+    pairs = lambda ptr: np.frombuffer(blob, dtype=np.uint64, count=2 * n, offset=ptr - base).reshape(n, 2)  # noqa: E731
+    vals = lambda ptr: [int(v) for v in pairs(ptr)[:, 0]]  # noqa: E731
+    return vals(t.fwd), vals(t.inv), vals(t.twist)
+
+
+def pass_pos(g, j, b, ep):
+    """Position in the block of the j-th residue of thread group g in a pass over bits [b, b + ep)."""
+    return (g & ((1 << b) - 1)) | (j << b) | ((g >> b) << (b + ep))
+
+
+def fwd_block(blk, r, q, fwd_slots, log_n, logc, logt, loge):
+    """k_ntt_fwd_blk on block r: passes from the high bits down; the first pass's
+    twiddles are common to all groups, the middle passes' come from the staged
+    copy of the table, the last pass reads the permuted slots (r, jj, g)."""
+    logm = log_n - logc
+    t_, e_ = 1 << logt, 1 << loge
+    p_ = (logm + loge - 1) // loge
+    erem = logm - (p_ - 1) * loge
+    th = np.arange(t_)
+    for pi in range(p_):
+        b = (p_ - 1 - pi) * loge
+        ep = erem if pi == 0 else loge
+        g_, epn = e_ >> ep, 1 << ep
+        pos = {(k, j): pass_pos(th + t_ * k, j, b, ep) for k in range(g_) for j in range(epn)}
+        x = {kj: blk[p] for kj, p in pos.items()}
+        for i in range(ep):
+            s_ = log_n - b - ep + i
+            half, nw = 1 << (ep - 1 - i), 1 << i
+            for k in range(g_):
+                g = th + t_ * k
+                for jj in range(nw):
+                    if b + ep == logm and g_ > 1:
+                        w = fwd_slots[(1 << s_) + (r << i) + jj]
+                    elif b == 0:
+                        idx = (1 << s_) + (r << (logm - ep + i)) + (jj << (logm - ep)) + g
+                        w = np.array([fwd_slots[v] for v in idx], dtype=object)
+                    else:
+                        idx = (1 << s_) + (r << (logm - b - ep + i)) + ((g >> b) << i) + jj
+                        w = np.array([fwd_slots[v] for v in idx], dtype=object)
+                    for u in range(half):
+                        j = jj * 2 * half + u
+                        tt = x[(k, j + half)] * w % q
+                        x[(k, j)], x[(k, j + half)] = (x[(k, j)] + tt) % q, (x[(k, j)] - tt) % q
+        for kj, p in pos.items():
+            blk[p] = x[kj]
+    return blk
+
+
+def inv_block(blk, q, inv, logm, logt, loge):
+    """k_ntt_inv_blk on one block: passes from the low bits up; in the first pass the
+    twiddle-1 butterflies, elsewhere inv[2^(B+I) + (g mod 2^B) + (jl << B)]."""
+    t_, e_ = 1 << logt, 1 << loge
+    p_ = (logm + loge - 1) // loge
+    erem = logm - (p_ - 1) * loge
+    th = np.arange(t_)
+    for pi in range(p_):
+        b = pi * loge
+        ep = erem if pi == p_ - 1 else loge
+        g_, epn = e_ >> ep, 1 << ep
+        pos = {(k, j): pass_pos(th + t_ * k, j, b, ep) for k in range(g_) for j in range(epn)}
+        x = {kj: blk[p] for kj, p in pos.items()}
+        for i in range(ep):
+            kb, half = b + i, 1 << i
+            nh = epn // (2 * half)
+            for k in range(g_):
+                gl = (th + t_ * k) & ((1 << b) - 1)
+                for jl in range(half):
+                    if b == 0 and jl == 0:
+                        w = 1
+                    else:
+                        w = np.array([inv[v] for v in (1 << kb) + gl + (jl << b)], dtype=object)
+                    for jh in range(nh):
+                        j = jh * 2 * half + jl
+                        tt = x[(k, j + half)] * w % q
+                        x[(k, j)], x[(k, j + half)] = (x[(k, j)] + tt) % q, (x[(k, j)] - tt) % q
+        for kj, p in pos.items():
+            blk[p] = x[kj]
+    return blk
+
+
+@pytest.mark.parametrize("log_n,logc,logt,loge", split_shapes("", full=True))
+def test_forward_kernels_with_library_tables(lib, log_n, logc, logt, loge):
+    n, m = 1 << log_n, 1 << (log_n - logc)
+    q = int(oracle.primes(2 * n, 1)[0])
+    psi = oracle.psi(q, 2 * n)
+    fwd_slots, _, _ = library_tables(lib, log_n, q)
+    rng = random.Random(log_n * 1000 + logc)
+    x = np.array([rng.randrange(q) for _ in range(n)], dtype=np.uint64)
+    # the column kernel's stages read slots 2^s + block directly (identity below the last pass)
+    row = np.concatenate(fwd_columns(col(x, log_n, logc), q, fwd_slots, logc))
+    for r in range(1 << logc):
+        row[r * m:(r + 1) * m] = fwd_block(row[r * m:(r + 1) * m].copy(), r, q, fwd_slots, log_n, logc, logt, loge)
+    want = oracle.ntt(x, q, psi)
+    assert [int(v) for v in row] == [int(v) for v in want]
+
+
+@pytest.mark.parametrize("log_n,logc,logt,loge", split_shapes("INV_", full=True))
+def test_inverse_kernels_with_library_tables(lib, log_n, logc, logt, loge):
+    n, m = 1 << log_n, 1 << (log_n - logc)
+    q = int(oracle.primes(2 * n, 1)[0])
+    psi = oracle.psi(q, 2 * n)
+    _, inv, twist = library_tables(lib, log_n, q)
+    rng = random.Random(log_n * 1000 + logc + 7)
+    y = np.array([rng.randrange(q) for _ in range(n)], dtype=np.uint64)
+    row = np.array([int(v) for v in y], dtype=object)
+    for r in range(1 << logc):
+        row[r * m:(r + 1) * m] = inv_block(row[r * m:(r + 1) * m].copy(), q, inv, log_n - logc, logt, loge)
     out = np.concatenate(inv_columns(col(row, log_n, logc), q, inv, twist, log_n, logc))
     want = oracle.intt(y, q, psi)
     assert [int(v) for v in out] == [int(v) for v in want]
