@@ -1,8 +1,9 @@
-"""Host-side check of the split NTT's kernel schedules (no GPU).
+"""Host-side check of the NTT kernels' schedules (no GPU).
 
-For every split shape in csrc/ntt_shapes.h (n >= 2^14) the forward and the
-inverse are replayed here at the production n, in exact modular arithmetic,
-following the kernels' own index arithmetic:
+For every shape in csrc/ntt_shapes.h -- the split shapes (n >= 2^14) and the
+one-CTA-per-row shapes (n <= 2^13) -- the forward and the inverse are
+replayed here at the production n, in exact modular arithmetic, following the
+kernels' own index arithmetic:
 - the column kernels: which thread slot holds which column element, the
   order of the stages, the shared-memory exchange between the two thread
   layouts and the twiddle index of every butterfly;
@@ -342,3 +343,42 @@ def test_inverse_kernels_with_library_tables(lib, log_n, logc, logt, loge):
     out = np.concatenate(inv_columns(col(row, log_n, logc), q, inv, twist, log_n, logc))
     want = oracle.intt(y, q, psi)
     assert [int(v) for v in out] == [int(v) for v in want]
+
+
+def one_cta_shapes(prefix: str):
+    """(log_n, log_t, log_e) of every one-CTA-per-row shape named FHE_<prefix>SHAPE_<n>."""
+    text = open(SHAPES_H).read()
+    out = []
+    for m in re.finditer(r"#define FHE_%sSHAPE_(\d+) (\d+), (\d+), (\d+), (\d+), (\d+)" % prefix, text):
+        log_n, logc, logt, loge, split = (int(m.group(i)) for i in (1, 2, 3, 4, 6))
+        if not split:
+            assert logc == 0
+            out.append((log_n, logt, loge))
+    return sorted(set(out))
+
+
+@pytest.mark.parametrize("log_n,logt,loge", one_cta_shapes(""))
+def test_one_cta_forward_with_library_tables(lib, log_n, logt, loge):
+    """k_ntt_fwd (n <= 2^13): the block kernel's passes over the whole row."""
+    n = 1 << log_n
+    q = int(oracle.primes(2 * n, 1)[0])
+    psi = oracle.psi(q, 2 * n)
+    fwd_slots, _, _ = library_tables(lib, log_n, q)
+    rng = random.Random(log_n * 7 + 1)
+    x = np.array([rng.randrange(q) for _ in range(n)], dtype=np.uint64)
+    got = fwd_block(np.array([int(v) for v in x], dtype=object), 0, q, fwd_slots, log_n, 0, logt, loge)
+    assert [int(v) for v in got] == [int(v) for v in oracle.ntt(x, q, psi)]
+
+
+@pytest.mark.parametrize("log_n,logt,loge", one_cta_shapes("INV_"))
+def test_one_cta_inverse_with_library_tables(lib, log_n, logt, loge):
+    """k_ntt_inv (n <= 2^13): the passes over the whole row, then the twist at every position."""
+    n = 1 << log_n
+    q = int(oracle.primes(2 * n, 1)[0])
+    psi = oracle.psi(q, 2 * n)
+    _, inv, twist = library_tables(lib, log_n, q)
+    rng = random.Random(log_n * 7 + 2)
+    y = np.array([rng.randrange(q) for _ in range(n)], dtype=np.uint64)
+    got = inv_block(np.array([int(v) for v in y], dtype=object), q, inv, log_n, logt, loge)
+    got = [int(v) * twist[p] % q for p, v in enumerate(got)]
+    assert got == [int(v) for v in oracle.intt(y, q, psi)]
