@@ -93,7 +93,12 @@ int fhe_root_of_unity(uint64_t q, int log_n, uint64_t *psi);
 /* Device view of a table blob: pointers into one caller-owned device buffer.
  * FHElium passes "schedule and twiddle Tensors" to every NTT call (same page,
  * section "Shared implementation and native path"); this struct is that
- * argument.  Filled by fhe_ntt_tables_bind; treat the fields as opaque. */
+ * argument.  Filled by fhe_ntt_tables_bind; treat the fields as opaque.
+ * Every entry point checks, before any launch, that the struct is exactly
+ * what fhe_ntt_tables_bind writes for `blob` (each array pointer at its
+ * offset inside the blob, `bytes` the layout size); any other struct gives
+ * FHE_EINVAL.  `blob` itself then goes through the device and overlap
+ * checks, so no kernel reads tables outside the caller's device blob. */
 typedef struct fhe_ntt_tables {
     int32_t log_n;            /* tables are for n = 2^log_n */
     int32_t L;                /* number of primes covered */
@@ -378,9 +383,11 @@ int fhe_rescale(uint64_t *out, const uint64_t *in, int log_n, int L, int batch, 
  *     fhe_keyswitch_ip with a caller workspace).
  *   - Allocation: none -- no cudaMalloc, cudaFree or allocating library
  *     routine is called.
- *   - Set-up: the first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Set-up: every call looks up the array's device address
+ *     (cudaGetSymbolAddress, with the operands' device current); nothing is
+ *     cached, so the address stays right after a cudaDeviceReset.  The
+ *     first call on a device also loads the library's device code there:
+ *     make that first call before any stream capture.
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents.  Nothing in it has to start at zero (each call
  *     writes every word it later reads), but calls whose kernels overlap on

@@ -60,10 +60,21 @@ int select_device(std::initializer_list<const void *> ptrs) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+// The struct must be exactly what fhe_ntt_tables_bind writes for its blob:
+// every sub-pointer at its layout offset from `blob` and `bytes` the layout's
+// size.  Only `blob` goes through the device and overlap checks, so a
+// sub-pointer anywhere else (another buffer, host memory) is refused here,
+// before any launch.
 int check_tables(const fhe_ntt_tables *t, int log_n, int L) {
-    if (!t || !t->q || !t->consts || !t->fwd || !t->inv || !t->twist || !t->blob) return FHE_EINVAL;
+    if (!t || !t->blob || !aligned16(t->blob)) return FHE_EINVAL;
+    if (t->log_n < 1 || t->log_n > kMaxLogN || t->L < 1 || t->L > kMaxTableL) return FHE_EINVAL;
     if (t->log_n != log_n || L > t->L) return FHE_EINVAL;
-    if (t->bytes < ntt_layout(t->log_n, t->L).bytes) return FHE_EINVAL;
+    const NttLayout lay = ntt_layout(t->log_n, t->L);
+    const char *base = (const char *)t->blob;
+    if (t->bytes != lay.bytes || (const char *)t->q != base + lay.off_q ||
+        (const char *)t->consts != base + lay.off_consts || (const char *)t->fwd != base + lay.off_fwd ||
+        (const char *)t->inv != base + lay.off_inv || (const char *)t->twist != base + lay.off_twist)
+        return FHE_EINVAL;
     return FHE_OK;
 }
 

@@ -14,12 +14,14 @@
 // The array is a file-scope __device__ variable of kScratchBytes.  Every GPU
 // that loads the library holds it until the process exits.  In host code its
 // name is only a host-side stand-in, not a device address, so it is never
-// passed to a kernel directly: the device address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, and cached.
+// passed to a kernel directly: every call looks the device address up with
+// cudaGetSymbolAddress, with the operands' device current.  The address is
+// not cached, because it belongs to the current context: after a
+// cudaDeviceReset the runtime loads the library's device code again and the
+// array may sit elsewhere.
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "fhe_internal.h"
 
@@ -27,27 +29,19 @@ namespace fhe {
 namespace {
 
 constexpr size_t kScratchBytes = (size_t)16 << 20;   // 16 MiB of extended digits
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint64_t g_ks_scratch[kScratchBytes / sizeof(uint64_t)];
 
-std::mutex g_setup_mutex;
-uint64_t *g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of g_ks_scratch on device `dev` (made current by the caller);
-// looked up on the first call for that device.
-int scratch_for_device(int dev, uint64_t **out) {
-    if (dev < 0 || dev >= kMaxDevices) return FHE_EDEVICE;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_ks_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return FHE_ECUDA;
-        }
-        g_scratch_ptr[dev] = (uint64_t *)p;
+// Device address of g_ks_scratch in the current context (the operands'
+// device, made current by the caller).  The first lookup on a device also
+// loads this library's device code there.
+int scratch_address(uint64_t **out) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ks_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return FHE_ECUDA;
     }
-    *out = g_scratch_ptr[dev];
+    *out = (uint64_t *)p;
     return FHE_OK;
 }
 
@@ -77,7 +71,7 @@ extern "C" int fhe_keyswitch_ip_noalloc(uint64_t *out, const uint64_t *in, size_
     if (cudaGetDevice(&cur) != cudaSuccess) return FHE_ECUDA;
     if (cur != a.device && cudaSetDevice(a.device) != cudaSuccess) return FHE_ECUDA;
     uint64_t *scratch = nullptr;
-    const int r = scratch_for_device(a.device, &scratch);
+    const int r = scratch_address(&scratch);
     if (r != FHE_OK) return r;
     // Same validation, kernels and launch order as the allocating entry point.
     return fhe_keyswitch_ip(out, in, in_stride, keys, log_n, L, K, dnum, batch, t_qp, modup, scratch, kScratchBytes,

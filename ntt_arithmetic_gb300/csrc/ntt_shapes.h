@@ -33,27 +33,13 @@
 #define FHE_SHAPE_8 0, 5, 3, 1, 0
 #define FHE_SHAPE_9 0, 6, 3, 1, 0
 #define FHE_SHAPE_10 0, 7, 3, 1, 0
-#ifndef FHE_SHAPE_11
 #define FHE_SHAPE_11 0, 7, 4, 4, 0
-#endif
-#ifndef FHE_SHAPE_12
 #define FHE_SHAPE_12 0, 8, 4, 2, 0
-#endif
-#ifndef FHE_SHAPE_13
 #define FHE_SHAPE_13 0, 8, 5, 2, 0
-#endif
-#ifndef FHE_SHAPE_14
 #define FHE_SHAPE_14 4, 6, 4, 8, 1
-#endif
-#ifndef FHE_SHAPE_15
 #define FHE_SHAPE_15 5, 6, 4, 8, 1
-#endif
-#ifndef FHE_SHAPE_16
 #define FHE_SHAPE_16 6, 6, 4, 8, 1
-#endif
-#ifndef FHE_SHAPE_17
 #define FHE_SHAPE_17 6, 7, 4, 4, 1
-#endif
 
 // Inverse shapes: split from n = 2^14 (measured against cluster shapes: 247
 // against 263 us at 2^16, 259 against 338 us at 2^17, 227 against 229 us at
@@ -71,18 +57,10 @@
 #define FHE_INV_SHAPE_11 0, 7, 4, 4, 0
 #define FHE_INV_SHAPE_12 0, 8, 4, 2, 0
 #define FHE_INV_SHAPE_13 0, 8, 5, 2, 0
-#ifndef FHE_INV_SHAPE_14
 #define FHE_INV_SHAPE_14 4, 6, 4, 8, 1
-#endif
-#ifndef FHE_INV_SHAPE_15
 #define FHE_INV_SHAPE_15 5, 6, 4, 8, 1
-#endif
-#ifndef FHE_INV_SHAPE_16
 #define FHE_INV_SHAPE_16 6, 6, 4, 8, 1
-#endif
-#ifndef FHE_INV_SHAPE_17
 #define FHE_INV_SHAPE_17 6, 7, 4, 4, 1
-#endif
 
 namespace fhe {
 

@@ -198,3 +198,48 @@ def test_butterfly_probe_validates_on_the_host(lib):
     assert lib.fhe_butterfly_probe(fake, 1, 1, None, None) == N.FHE_EINVAL
     t.log_n = 10                                # the probe reads 2048 table entries
     assert lib.fhe_butterfly_probe(fake, 1, 1, ctypes.byref(t), None) == N.FHE_EINVAL
+
+
+def test_tampered_table_struct_fails_before_launch(lib):
+    """A table struct whose array pointers are not where fhe_ntt_tables_bind
+    put them (another buffer, host memory, a shifted offset) or whose size or
+    shape fields were edited is refused with FHE_EINVAL before anything is
+    launched, so no kernel reads twiddles from outside the caller's blob."""
+    log_n, L = 5, 2
+    nb = ctypes.c_size_t()
+    lib.fhe_ntt_tables_bytes(log_n, L, ctypes.byref(nb))
+    blob = np.zeros(nb.value, dtype=np.uint8)
+    qs = [int(v) for v in oracle.primes(2 << log_n, L)]
+    lib.fhe_ntt_tables_build_host(log_n, L, (ctypes.c_uint64 * L)(*qs), blob.ctypes.data_as(ctypes.c_void_p), nb.value)
+    other = np.zeros(nb.value, dtype=np.uint8)
+    host = np.zeros(4 << log_n, dtype=np.uint64)
+    hp = ctypes.c_void_p(host.ctypes.data)
+    fields = ["q", "consts", "fwd", "inv", "twist"]
+    before = lib.fhe_launch_count()
+    for field in fields + ["bytes", "L", "log_n", "blob"]:
+        for how in ("other", "shift"):
+            t = N.NttTables()
+            assert lib.fhe_ntt_tables_bind(ctypes.c_void_p(blob.ctypes.data), nb.value, log_n, L, ctypes.byref(t)) == 0
+            if field in fields:
+                v = getattr(t, field)
+                setattr(t, field, other.ctypes.data + (v - blob.ctypes.data) if how == "other" else v + 16)
+            elif field == "bytes":
+                t.bytes = t.bytes + 256 if how == "other" else t.bytes - 16
+            elif field == "L":
+                t.L = L + 1 if how == "other" else 0
+            elif field == "log_n":
+                t.log_n = 0 if how == "other" else 18
+            else:
+                t.blob = other.ctypes.data if how == "other" else t.blob + 8
+            ref = ctypes.byref(t)
+            assert lib.fhe_ntt_fwd(hp, log_n, 1, 1, ref, None) == N.FHE_EINVAL, (field, how)
+            assert lib.fhe_ntt_inv(hp, log_n, 1, 1, ref, None) == N.FHE_EINVAL, (field, how)
+            assert lib.fhe_mul_ntt(hp, hp, hp, log_n, 1, 1, ref, None) == N.FHE_EINVAL, (field, how)
+            assert lib.fhe_tensor(hp, hp, hp, log_n, 1, 1, ref, None) == N.FHE_EINVAL, (field, how)
+            assert lib.fhe_automorph(hp, hp, log_n, 1, 1, 3, 1, ref, None) == N.FHE_EINVAL, (field, how)
+            assert lib.fhe_butterfly_probe(hp, 1, 1, ref, None) == N.FHE_EINVAL, (field, how)
+    # the untouched struct passes the table check and stops only at the device check (host memory)
+    t = N.NttTables()
+    assert lib.fhe_ntt_tables_bind(ctypes.c_void_p(blob.ctypes.data), nb.value, log_n, L, ctypes.byref(t)) == 0
+    assert lib.fhe_ntt_fwd(hp, log_n, 1, 1, ctypes.byref(t), None) == N.FHE_EDEVICE
+    assert lib.fhe_launch_count() == before
