@@ -50,8 +50,33 @@ BFLY_PER_CLK_SM = 1.0 / (3 / 25.2 + 2 / 32.0 + 4 / 64.0)
 SMS, SM_MAX_MHZ = 152, 2070.0
 ALU_PEAK_BFLY = SMS * BFLY_PER_CLK_SM * SM_MAX_MHZ * 1e6
 BFLY_PER_FWD = NPOLY * L * (N // 2) * LOG_N
+BFLY_PER_INV = INV_T * (N // 2) * LOG_N
 NTT_BYTES_PER_FWD = 16 * NPOLY * L * N     # read + write every residue once
+NTT_BYTES_PER_INV = 16 * INV_T * N
 KS_MIN_BYTES_X4 = 8 * N * (PAIRS * (L + 2 * (L + K)) + DNUM * 2 * (L + K))   # 285.2 MB
+
+
+def keyswitch_alu_floor_s(pairs: int = PAIRS) -> float:
+    """Seconds the integer multiply pipe needs for `pairs` key switches of the
+    bench shape if it did nothing else: every 32-bit product the arithmetic
+    needs, at the pipe's measured per-SM rates (low 64, high 32, wide 25.2 per
+    clock) on 152 SMs at the maximum clock -- the same derivation as
+    ALU_PEAK_BFLY.  Lazy Shoup product (butterfly, Garner step): 3 wide +
+    2 high + 4 low; multiply-accumulate of 25-bit halves: 3 wide; reduction
+    of a 105-bit sum: 5 wide + 2 high + 3 low.  Per (coefficient, digit):
+    alpha (alpha - 1) / 2 Garner products, then per target outside the digit
+    alpha - 1 multiply-accumulates and one reduction; per output residue of
+    the inner product: 2 dnum multiply-accumulates and 2 reductions."""
+    lo, hi, wide = 1 / 64.0, 1 / 32.0, 1 / 25.2          # SM-cycles per 32-bit product
+    shoup, mac, red = 3 * wide + 2 * hi + 4 * lo, 3 * wide, 5 * wide + 2 * hi + 3 * lo
+    alpha = L // DNUM
+    targets = L + K - alpha
+    bfly = pairs * DNUM * (L + K) * (N // 2) * LOG_N
+    units = pairs * DNUM * N
+    ip = pairs * (L + K) * N
+    cycles = (bfly * shoup + units * (alpha * (alpha - 1) // 2 * shoup + targets * ((alpha - 1) * mac + red))
+              + ip * (2 * DNUM * mac + 2 * red))
+    return cycles / (SMS * SM_MAX_MHZ * 1e6)
 
 
 def peaks():
@@ -423,9 +448,12 @@ def ours(args):
 
     clocks = clock_record(poll, clk)
     hbm, hbm_kind = peaks()
-    fwd_s = kern[0] * 1e-3
+    fwd_s, inv_s, ks_s = kern[0] * 1e-3, kern[4] * 1e-3, kern[5] * 1e-3
     achieved_bfly = BFLY_PER_FWD / fwd_s
+    achieved_inv = BFLY_PER_INV / inv_s
     ceiling = butterfly_ceiling(st, device)   # outside the timed region
+    ks_alu_s = keyswitch_alu_floor_s()
+    ks_hbm_s = KS_MIN_BYTES_X4 / (hbm * 1e9)
     line = {
         "metric": METRIC,
         "value": whole_job_rate(UNITS, ws, ms_max),
@@ -457,9 +485,32 @@ def ours(args):
                      "kernel": "forward NTT call = k_ntt_fwd_cols<16,6,3> (first 6 stages, strided columns) + "
                                "k_ntt_fwd_blk<16,6,6,4,8> (last 10 stages, one CTA per 1024-residue block); "
                                "n=2^16, 384 rows; traffic = both launches",
+                     "peak_kind": "derived: measured integer-pipe rates x 152 SMs x 2070 MHz",
                      "measured_butterfly_ceiling": ceiling / 1e9, "frac_of_measured_ceiling": achieved_bfly / ceiling,
                      "ceiling_note": "fhe_butterfly_probe: the same butterfly register-resident, no memory traffic",
-                     "hbm_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9, "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind},
+                     "hbm_gbs": NTT_BYTES_PER_FWD / fwd_s / 1e9, "hbm_peak_gbs": hbm, "hbm_peak_kind": hbm_kind,
+                     "hbm_frac": NTT_BYTES_PER_FWD / fwd_s / 1e9 / hbm,
+                     "hbm_frac_bound_at_ceiling": NTT_BYTES_PER_FWD / (BFLY_PER_FWD / ceiling) / 1e9 / hbm},
+        "roofline_ntt_inv": {"bound": "alu", "achieved": achieved_inv / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
+                             "unit": "Gbutterfly/s", "frac": achieved_inv / ALU_PEAK_BFLY,
+                             "traffic": kernel_traffic("k_ntt_inv", INV_T), "traffic_unit": "bytes/launch",
+                             "algorithmic_bytes": NTT_BYTES_PER_INV,
+                             "kernel": "inverse NTT call = k_ntt_inv_blk<16,6,6,4,8> (first 10 stages per block) + "
+                                       "k_ntt_inv_cols<16,6,3> (last 6 stages and the twist n^-1 psi^-j); n=2^16, "
+                                       "288 rows; traffic = both launches",
+                             "frac_of_measured_ceiling": achieved_inv / ceiling,
+                             "hbm_gbs": NTT_BYTES_PER_INV / inv_s / 1e9, "hbm_frac": NTT_BYTES_PER_INV / inv_s / 1e9 / hbm,
+                             "poly_prime_per_s": INV_T / inv_s},
+        "roofline_keyswitch": {"bound": "alu" if ks_alu_s >= ks_hbm_s else "hbm",
+                               "achieved": PAIRS / ks_s, "peak": PAIRS / max(ks_alu_s, ks_hbm_s),
+                               "unit": "key switches/s", "frac": max(ks_alu_s, ks_hbm_s) / ks_s,
+                               "alu_floor_ms": ks_alu_s * 1e3, "hbm_floor_ms": ks_hbm_s * 1e3, "measured_ms": ks_s * 1e3,
+                               "frac_alu_at_measured_ceiling": ks_alu_s * (ALU_PEAK_BFLY / ceiling) / ks_s,
+                               "hbm_bytes_min": KS_MIN_BYTES_X4,
+                               "work": "4 key switches of [24][n] over 24 + 8 primes, dnum = 3: ModUp (28 Garner products "
+                                       "+ 24 x (7 multiply-accumulates + 1 reduction) per coefficient and digit), "
+                                       "384 NTT rows, inner product (6 multiply-accumulates + 2 reductions per output "
+                                       "residue); HBM floor: inputs + keys (read once) + outputs"},
         "clocks": clocks,
         "gpu_launches": launches,
         "e2e": {"value": whole_job_rate(UNITS, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms, "steps": args.steps,

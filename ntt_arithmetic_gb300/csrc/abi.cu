@@ -244,6 +244,12 @@ int keyswitch_call(uint64_t *out, const uint64_t *in, size_t in_stride, const ui
                           t_qp, modup, stream)) < 0)
         return finish(-1);
     launched += r;
+    if (R == 0) {
+        // the NTT of the digits fused with the inner product where a fused kernel exists
+        if ((r = launch_ntt_fwd_ip(out, workspace, keys, log_n, LK, dnum, batch, t_qp, stream)) < 0)
+            return finish(-1);
+        if (r > 0) return finish(launched + r);
+    }
     if ((r = launch_ntt(workspace, log_n, LK, (long)batch * dnum * LK, t_qp, false, stream)) < 0) return finish(-1);
     launched += r;
     r = R > 0 ? launch_ks_ip_aut(out, workspace, keys, log_n, LK, dnum, batch, R, g, t_qp, stream)

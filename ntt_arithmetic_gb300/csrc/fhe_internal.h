@@ -85,6 +85,13 @@ int launch_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int
                  const void *bconv, void *stream);
 int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK,
                  int dnum, int batch, const fhe_ntt_tables *t, void *stream);
+// Forward NTT of the extended digits ext [batch][dnum][LK][n] (ModUp output,
+// overwritten by the column stages) fused with the inner product into out
+// [batch][2][LK][n].  Returns 0 without launching when no fused kernel
+// exists for the shape (n < 2^14, dnum > 4): the caller then runs
+// launch_ntt + launch_ks_ip.
+int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,
+                      const fhe_ntt_tables *t, void *stream);
 
 int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, int batch, bool ntt_domain,
                    bool nearest, const fhe_ntt_tables *t_qp, const void *md, uint64_t *ws, void *stream);

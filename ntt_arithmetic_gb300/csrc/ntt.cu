@@ -273,7 +273,9 @@ __device__ __forceinline__ void fwd_compute(uint64_t (&x)[SH::E], const Ctx &c) 
     }
 }
 
-template <class SH, int PI>
+// KEEP: the reduced block is left in shared memory (swizzled) instead of
+// being stored to `blk` (the fused key-switch kernel consumes it there).
+template <class SH, int PI, bool KEEP = false>
 __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, uint64_t *blk, const Ctx &c) {
     constexpr int LOGE = SH::LOGE;
     constexpr int B = (SH::P - 1 - PI) * LOGE;
@@ -284,12 +286,15 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
         __syncthreads();
         constexpr int B2 = (SH::P - 2 - PI) * LOGE;
         smem_load<SH, B2, LOGE>(x, sm, c.t);
-        fwd_passes<SH, PI + 1>(x, sm, blk, c);
+        fwd_passes<SH, PI + 1, KEEP>(x, sm, blk, c);
     } else {
         const uint32_t c58 = (uint32_t)c.kc[K_C58];
 #pragma unroll
         for (int i = 0; i < SH::E; i++) x[i] = reduce_small(x[i], c.q, c58);
-        if constexpr (B == 0 && SH::E >= 2) {
+        if constexpr (KEEP) {
+            static_assert(B == 0, "the fused key switch runs on the split shapes");
+            smem_store<SH, B, EP>(x, sm, c.t);
+        } else if constexpr (B == 0 && SH::E >= 2) {
             smem_store<SH, B, EP>(x, sm, c.t);   // each thread rewrites the positions it read
             __syncthreads();
             block_store_coalesced<SH>(sm, blk, c.t);
@@ -456,6 +461,83 @@ k_ntt_fwd_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__
     cp_async_wait_all();
     __syncthreads();   // the staged twiddles are visible to every thread
     fwd_passes<SH, 0>(x, sm, blk, c);
+}
+
+// The last LOGM stages of the extended digits' forward NTT fused with the
+// key-switch inner product (FHElium, "Eager, Compile, and native
+// execution", section "CUDA execution": "key-switch multiply-accumulate"):
+// CTA (l, r, b) transforms block r of row (b, j, l) for every digit j < DN,
+// keeps the DN reduced blocks in shared memory, then computes
+//   out[b][c][l][p] = sum_j D_j[p] keys[j][c][l][p]  mod q_l   (c = 0, 1)
+// for the block's positions p, with each key word read once per CTA and the
+// output written once: the transformed digits never return to HBM.  The
+// batch index varies fastest over the grid, so the CTAs that read the same
+// key blocks run together and the keys come from DRAM about once per call.
+// Sums are exact multiply-accumulates of 25-bit halves reduced once.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int DN>
+__global__ void __launch_bounds__(1 << LOGT, MINB)
+k_ntt_fwd_blk_ip(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, const uint64_t *__restrict__ keys,
+                 int LK, int batch, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    extern __shared__ __align__(16) uint64_t sm[];   // [DN][M] digit blocks, then the staged twiddles
+    const int b = (int)(blockIdx.x % (unsigned)batch);
+    const int rest = (int)(blockIdx.x / (unsigned)batch);
+    Ctx c;
+    c.t = threadIdx.x;
+    c.r = rest & (SH::C - 1);
+    const int l = rest >> SH::LOGC;
+    c.tw = tw + (long)l * SH::N;
+    c.kc = consts + (long)l * K_COUNT;
+    c.q = c.kc[K_Q];
+    ulonglong2 *etw = reinterpret_cast<ulonglong2 *>(sm + DN * SH::M);
+    c.etw = etw;
+    etw_issue_pass<SH, 0>(etw, c.tw, c.r, c.t);
+    cp_async_commit();
+    const long plane = (long)LK << LOGN;   // one [LK][n] block
+    const long boff = (long)l * SH::N + (long)c.r * SH::M;
+    if (c.t == 0) {
+        // the later digit blocks and this block's keys, fetched into L2 while the first digit is transformed
+        for (int j = 1; j < DN; j++)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ext + ((long)b * DN + j) * plane + boff),
+                         "r"(SH::M * 8) : "memory");
+        for (int j = 0; j < 2 * DN; j++)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(keys + (long)j * plane + boff),
+                         "r"(SH::M * 8) : "memory");
+    }
+#pragma unroll 1
+    for (int j = 0; j < DN; j++) {
+        uint64_t x[SH::E];
+        global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, ext + ((long)b * DN + j) * plane + boff, c.t);
+        if (j == 0) {
+            cp_async_wait_all();
+            __syncthreads();   // the staged twiddles are visible to every thread
+        }
+        fwd_passes<SH, 0, true>(x, sm + j * SH::M, nullptr, c);
+    }
+    __syncthreads();   // every digit block is in shared memory
+    const uint64_t mu = c.kc[K_MU12];
+    const uint32_t c58 = (uint32_t)c.kc[K_C58];
+    uint64_t *o0 = out + (long)b * 2 * plane + boff, *o1 = o0 + plane;
+#pragma unroll 2
+    for (int k = 0; k < SH::E / 2; k++) {
+        const int p = 2 * (c.t + SH::T * k);
+        Mac25 a0x, a0y, a1x, a1y;
+#pragma unroll
+        for (int j = 0; j < DN; j++) {
+            const ulonglong2 d = *reinterpret_cast<const ulonglong2 *>(sm + j * SH::M + swz<SH::LOGE>(p));
+            const ulonglong2 k0 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j) * plane + boff + p));
+            const ulonglong2 k1 = __ldg(reinterpret_cast<const ulonglong2 *>(keys + (2L * j + 1) * plane + boff + p));
+            const Split25 dx = split25(d.x), dy = split25(d.y);
+            mac25(a0x, dx, split25(k0.x));
+            mac25(a0y, dy, split25(k0.y));
+            mac25(a1x, dx, split25(k1.x));
+            mac25(a1y, dy, split25(k1.y));
+        }
+        __stcs(reinterpret_cast<ulonglong2 *>(o0 + p),
+               make_ulonglong2(mac25_reduce(a0x, 0, c.q, mu, c58), mac25_reduce(a0y, 0, c.q, mu, c58)));
+        __stcs(reinterpret_cast<ulonglong2 *>(o1 + p),
+               make_ulonglong2(mac25_reduce(a1x, 0, c.q, mu, c58), mac25_reduce(a1y, 0, c.q, mu, c58)));
+    }
 }
 
 // ---------------------------------------------------------------- inverse --
@@ -802,7 +884,61 @@ int launch_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStr
     else return launch_shape<LOGN, LOGC, LOGT, LOGE, MINB, true>(res, L, rows, t, st);
 }
 
+// Forward NTT of the extended digits fused with the inner product (split
+// shapes): the column kernel on every row of ext, then k_ntt_fwd_blk_ip.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT, int DN>
+int launch_fwd_ip_dn(uint64_t *out, uint64_t *ext, const uint64_t *keys, int LK, int batch, const fhe_ntt_tables *t,
+                     cudaStream_t st) {
+    if constexpr (!SPLIT) {
+        return 0;
+    } else {
+        using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+        constexpr int LOGTPC = LOGC / 2;
+        constexpr int CPR = SH::M / (256 >> LOGTPC);
+        const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(t->fwd);
+        const int items = batch * DN;   // rows of one prime in ext: [batch][DN][LK][n]
+        const int nch = (items + 3) / 4, chunk = (items + nch - 1) / nch;
+        const int nchunks = (items + chunk - 1) / chunk;
+        k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)LK * nchunks * CPR), 256, 0, st>>>(ext, LK, items, chunk,
+                                                                                                tw, t->consts);
+        if (cudaGetLastError() != cudaSuccess) return -1;
+        auto kern = k_ntt_fwd_blk_ip<LOGN, LOGC, LOGT, LOGE, MINB, DN>;
+        const size_t smem = (size_t)(DN * SH::M + 2 * SH::FWD_TW) * sizeof(uint64_t);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        kern<<<(unsigned)((long)LK * SH::C * batch), SH::T, smem, st>>>(out, ext, keys, LK, batch, tw, t->consts);
+        if (cudaGetLastError() != cudaSuccess) return -1;
+        return 2;
+    }
+}
+
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT>
+int launch_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int LK, int dnum, int batch,
+                  const fhe_ntt_tables *t, cudaStream_t st) {
+    switch (dnum) {
+        case 1: return launch_fwd_ip_dn<LOGN, LOGC, LOGT, LOGE, MINB, SPLIT, 1>(out, ext, keys, LK, batch, t, st);
+        case 2: return launch_fwd_ip_dn<LOGN, LOGC, LOGT, LOGE, MINB, SPLIT, 2>(out, ext, keys, LK, batch, t, st);
+        case 3: return launch_fwd_ip_dn<LOGN, LOGC, LOGT, LOGE, MINB, SPLIT, 3>(out, ext, keys, LK, batch, t, st);
+        case 4: return launch_fwd_ip_dn<LOGN, LOGC, LOGT, LOGE, MINB, SPLIT, 4>(out, ext, keys, LK, batch, t, st);
+        default: return 0;
+    }
+}
+
 }  // namespace
+
+int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,
+                      const fhe_ntt_tables *t, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((long)LK * batch * (1L << (log_n - 10)) >= (1L << 31)) return 0;
+    switch (log_n) {
+        case 14: return launch_fwd_ip<14, FHE_SHAPE_14>(out, ext, keys, LK, dnum, batch, t, st);
+        case 15: return launch_fwd_ip<15, FHE_SHAPE_15>(out, ext, keys, LK, dnum, batch, t, st);
+        case 16: return launch_fwd_ip<16, FHE_SHAPE_16>(out, ext, keys, LK, dnum, batch, t, st);
+        case 17: return launch_fwd_ip<17, FHE_SHAPE_17>(out, ext, keys, LK, dnum, batch, t, st);
+        default: return 0;
+    }
+}
 
 int launch_ntt(uint64_t *res, int log_n, int L, long rows, const fhe_ntt_tables *t, bool inverse, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;

@@ -204,6 +204,42 @@ def test_keyswitch_vs_oracle(g, log_n, L, K, dnum, batch):
     assert_reduced(got, qp)
 
 
+@pytest.mark.parametrize("log_n,L,K,dnum,batch", [(14, 7, 3, 3, 3), (15, 8, 2, 2, 2), (17, 4, 2, 4, 1),
+                                                  (14, 5, 3, 1, 2), (16, 24, 8, 3, 4)])
+def test_keyswitch_fused_ntt_ip(g, log_n, L, K, dnum, batch):
+    """For n >= 2^14 and dnum <= 4 the key switch runs the digits' NTT fused
+    with the inner product (the block stages of every digit of one (limb,
+    block, item) in one CTA, then the products with the keys).  Every output
+    row is compared with the oracle, and bit for bit with the unfused path
+    (decompose = ModUp + NTT of the digits, then apply = inner product), for
+    the exact and the approximate ModUp; ragged digits (3, 3, 1), one- and
+    four-digit shapes and the full bench shape (4 ciphertexts, 24 + 8
+    primes, dnum = 3).  The call launches 3 kernels: ModUp, the column
+    stages, the fused block stages + inner product."""
+    import torch
+    n = 1 << log_n
+    qp = g.qp_basis(log_n, L, K)
+    t = g.tables(log_n, tuple(qp))
+    mt = g.api.ModupTables(L, K, dnum, qp)
+    ps = oracle.psis(qp, n)
+    x = inputs.uniform_residues((batch, L, n), qp[:L], 40 + log_n, buffer=0)
+    keys = inputs.uniform_residues((dnum, 2, L + K, n), qp, 41 + log_n, buffer=1)
+    dx, dk = g.dev(x), g.dev(keys)
+    for approx in (False, True):
+        out = torch.empty((batch, 2, L + K, n), dtype=torch.uint64, device="cuda")
+        c0 = g.api.launch_count()
+        g.api.keyswitch_ip(out, dx, dk, L, K, dnum, t, mt, approx=approx)
+        assert g.api.launch_count() - c0 == 3
+        got = g.host(out)
+        assert np.array_equal(got, oracle.keyswitch_batch(x, keys, qp, ps, L, K, dnum, approx=approx)), approx
+        assert_reduced(got, qp)
+        digits = torch.empty((batch, dnum, L + K, n), dtype=torch.uint64, device="cuda")
+        g.api.keyswitch_decompose(digits, dx, L, K, dnum, t, mt, approx=approx)
+        split = torch.empty_like(out)
+        g.api.keyswitch_apply(split, digits, dk, L, K, dnum, t)
+        assert g.same_bits(split, out), approx
+
+
 def test_pointwise_aliasing_and_extremes(g):
     import torch
     log_n, n, L = 11, 2048, 6
