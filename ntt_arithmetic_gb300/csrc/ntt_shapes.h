@@ -17,7 +17,11 @@
 // blocks of 2048 at n = 2^16 (245 against 250 us forward, 234 against 237 us
 // inverse on 384 rows), at 2^15 (248 against 253 / 230 against 234 us) and at
 // 2^14 (249 against 257 us forward); blocks of 4096 (256 threads) or 8
-// residues per thread were 8 % slower.  At 2^17 blocks of 1024 would need 127
+// residues per thread were 8 % slower.  The forward block kernels of 1024
+// residues run at 10 CTAs per SM (96 registers, no spills): 247 / 244 / 249
+// against 253 / 249 / 253 us at n = 2^14 / 2^15 / 2^16 with 8 per SM (126
+// registers); 12 per SM (80 registers) spilled and was slower, and the
+// inverse block kernels gained nothing from 10.  At 2^17 blocks of 1024 would need 127
 // staged twiddle rows per inverse column CTA (65 KB), so it keeps blocks of
 // 2048.
 // The inverse shapes (FHE_INV_SHAPE_n) have the same five fields; a split
@@ -36,9 +40,9 @@
 #define FHE_SHAPE_11 0, 7, 4, 4, 0
 #define FHE_SHAPE_12 0, 8, 4, 2, 0
 #define FHE_SHAPE_13 0, 8, 5, 2, 0
-#define FHE_SHAPE_14 4, 6, 4, 8, 1
-#define FHE_SHAPE_15 5, 6, 4, 8, 1
-#define FHE_SHAPE_16 6, 6, 4, 8, 1
+#define FHE_SHAPE_14 4, 6, 4, 10, 1
+#define FHE_SHAPE_15 5, 6, 4, 10, 1
+#define FHE_SHAPE_16 6, 6, 4, 10, 1
 #define FHE_SHAPE_17 6, 7, 4, 4, 1
 
 // Inverse shapes: split from n = 2^14 (measured against cluster shapes: 247

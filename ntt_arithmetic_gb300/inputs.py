@@ -70,12 +70,14 @@ def uniform_row(q: int, n: int, seed: int, buffer: int, row: int) -> np.ndarray:
     return _sample(np.array([int(q)], dtype=np.uint64), keys, n)[0]
 
 
-def uniform_residues(shape, qs, seed: int, buffer: int = 0) -> np.ndarray:
+def uniform_residues(shape, qs, seed: int, buffer: int = 0, threads: int = 1) -> np.ndarray:
     """Array of ``shape`` = (..., L, n) with row [..., l, :] uniform in [0, qs[l]).
 
     Rows are keyed by (seed, buffer, flat row index), so two buffers with
     different ``buffer`` ids are independent and regenerating any one row
-    gives the same values (see ``uniform_row``).
+    gives the same values (see ``uniform_row``).  ``threads`` > 1 fills
+    chunks of rows concurrently (numpy releases the GIL in the array
+    arithmetic); the values do not depend on it.
     """
     shape = tuple(int(s) for s in shape)
     L, n = shape[-2], shape[-1]
@@ -87,9 +89,19 @@ def uniform_residues(shape, qs, seed: int, buffer: int = 0) -> np.ndarray:
     rows = int(np.prod(shape[:-1]))
     out = np.empty((rows, n), dtype=np.uint64)
     chunk = max(1, (1 << 22) // max(n, 1))      # bound temporaries to ~4M elements
-    for r0 in range(0, rows, chunk):
+
+    def fill(r0: int) -> None:
         r = np.arange(r0, min(rows, r0 + chunk), dtype=np.uint64)
         out[r0:r0 + r.size] = _sample(qs[(r % np.uint64(L)).astype(np.int64)], _keys(seed, buffer, r), n)
+
+    starts = range(0, rows, chunk)
+    if threads > 1 and rows > chunk:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(fill, starts))
+    else:
+        for r0 in starts:
+            fill(r0)
     return out.reshape(shape)
 
 

@@ -132,9 +132,10 @@ def test_ntt_n65536_L24_batch16_full(g):
 
 @pytest.mark.parametrize("domain", ["ntt", "coeff"])
 def test_automorph_n65536_all_galois_elements(g, domain):
-    """k = 5^r mod 2^17 for r in {1, 2, 4, ..., 2^15}: every output row of a
-    sample of rows against the oracle, plus sigma_k then sigma_{k^-1} == id on
-    the whole [16][24][2^16] tensor."""
+    """k = 5^r mod 2^17 for r in {1, 2, 4, ..., 2^15}: two sampled rows per k
+    against the oracle and sigma_k then sigma_{k^-1} == id on the whole
+    [16][24][2^16] tensor; for k = 5^32 mod 2^17 and for the conjugation
+    k = 2n - 1, every one of the 384 output rows against the oracle."""
     import torch
     log_n, n, L = 16, 1 << 16, 24
     qs = g.primes(log_n, L)
@@ -158,10 +159,15 @@ def test_automorph_n65536_all_galois_elements(g, domain):
             else:
                 want = oracle.automorph_coeff(x[b, l], q, k)
             assert np.array_equal(got[b, l], want), (k, b, l)
+        if j == 5:
+            assert np.array_equal(got, oracle.automorph_batch(x, qs, ps, k, domain == "ntt")), k
         g.api.automorph(back, out, kinv, t, domain=domain)
         assert g.same_bits(back, d), k
         if k == 1:
             assert g.same_bits(out, d)
+    k = 2 * n - 1
+    g.api.automorph(out, d, k, t, domain=domain)
+    assert np.array_equal(g.host(out), oracle.automorph_batch(x, qs, ps, k, domain == "ntt")), k
 
 
 def test_automorph_coeff_full_rows(g):
