@@ -507,6 +507,7 @@ def ours(args):
                                "alu_floor_ms": ks_alu_s * 1e3, "hbm_floor_ms": ks_hbm_s * 1e3, "measured_ms": ks_s * 1e3,
                                "frac_alu_at_measured_ceiling": ks_alu_s * (ALU_PEAK_BFLY / ceiling) / ks_s,
                                "hbm_bytes_min": KS_MIN_BYTES_X4,
+                               "traffic": kernel_traffic("keyswitch", KS_T), "traffic_unit": "bytes/call",
                                "work": "4 key switches of [24][n] over 24 + 8 primes, dnum = 3: ModUp (28 Garner products "
                                        "+ 24 x (7 multiply-accumulates + 1 reduction) per coefficient and digit), "
                                        "384 NTT rows, inner product (6 multiply-accumulates + 2 reductions per output "
