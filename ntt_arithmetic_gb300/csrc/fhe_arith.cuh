@@ -177,18 +177,36 @@ FHE_HD void mac25(Mac25 &acc, const Split25 &v, const Split25 &m) {
     acc.s01 += (uint64_t)v.sum * m.sum;
 #endif
 }
-// (sum + extra) mod q with X = s1 2^50 + (s01 - s0 - s1) 2^25 + s0 + extra
-// < 2^105 (extra < 2^60), through barrett_reduce128.
-FHE_HD uint64_t mac25_reduce(const Mac25 &acc, uint64_t extra, uint64_t q, uint64_t mu12, uint32_t c58) {
+// X = s1 2^50 + (s01 - s0 - s1) 2^25 + s0 + extra < 2^105 (extra < 2^60) as
+// a 128-bit hi:lo.
+FHE_HD void mac25_combine(const Mac25 &acc, uint64_t extra, uint64_t &hi, uint64_t &lo) {
     const uint64_t mid = acc.s01 - acc.s0 - acc.s1;
-    uint64_t lo = acc.s0 + extra, hi = 0;
+    lo = acc.s0 + extra;
+    hi = 0;
     uint64_t t = mid << 25;
     lo += t;
     hi += (mid >> 39) + (lo < t ? 1 : 0);
     t = acc.s1 << 50;
     lo += t;
     hi += (acc.s1 >> 14) + (lo < t ? 1 : 0);
+}
+
+// (sum + extra) mod q, through barrett_reduce128.
+FHE_HD uint64_t mac25_reduce(const Mac25 &acc, uint64_t extra, uint64_t q, uint64_t mu12, uint32_t c58) {
+    uint64_t hi, lo;
+    mac25_combine(acc, extra, hi, lo);
     return barrett_reduce128(hi, lo, q, mu12, c58);
+}
+
+// The Barrett step of mac25_reduce without the final small-quotient
+// reduction: a value congruent to X mod q below (3 + X / 2^100) q -- e.g.
+// < 11 q for the up to 8 terms of a digit's basis extension.  For results
+// that feed a forward NTT, whose lazy butterflies accept inputs of this size.
+FHE_HD uint64_t mac25_reduce_lazy(const Mac25 &acc, uint64_t extra, uint64_t q, uint64_t mu12) {
+    uint64_t hi, lo;
+    mac25_combine(acc, extra, hi, lo);
+    const uint64_t x = (hi << 16) | (lo >> 48);
+    return lo - umulhi64(x, mu12) * q;
 }
 
 // Forward (Cooley-Tukey) butterfly with the psi-merged twiddle w (Roy et

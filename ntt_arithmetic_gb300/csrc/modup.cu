@@ -16,7 +16,7 @@
 // reduced modulo each target prime without correcting e D: alpha products
 // for the brackets, then alpha multiply-accumulates per target.
 // The extension sums are exact multiply-accumulates of 25-bit halves with one
-// Barrett reduction per target (mac25 in fhe_arith.cuh).  Each CTA stages its
+// Barrett step per target (mac25 in fhe_arith.cuh), left below (4 + alpha) q.  Each CTA stages its
 // digit's extension weights and the targets' reduction constants in shared
 // memory, so the inner loop reads them as broadcasts.
 #include <cuda_runtime.h>
@@ -43,7 +43,6 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
     // this digit's extension weights and the targets' constants, staged in shared memory
     __shared__ ulonglong2 s_mr[kMaxBasis * MAXA];
     __shared__ ulonglong2 s_qm[kMaxBasis];     // (q, floor(2^100 / q) << 12)
-    __shared__ uint32_t s_c58[kMaxBasis];
     {
         const ulonglong2 *src_mr = mr + (long)j * LK * alpha;
         for (int e = threadIdx.x; e < LK * MAXA; e += blockDim.x) {
@@ -53,15 +52,14 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
         for (int l = threadIdx.x; l < LK; l += blockDim.x) {
             const uint64_t *kc = consts + (long)l * K_COUNT;
             s_qm[l] = make_ulonglong2(__ldg(kc + K_Q), __ldg(kc + K_MU12));
-            s_c58[l] = (uint32_t)__ldg(kc + K_C58);
         }
         __syncthreads();
     }
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
         uint64_t x[MAXA], v[MAXA];
-        const uint64_t *src = in + (long)bi * in_stride + (long)lo * n + i;
+        const uint64_t *src = in + (long)bi * in_stride + ((long)lo << log_n) + i;
 #pragma unroll
-        for (int a = 0; a < MAXA; a++) x[a] = a < cnt ? __ldcs(src + a * n) : 0;
+        for (int a = 0; a < MAXA; a++) x[a] = a < cnt ? __ldcs(src + ((long)a << log_n)) : 0;
         if constexpr (APPROX) {
 #pragma unroll
             for (int a = 0; a < MAXA; a++) {
@@ -89,10 +87,10 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
             }
         }
         }
-        uint64_t *dst = ext + ((long)bi * dnum + j) * LK * n + i;
+        uint64_t *dst = ext + (((long)bi * dnum + j) * LK << log_n) + i;
 #pragma unroll
         for (int a = 0; a < MAXA; a++)
-            if (a < cnt) __stcs(dst + (long)(lo + a) * n, x[a]);   // limbs of the digit are copies
+            if (a < cnt) __stcs(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
         Split25 vs[MAXA];
 #pragma unroll
         for (int a = 0; a < MAXA; a++) vs[a] = split25(v[a]);
@@ -107,8 +105,11 @@ k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_str
                 }
             }
             const ulonglong2 qm = s_qm[l];
-            // exact: the weight of v_0 is 1
-            __stcs(dst + (long)l * n, mac25_reduce(acc, APPROX ? 0 : v[0], qm.x, qm.y, s_c58[l]));
+            // exact: the weight of v_0 is 1.  Stored below (4 + alpha) q (< 11 q at
+            // alpha = 8), not fully reduced: the extended digits only feed the
+            // forward NTT, whose lazy butterflies and final reduction take inputs
+            // of that size (every value stays below 2^57).
+            __stcs(dst + ((long)l << log_n), mac25_reduce_lazy(acc, APPROX ? 0 : v[0], qm.x, qm.y));
         }
     }
 }

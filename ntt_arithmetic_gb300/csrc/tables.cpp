@@ -497,6 +497,9 @@ int selftest_arith(uint64_t seed, int iters) {
             }
             const uint64_t extra = it % 3 == 0 ? next() % q : 0;
             if (mac25_reduce(acc, extra, q, mu12, c58) != (uint64_t)((ref_sum + extra) % q)) return 14;
+            // the lazy form: congruent, below (4 + terms) q
+            const uint64_t lz = mac25_reduce_lazy(acc, extra, q, mu12);
+            if (lz % q != (uint64_t)((ref_sum + extra) % q) || lz >= (uint64_t)(4 + terms) * q) return 15;
         }
     }
     return 0;
