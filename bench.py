@@ -107,6 +107,10 @@ def kernel_traffic(key: str, rows_per_launch: int):
         return None
 
 
+TRAFFIC_SOURCE = ("dram__bytes_read.sum + dram__bytes_write.sum of the launches of one call, from the committed ncu "
+                  "capture that profiles/traffic.json names; null when the kernels' sources changed since that capture")
+
+
 def ntt_fwd_traffic():
     return kernel_traffic("k_ntt_fwd", NPOLY * L)
 
@@ -351,6 +355,59 @@ def run_step(st, step: int, ev=None, X=None, KS=None):
     rec(6)
 
 
+def run_step_halves(st, step: int, streams):
+    """The same step as run_step, as two independent halves of 2 ciphertext
+    pairs each, one per stream: the halves' kernels may run at the same time,
+    so one half's HBM-bound kernels (automorphism, products) can share the
+    SMs with the other half's integer-pipe-bound ones (NTT, ModUp)."""
+    from ntt_arithmetic_gb300 import api
+    k = pow(5, 1 << (step % 16), 2 * N)
+    X, Y, D, KS = st["X"], st["Y"], st["D"], st["KS"]
+    h = PAIRS // 2
+    wsh = st["ws"].view(PAIRS, -1)
+    for i, s in enumerate(streams):
+        sl = slice(i * h, (i + 1) * h)
+        for a in range(2):
+            api.ntt_fwd(X[a, sl], st["tq"], stream=s)
+        for a in range(2):
+            api.automorph(Y[a, sl], X[a, sl], k, st["tq"], domain="ntt", stream=s)
+            api.mul_ntt(Y[a, sl], X[a, sl], Y[a, sl], st["tq"], stream=s)
+        api.tensor(D[sl], Y[0, sl], Y[1, sl], st["tq"], stream=s)
+        api.ntt_inv(D[sl], st["tq"], stream=s)
+        api.keyswitch_ip(KS[sl], D[sl], st["keys"], L, K, DNUM, st["tqp"], st["modup"], wsh[sl].reshape(-1),
+                         stream=s, in_offset=2 * L * N, in_stride=3 * L * N, batch=h)
+
+
+def two_stream_ms(st, steps: int, warmup: int, device) -> float:
+    """Mean ms per step of run_step_halves, between events on the main
+    stream that both halves' streams wait for / are waited on."""
+    import torch
+    main = torch.cuda.current_stream(device)
+    streams = [torch.cuda.Stream(device), torch.cuda.Stream(device)]
+
+    def one(i):
+        ev = torch.cuda.Event()
+        ev.record(main)
+        for s in streams:
+            s.wait_event(ev)
+        run_step_halves(st, i, streams)
+        for s in streams:
+            done = torch.cuda.Event()
+            done.record(s)
+            main.wait_event(done)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    for i in range(steps):
+        one(warmup + i)
+    b.record(main)
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) / steps
+
+
 def e2e_steps(st, steps: int, device) -> float:
     """Mean ms per step end to end: every step copies its input X from pinned
     host memory and reads its key-switch output back to pinned host memory.
@@ -445,6 +502,9 @@ def ours(args):
     barrier()
     e2e_steps(st, max(3, args.warmup), device)          # warm-up of the copy pipeline (streams, pinned buffers)
     e2e_ms = max_over_ranks(e2e_steps(st, args.steps, device), device)
+    # the same work as two concurrent halves on two streams (reported beside the main figure)
+    barrier()
+    two_ms = max_over_ranks(two_stream_ms(st, args.steps, max(3, args.warmup), device), device)
 
     clocks = clock_record(poll, clk)
     hbm, hbm_kind = peaks()
@@ -481,7 +541,8 @@ def ours(args):
         "keyswitch_x4_hbm_bound_frac": (KS_MIN_BYTES_X4 / (kern[5] * 1e-3) / 1e9) / hbm,
         "roofline": {"bound": "alu", "achieved": achieved_bfly / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
                      "unit": "Gbutterfly/s", "frac": achieved_bfly / ALU_PEAK_BFLY, "traffic": ntt_fwd_traffic(),
-                     "traffic_unit": "bytes/launch", "algorithmic_bytes": NTT_BYTES_PER_FWD,
+                     "traffic_unit": "bytes/launch", "traffic_source": TRAFFIC_SOURCE,
+                     "algorithmic_bytes": NTT_BYTES_PER_FWD,
                      "kernel": "forward NTT call = k_ntt_fwd_cols<16,6,3> (first 6 stages, strided columns) + "
                                "k_ntt_fwd_blk<16,6,6,4,8> (last 10 stages, one CTA per 1024-residue block); "
                                "n=2^16, 384 rows; traffic = both launches",
@@ -494,6 +555,7 @@ def ours(args):
         "roofline_ntt_inv": {"bound": "alu", "achieved": achieved_inv / 1e9, "peak": ALU_PEAK_BFLY / 1e9,
                              "unit": "Gbutterfly/s", "frac": achieved_inv / ALU_PEAK_BFLY,
                              "traffic": kernel_traffic("k_ntt_inv", INV_T), "traffic_unit": "bytes/launch",
+                             "traffic_source": TRAFFIC_SOURCE,
                              "algorithmic_bytes": NTT_BYTES_PER_INV,
                              "kernel": "inverse NTT call = k_ntt_inv_blk<16,6,6,4,8> (first 10 stages per block) + "
                                        "k_ntt_inv_cols<16,6,3> (last 6 stages and the twist n^-1 psi^-j); n=2^16, "
@@ -508,12 +570,17 @@ def ours(args):
                                "frac_alu_at_measured_ceiling": ks_alu_s * (ALU_PEAK_BFLY / ceiling) / ks_s,
                                "hbm_bytes_min": KS_MIN_BYTES_X4,
                                "traffic": kernel_traffic("keyswitch", KS_T), "traffic_unit": "bytes/call",
+                               "traffic_source": TRAFFIC_SOURCE,
                                "work": "4 key switches of [24][n] over 24 + 8 primes, dnum = 3: ModUp (28 Garner products "
                                        "+ 24 x (7 multiply-accumulates + 1 reduction) per coefficient and digit), "
                                        "384 NTT rows, inner product (6 multiply-accumulates + 2 reductions per output "
                                        "residue); HBM floor: inputs + keys (read once) + outputs"},
         "clocks": clocks,
         "gpu_launches": launches,
+        "two_streams": {"value": whole_job_rate(UNITS, ws, two_ms), "unit": UNIT, "ms_per_step": two_ms,
+                        "note": "the step's 4 ciphertext pairs as two independent halves of 2, each on its own "
+                                "stream, so that one half's HBM-bound kernels overlap the other's integer-bound "
+                                "ones; the line's value and kernel times are the one-stream step's"},
         "e2e": {"value": whole_job_rate(UNITS, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms, "steps": args.steps,
                 "h2d_bytes_per_step": st["x_pinned"].numel() * 8, "d2h_bytes_per_step": st["ks_pinned"].numel() * 8,
                 "pipelining": "input/output copies on their own streams, double-buffered across steps"},
@@ -1209,7 +1276,8 @@ def row_bench(args):
     else:
         roof["peak_kind"] = "derived: measured integer-pipe rates x 152 SMs x 2070 MHz"
     roof.update({"achieved": achieved, "frac": achieved / roof["peak"], "kernel_ms": kms,
-                 "traffic": kernel_traffic(row.name, row.traffic_rows), "traffic_unit": "bytes/launch"})
+                 "traffic": kernel_traffic(row.name, row.traffic_rows), "traffic_unit": "bytes/launch",
+                 "traffic_source": TRAFFIC_SOURCE})
     barrier()
     n_e2e = max(1, min(args.steps, 5))
     f0, f1 = _events(2)

@@ -41,3 +41,24 @@ def test_pr1_row_step_is_the_negacyclic_product():
         a = inputs.uniform_residues((1, row.L, n), row.q, 1, buffer=0)[0, l]
         b = inputs.uniform_residues((1, row.L, n), row.q, 1, buffer=1)[0, l]
         assert np.array_equal(got[l], oracle.negacyclic_mul(a, b, int(q))), l
+
+
+def test_two_stream_step_matches_the_plain_step():
+    """The bench's two-stream form of the step (two halves of 2 ciphertext
+    pairs on two streams) leaves the same key-switch output as the plain
+    one-stream step."""
+    import torch
+    import gpu_util  # noqa: F401  (builds the library)
+    import bench
+    dev = torch.device("cuda", 0)
+    st = bench.build_state(dev, seed=6)
+    bench.run_step(st, 3)
+    torch.cuda.synchronize()
+    want = st["KS"].cpu().numpy().copy()
+    st["X"].copy_(st["x_pinned"])
+    st["KS"].zero_()
+    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    torch.cuda.synchronize()
+    bench.run_step_halves(st, 3, streams)
+    torch.cuda.synchronize()
+    assert np.array_equal(st["KS"].cpu().numpy(), want)
