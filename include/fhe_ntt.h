@@ -234,7 +234,12 @@ int fhe_keyswitch_workspace_bytes(int log_n, int L, int K, int dnum, int batch, 
  * workspace: device buffer of at least fhe_keyswitch_workspace_bytes; its
  * contents on entry are ignored and on return are unspecified.  out, in,
  * keys and workspace must be pairwise disjoint (FHE_EALIAS); in_stride, if
- * nonzero, must be >= L * n and even. */
+ * nonzero, must be >= L * n and even.
+ * Launches on `stream`, no host sync: ModUp; then, for n >= 2^14 and
+ * dnum <= 4, the column stages of the digits' NTT and one kernel that runs
+ * their block stages and the inner product together (the transformed digits
+ * never return to memory; 3 launches in all); otherwise the digits' NTT and
+ * a separate inner-product kernel. */
 int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
                      int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
                      const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream);
