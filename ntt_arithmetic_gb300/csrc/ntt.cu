@@ -304,13 +304,16 @@ __device__ __forceinline__ void fwd_passes(uint64_t (&x)[SH::E], uint64_t *sm, u
     }
 }
 
-// Row (batch item b, limb l) of this CTA's group of C blocks.  Rows are
-// numbered limb-major (all batch items of limb 0, then of limb 1, ...), so the CTAs
-// resident at one time share a few primes' twiddle tables and a table is
-// fetched from DRAM about once per launch however long the chain is.
+// Row (batch item b, limb l) of the group of C blocks of CTA index `bid`.
+// Rows are numbered limb-major (all batch items of limb 0, then of limb 1,
+// ...), so the CTAs resident at one time share a few primes' twiddle tables
+// and a table is fetched from DRAM about once per launch however long the
+// chain is.  A kernel that consumes what the kernel before it wrote in this
+// order walks it backwards (bid = gridDim.x - 1 - blockIdx.x): the rows
+// written last are read first, while they are still in L2.
 template <int LOGC>
-__device__ __forceinline__ long row_of(int L, int batch, int &l) {
-    const long cl = (long)(blockIdx.x >> LOGC);
+__device__ __forceinline__ long row_of(int L, int batch, int &l, unsigned bid = blockIdx.x) {
+    const long cl = (long)(bid >> LOGC);
     l = (int)(cl / batch);
     return (cl - (long)l * batch) * L + l;
 }
@@ -445,9 +448,11 @@ k_ntt_fwd_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
     c.t = threadIdx.x;
-    c.r = (int)(blockIdx.x & (SH::C - 1));
+    // last rows first: the column kernel wrote them last, so they are still in L2
+    const unsigned bid = gridDim.x - 1 - blockIdx.x;
+    c.r = (int)(bid & (SH::C - 1));
     int l;
-    const long row = row_of<LOGC>(L, batch, l);
+    const long row = row_of<LOGC>(L, batch, l, bid);
     uint64_t *blk = res + row * SH::N + (long)c.r * SH::M;
     c.tw = tw + (long)l * SH::N;
     c.kc = consts + (long)l * K_COUNT;
@@ -480,8 +485,9 @@ k_ntt_fwd_blk_ip(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, c
                  int LK, int batch, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];   // [DN][M] digit blocks, then the staged twiddles
-    const int b = (int)(blockIdx.x % (unsigned)batch);
-    const int rest = (int)(blockIdx.x / (unsigned)batch);
+    const unsigned bid = gridDim.x - 1 - blockIdx.x;   // last rows first (still in L2)
+    const int b = (int)(bid % (unsigned)batch);
+    const int rest = (int)(bid / (unsigned)batch);
     Ctx c;
     c.t = threadIdx.x;
     c.r = rest & (SH::C - 1);
@@ -735,9 +741,10 @@ k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
     __shared__ __align__(16) ulonglong2 stw[C - 1][COLS];   // twiddle 2^S + jlo of column cl at [2^S + jlo - 1][cl]
     __shared__ uint64_t tile[C][COLS];
     // limb-major (as row_of): the CTAs running together share a prime
-    const int part = (int)(blockIdx.x % CPR);
+    const unsigned bid = gridDim.x - 1 - blockIdx.x;   // last rows first (still in L2)
+    const int part = (int)(bid % CPR);
     const int nch = (batch + chunk - 1) / chunk;
-    const int rest = (int)(blockIdx.x / CPR);
+    const int rest = (int)(bid / CPR);
     const int l = rest / nch, b0 = (rest - l * nch) * chunk;
     const int b1 = min(batch, b0 + chunk);
     const int cl = threadIdx.x % COLS, g = threadIdx.x / COLS;
