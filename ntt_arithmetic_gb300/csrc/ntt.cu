@@ -35,6 +35,11 @@
 // per-thread twiddles of the remaining stages are read from the table
 // coalesced.
 //
+// Caching: residues move with the .cg (L2, no L1) policy, not the
+// evict-first streaming policy: the kernel that runs next -- the other half of
+// a split transform, or the product or automorphism that reads the transform's
+// output -- then finds part of them in L2.
+//
 // Arithmetic: lazy Shoup butterflies (fhe_arith.cuh).  Values grow by < 4q
 // per stage with no comparisons (forward: < 69 q after 17 stages; inverse:
 // < 128 q, the twiddle-1 butterflies of its first pass doubling instead) and
@@ -156,13 +161,13 @@ __device__ __forceinline__ void global_load(uint64_t (&x)[SH::E], const uint64_t
         if constexpr (B == 0 && EP >= 1) {
 #pragma unroll
             for (int j = 0; j < EPN; j += 2) {
-                const ulonglong2 v = __ldcs(reinterpret_cast<const ulonglong2 *>(blk + pass_pos<B, EP>(g, j)));
+                const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2 *>(blk + pass_pos<B, EP>(g, j)));
                 x[k * EPN + j] = v.x;
                 x[k * EPN + j + 1] = v.y;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < EPN; j++) x[k * EPN + j] = __ldcs(blk + pass_pos<B, EP>(g, j));
+            for (int j = 0; j < EPN; j++) x[k * EPN + j] = __ldcg(blk + pass_pos<B, EP>(g, j));
         }
     }
 }
@@ -176,11 +181,11 @@ __device__ __forceinline__ void global_store(const uint64_t (&x)[SH::E], uint64_
         if constexpr (B == 0 && EP >= 1) {
 #pragma unroll
             for (int j = 0; j < EPN; j += 2)
-                __stcs(reinterpret_cast<ulonglong2 *>(blk + pass_pos<B, EP>(g, j)),
+                __stcg(reinterpret_cast<ulonglong2 *>(blk + pass_pos<B, EP>(g, j)),
                        make_ulonglong2(x[k * EPN + j], x[k * EPN + j + 1]));
         } else {
 #pragma unroll
-            for (int j = 0; j < EPN; j++) __stcs(blk + pass_pos<B, EP>(g, j), x[k * EPN + j]);
+            for (int j = 0; j < EPN; j++) __stcg(blk + pass_pos<B, EP>(g, j), x[k * EPN + j]);
         }
     }
 }
@@ -196,7 +201,7 @@ __device__ __forceinline__ void block_load_coalesced(uint64_t *sm, const uint64_
 #pragma unroll
     for (int k = 0; k < SH::E / 2; k++) {
         const int p = 2 * (t + SH::T * k);
-        *reinterpret_cast<ulonglong2 *>(sm + swz<SH::LOGE>(p)) = __ldcs(reinterpret_cast<const ulonglong2 *>(blk + p));
+        *reinterpret_cast<ulonglong2 *>(sm + swz<SH::LOGE>(p)) = __ldcg(reinterpret_cast<const ulonglong2 *>(blk + p));
     }
 }
 
@@ -205,7 +210,7 @@ __device__ __forceinline__ void block_store_coalesced(const uint64_t *sm, uint64
 #pragma unroll
     for (int k = 0; k < SH::E / 2; k++) {
         const int p = 2 * (t + SH::T * k);
-        __stcs(reinterpret_cast<ulonglong2 *>(blk + p), *reinterpret_cast<const ulonglong2 *>(sm + swz<SH::LOGE>(p)));
+        __stcg(reinterpret_cast<ulonglong2 *>(blk + p), *reinterpret_cast<const ulonglong2 *>(sm + swz<SH::LOGE>(p)));
     }
 }
 
@@ -395,14 +400,14 @@ k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
     uint64_t *p = res + ((long)b0 * L + l) * ((long)1 << LOGN) + part * COLS + cl;
     uint64_t xn[VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; i++) xn[i] = __ldcs(p + (long)(g + TPC * i) * M);
+    for (int i = 0; i < VPT; i++) xn[i] = __ldcg(p + (long)(g + TPC * i) * M);
     for (int b = b0; b < b1; b++, p += rstride) {
         uint64_t x[VPT];
 #pragma unroll
         for (int i = 0; i < VPT; i++) x[i] = xn[i];
         if (b + 1 < b1) {
 #pragma unroll
-            for (int i = 0; i < VPT; i++) xn[i] = __ldcs(p + rstride + (long)(g + TPC * i) * M);
+            for (int i = 0; i < VPT; i++) xn[i] = __ldcg(p + rstride + (long)(g + TPC * i) * M);
         }
 #pragma unroll
         for (int S = 0; S < LOGVPT; S++) {
@@ -433,7 +438,7 @@ k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
             }
         }
 #pragma unroll
-        for (int i = 0; i < VPT; i++) __stcs(p + (long)(LOGTPC > 0 ? VPT * g + i : g + TPC * i) * M, x[i]);
+        for (int i = 0; i < VPT; i++) __stcg(p + (long)(LOGTPC > 0 ? VPT * g + i : g + TPC * i) * M, x[i]);
     }
 }
 
@@ -539,9 +544,9 @@ k_ntt_fwd_blk_ip(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, c
             mac25(a1x, dx, split25(k1.x));
             mac25(a1y, dy, split25(k1.y));
         }
-        __stcs(reinterpret_cast<ulonglong2 *>(o0 + p),
+        __stcg(reinterpret_cast<ulonglong2 *>(o0 + p),
                make_ulonglong2(mac25_reduce(a0x, 0, c.q, mu, c58), mac25_reduce(a0y, 0, c.q, mu, c58)));
-        __stcs(reinterpret_cast<ulonglong2 *>(o1 + p),
+        __stcg(reinterpret_cast<ulonglong2 *>(o1 + p),
                make_ulonglong2(mac25_reduce(a1x, 0, c.q, mu, c58), mac25_reduce(a1y, 0, c.q, mu, c58)));
     }
 }
@@ -760,7 +765,7 @@ k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
         uint64_t x[VPT];
         ulonglong2 tv[VPT];
 #pragma unroll
-        for (int i = 0; i < VPT; i++) x[i] = __ldcs(p + (long)(VPT * g + i) * M);
+        for (int i = 0; i < VPT; i++) x[i] = __ldcg(p + (long)(VPT * g + i) * M);
 #pragma unroll
         for (int i = 0; i < VPT; i++) tv[i] = __ldg(tt + (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M);
         cp_async_wait_all();
@@ -795,7 +800,7 @@ k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ul
         }
 #pragma unroll
         for (int i = 0; i < VPT; i++)
-            __stcs(p + (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M, twist(x[i], tv[i], q));
+            __stcg(p + (long)(LOGTPC > 0 ? g + TPC * i : VPT * g + i) * M, twist(x[i], tv[i], q));
     }
 }
 
