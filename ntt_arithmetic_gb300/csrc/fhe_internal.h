@@ -90,6 +90,13 @@ int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int l
 // [batch][2][LK][n].  Returns 0 without launching when no fused kernel
 // exists for the shape (n < 2^14, dnum > 4): the caller then runs
 // launch_ntt + launch_ks_ip.
+// ModDown's forward NTT of its correction d [batch][L][n] (overwritten by
+// the column stages) fused with the last step out = (in - NTT(d)) P^-1 mod q_l,
+// in the NTT-domain input [batch][L+K][n] and pinv the blob's [L] (P^-1 mod
+// q_l, Shoup companion) pairs.  Returns 0 without launching for n < 2^14: the
+// caller then runs launch_ntt + its own last-step kernel.
+int launch_ntt_fwd_moddown(uint64_t *out, uint64_t *d, const uint64_t *in, int log_n, int L, int K, int batch,
+                           const fhe_ntt_tables *t_q, const void *pinv, void *stream);
 int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,
                       const fhe_ntt_tables *t, void *stream);
 

@@ -198,7 +198,11 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
     launched++;
     if (!ntt_domain) return launched;
     const fhe_ntt_tables tq = tables_slice(t_qp, 0, L);
-    int r = launch_ntt(d, log_n, L, (long)batch * L, &tq, false, stream);
+    // the forward NTT of d fused with the last step where a fused kernel exists
+    int r = launch_ntt_fwd_moddown(out, d, in, log_n, L, K, batch, &tq, md + lay.off_pinv, stream);
+    if (r < 0) return -1;
+    if (r > 0) return launched + r;
+    r = launch_ntt(d, log_n, L, (long)batch * L, &tq, false, stream);
     if (r < 0) return -1;
     launched += r;
     const long pairs = ((long)batch * L << log_n) / 2;

@@ -551,6 +551,54 @@ k_ntt_fwd_blk_ip(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, c
     }
 }
 
+// The block stages of the forward NTT of ModDown's correction d fused with
+// ModDown's last step (FHElium, "Eager, Compile, and native execution",
+// section "CUDA execution": "QP-to-Q ModDown"): CTA (row (b, l), block r)
+// transforms block r of d[b][l] and writes
+//   out[b][l][p] = (in[b][l][p] - NTT(d)[b][l][p]) P^-1  mod q_l
+// for the block's positions p, with in the NTT-domain input over Q u P
+// (item stride L + K rows).  The transformed d never returns to HBM.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
+__global__ void __launch_bounds__(1 << LOGT, MINB)
+k_ntt_fwd_blk_md(uint64_t *__restrict__ out, const uint64_t *__restrict__ d, const uint64_t *__restrict__ in, int L,
+                 int K, int batch, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts,
+                 const ulonglong2 *__restrict__ pinv) {
+    using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+    extern __shared__ __align__(16) uint64_t sm[];
+    Ctx c;
+    c.t = threadIdx.x;
+    const unsigned bid = gridDim.x - 1 - blockIdx.x;   // last rows first (still in L2)
+    c.r = (int)(bid & (SH::C - 1));
+    int l;
+    const long row = row_of<LOGC>(L, batch, l, bid);
+    const long b = row / L;
+    c.tw = tw + (long)l * SH::N;
+    c.kc = consts + (long)l * K_COUNT;
+    c.q = c.kc[K_Q];
+    ulonglong2 *etw = reinterpret_cast<ulonglong2 *>(sm + SH::M);
+    c.etw = etw;
+    etw_issue_pass<SH, 0>(etw, c.tw, c.r, c.t);
+    cp_async_commit();
+    uint64_t x[SH::E];
+    global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, d + row * SH::N + (long)c.r * SH::M, c.t);
+    cp_async_wait_all();
+    __syncthreads();   // the staged twiddles are visible to every thread
+    fwd_passes<SH, 0, true>(x, sm, nullptr, c);
+    __syncthreads();   // the reduced block is in shared memory
+    const ulonglong2 pi = __ldg(pinv + l);
+    const uint64_t *src = in + ((b * (L + K) + l) << LOGN) + (long)c.r * SH::M;
+    uint64_t *dst = out + row * SH::N + (long)c.r * SH::M;
+#pragma unroll
+    for (int k = 0; k < SH::E / 2; k++) {
+        const int p = 2 * (c.t + SH::T * k);
+        const ulonglong2 dv = *reinterpret_cast<const ulonglong2 *>(sm + swz<SH::LOGE>(p));
+        const ulonglong2 xv = __ldcs(reinterpret_cast<const ulonglong2 *>(src + p));
+        __stcs(reinterpret_cast<ulonglong2 *>(dst + p),
+               make_ulonglong2(reduce4(shoup_lazy(xv.x + c.q - dv.x, pi.x, pi.y, c.q), c.q),
+                               reduce4(shoup_lazy(xv.y + c.q - dv.y, pi.x, pi.y, c.q), c.q)));
+    }
+}
+
 // ---------------------------------------------------------------- inverse --
 //
 // Cyclic Cooley-Tukey (decimation in time) on the bit-reversed input, then the
@@ -925,6 +973,34 @@ int launch_fwd_ip_dn(uint64_t *out, uint64_t *ext, const uint64_t *keys, int LK,
     }
 }
 
+// ModDown's forward NTT of d fused with its last step (split shapes): the
+// column kernel on every row of d, then k_ntt_fwd_blk_md.
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT>
+int launch_fwd_md(uint64_t *out, uint64_t *d, const uint64_t *in, int L, int K, int batch, const fhe_ntt_tables *t,
+                  const ulonglong2 *pinv, cudaStream_t st) {
+    if constexpr (!SPLIT) {
+        return 0;
+    } else {
+        using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
+        constexpr int LOGTPC = LOGC / 2;
+        constexpr int CPR = SH::M / (256 >> LOGTPC);
+        const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(t->fwd);
+        const int nch = (batch + 3) / 4, chunk = (batch + nch - 1) / nch;
+        const int nchunks = (batch + chunk - 1) / chunk;
+        k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)L * nchunks * CPR), 256, 0, st>>>(d, L, batch, chunk,
+                                                                                                tw, t->consts);
+        if (cudaGetLastError() != cudaSuccess) return -1;
+        auto kern = k_ntt_fwd_blk_md<LOGN, LOGC, LOGT, LOGE, MINB>;
+        const size_t smem = (size_t)SH::smem_words(false) * sizeof(uint64_t);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        kern<<<(unsigned)((long)batch * L * SH::C), SH::T, smem, st>>>(out, d, in, L, K, batch, tw, t->consts, pinv);
+        if (cudaGetLastError() != cudaSuccess) return -1;
+        return 2;
+    }
+}
+
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT>
 int launch_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int LK, int dnum, int batch,
                   const fhe_ntt_tables *t, cudaStream_t st) {
@@ -948,6 +1024,19 @@ int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int lo
         case 15: return launch_fwd_ip<15, FHE_SHAPE_15>(out, ext, keys, LK, dnum, batch, t, st);
         case 16: return launch_fwd_ip<16, FHE_SHAPE_16>(out, ext, keys, LK, dnum, batch, t, st);
         case 17: return launch_fwd_ip<17, FHE_SHAPE_17>(out, ext, keys, LK, dnum, batch, t, st);
+        default: return 0;
+    }
+}
+
+int launch_ntt_fwd_moddown(uint64_t *out, uint64_t *d, const uint64_t *in, int log_n, int L, int K, int batch,
+                           const fhe_ntt_tables *t_q, const void *pinv, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const ulonglong2 *pi = (const ulonglong2 *)pinv;
+    switch (log_n) {
+        case 14: return launch_fwd_md<14, FHE_SHAPE_14>(out, d, in, L, K, batch, t_q, pi, st);
+        case 15: return launch_fwd_md<15, FHE_SHAPE_15>(out, d, in, L, K, batch, t_q, pi, st);
+        case 16: return launch_fwd_md<16, FHE_SHAPE_16>(out, d, in, L, K, batch, t_q, pi, st);
+        case 17: return launch_fwd_md<17, FHE_SHAPE_17>(out, d, in, L, K, batch, t_q, pi, st);
         default: return 0;
     }
 }

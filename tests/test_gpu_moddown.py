@@ -68,7 +68,8 @@ def test_rescale_chain(g, domain, nearest):
 
 
 @pytest.mark.parametrize("log_n,L,K,batch", [(11, 7, 3, 3), (12, 5, 16, 2), (10, 9, 2, 5), (13, 3, 4, 1),
-                                             (1, 2, 1, 3), (4, 1, 16, 2), (17, 2, 8, 1)])
+                                             (1, 2, 1, 3), (4, 1, 16, 2), (17, 2, 8, 1), (14, 5, 3, 3),
+                                             (15, 4, 2, 2)])
 @pytest.mark.parametrize("domain", ["coeff", "ntt"])
 def test_moddown_shapes(g, log_n, L, K, batch, domain):
     qp = g.qp_basis(log_n, L, K)
@@ -146,7 +147,8 @@ def test_moddown_arguments(g):
 
 def test_moddown_launch_count(g):
     """Coefficient domain: one fused pass; NTT domain: copy of the P limbs,
-    inverse NTT, conversion, forward NTT over Q and the final product."""
+    inverse NTT, conversion, forward NTT over Q and the final product (the
+    last two in one kernel's block stages for n >= 2^14)."""
     import torch
     log_n, L, K, batch = 12, 4, 2, 1
     n = 1 << log_n
@@ -162,6 +164,19 @@ def test_moddown_launch_count(g):
     c2 = g.api.launch_count()
     assert c1 - c0 == 1
     assert c2 - c1 == 5
+    # n >= 2^14: the forward NTT's block stages carry the final product (copy, inverse NTT in two launches,
+    # conversion, column stages, block stages + product)
+    log_n = 14
+    n = 1 << log_n
+    qp = g.qp_basis(log_n, L, K)
+    t = g.tables(log_n, tuple(qp))
+    md = g.api.ModdownTables(L, K, qp)
+    xh = inputs.uniform_residues((batch, L + K, n), qp, 741, buffer=1)
+    out = torch.empty((batch, L, n), dtype=torch.uint64, device="cuda")
+    c0 = g.api.launch_count()
+    g.api.moddown(out, g.dev(xh), L, K, t, md, domain="ntt")
+    assert g.api.launch_count() - c0 == 6
+    assert np.array_equal(g.host(out), _want(xh, qp, L, K, "ntt", True))
 
 
 @pytest.mark.parametrize("domain", ["coeff", "ntt"])
