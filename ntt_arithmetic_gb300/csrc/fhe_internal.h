@@ -95,6 +95,11 @@ int launch_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int l
 // in the NTT-domain input [batch][L+K][n] and pinv the blob's [L] (P^-1 mod
 // q_l, Shoup companion) pairs.  Returns 0 without launching for n < 2^14: the
 // caller then runs launch_ntt + its own last-step kernel.
+// Inverse NTT of rows read from another buffer: row (b, l) of src at
+// src + b * src_item + l * n (src unchanged), result in dst [batch][L][n].
+// Returns 0 without launching for n < 2^14 (copy the rows, then launch_ntt).
+int launch_ntt_inv_from(uint64_t *dst, const uint64_t *src, long src_item, int log_n, int L, int batch,
+                        const fhe_ntt_tables *t, void *stream);
 int launch_ntt_fwd_moddown(uint64_t *out, uint64_t *d, const uint64_t *in, int log_n, int L, int K, int batch,
                            const fhe_ntt_tables *t_q, const void *pinv, void *stream);
 int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,

@@ -11,7 +11,8 @@
 //   1. the P residues of X + h are converted exactly to c mod q_l by Garner's
 //      mixed radix (the same construction as the key-switch ModUp; the radix
 //      sum is an exact multiply-accumulate reduced once) and
-//      d_l = c - h mod q_l is written (coefficient domain);
+//      d_l = c - h mod q_l is written (coefficient domain; in the NTT-domain
+//      path as a value below (6 + K) q congruent to it, for the forward NTT);
 //   2. out_l = (x_l - d_l) P^-1 mod q_l.
 // In the coefficient domain both steps run in one pass (one read of every
 // input limb, one write of every output limb).  In the NTT domain the P limbs
@@ -113,10 +114,18 @@ k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long 
                     mac25(acc, vs[a], split25_entry(m.x, m.y));
                 }
             }
-            uint64_t c = mac25_reduce(acc, v[0], q, qm.y, STAGED ? s_c58[l] : (uint32_t)__ldg(kc + K_C58));
-            if (nearest) {
-                const uint64_t h = __ldg(hq + l);
-                c = c >= h ? c - h : c + q - h;
+            uint64_t c;
+            if constexpr (FUSED) {
+                c = mac25_reduce(acc, v[0], q, qm.y, STAGED ? s_c58[l] : (uint32_t)__ldg(kc + K_C58));
+                if (nearest) {
+                    const uint64_t h = __ldg(hq + l);
+                    c = c >= h ? c - h : c + q - h;
+                }
+            } else {
+                // d only feeds the forward NTT over Q, whose lazy butterflies take
+                // inputs of a few q: left below (5 + K) q, not fully reduced
+                c = mac25_reduce_lazy(acc, v[0], q, qm.y);
+                if (nearest) c += q - __ldg(hq + l);
             }
             if constexpr (FUSED) {
                 const uint64_t x = __ldcs(src + b * src_item - ((long)(L - l) << log_n) + i);
@@ -178,13 +187,18 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
     uint64_t *d = ntt_domain ? ws : out;                // [batch][L][n]; the output itself when fused
     if (ntt_domain) {
         uint64_t *pl = ws + ((long)batch * L << log_n);   // [batch][K][n]
-        const long pairs = ((long)batch * K << log_n) / 2;
-        k_copy_limbs<<<stream_grid(pairs, kThreads, 8), kThreads, 0, st>>>(pl, in, pairs, log_n, L, K);
-        if (cudaGetLastError() != cudaSuccess) return -1;
-        launched++;
         const fhe_ntt_tables tp = tables_slice(t_qp, L, K);
-        int r = launch_ntt(pl, log_n, K, (long)batch * K, &tp, true, stream);
+        // the inverse NTT of the P limbs reads them from `in` where its block kernel can
+        int r = launch_ntt_inv_from(pl, in + ((long)L << log_n), (long)(L + K) << log_n, log_n, K, batch, &tp, stream);
         if (r < 0) return -1;
+        if (r == 0) {
+            const long pairs = ((long)batch * K << log_n) / 2;
+            k_copy_limbs<<<stream_grid(pairs, kThreads, 8), kThreads, 0, st>>>(pl, in, pairs, log_n, L, K);
+            if (cudaGetLastError() != cudaSuccess) return -1;
+            launched++;
+            r = launch_ntt(pl, log_n, K, (long)batch * K, &tp, true, stream);
+            if (r < 0) return -1;
+        }
         launched += r;
         src = pl;
         src_item = (long)K << log_n;

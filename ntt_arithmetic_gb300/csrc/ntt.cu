@@ -744,8 +744,10 @@ k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__rest
 // and stores the block in place, unreduced.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
-k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
+k_ntt_inv_blk(uint64_t *res, const uint64_t *src, long src_item, int L, int batch, const ulonglong2 *__restrict__ tw,
               const uint64_t *__restrict__ consts) {
+    // reads row (b, l) at src + b src_item + l N (src = res, src_item = L N:
+    // in place) and writes it to res + (b L + l) N
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     static_assert(SH::E >= 2, "the block is loaded through shared memory");
     extern __shared__ __align__(16) uint64_t sm[];
@@ -755,6 +757,7 @@ k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__
     int l;
     const long row = row_of<LOGC>(L, batch, l);
     uint64_t *blk = res + row * SH::N + (long)c.r * SH::M;
+    const uint64_t *sblk = src + (row / L) * src_item + (long)l * SH::N + (long)c.r * SH::M;
     c.tw = tw + (long)l * SH::N;
     c.kc = consts + (long)l * K_COUNT;
     c.q = c.kc[K_Q];
@@ -763,7 +766,7 @@ k_ntt_inv_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__
     for (int u = 1 + c.t; u < SH::INV_TW; u += SH::T) cp_async16(etw + u, c.tw + u);
     cp_async_commit();
     uint64_t x[SH::E];
-    block_load_coalesced<SH>(sm, blk, c.t);
+    block_load_coalesced<SH>(sm, sblk, c.t);
     cp_async_wait_all();
     __syncthreads();   // the block and the staged twiddles are visible to every thread
     smem_load<SH, 0, SH::P == 1 ? SH::EREM : LOGE>(x, sm, c.t);
@@ -914,7 +917,8 @@ int launch_fwd(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStr
 
 // Split inverse: one CTA per block (the local stages), then the column kernel.
 template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
-int launch_split_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st) {
+int launch_split_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaStream_t st,
+                     const uint64_t *src = nullptr, long src_item = 0) {
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     constexpr int LOGTPC = LOGC / 2;                  // threads per column
     constexpr int CPR = SH::M / (256 >> LOGTPC);      // column-kernel CTAs per row
@@ -926,7 +930,11 @@ int launch_split_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, c
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
-    kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, L, batch, tw, t->consts);
+    if (!src) {
+        src = res;
+        src_item = (long)L << LOGN;
+    }
+    kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, src, src_item, L, batch, tw, t->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
     // batch items per column CTA: up to 4, balanced, so the staged twiddles
     // serve several items and the grid still spans several waves
@@ -1013,6 +1021,15 @@ int launch_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int LK, in
     }
 }
 
+// A split inverse reading its rows from another buffer (row (b, l) at
+// src + b src_item + l n) and leaving the result in dst [batch][L][n].
+template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int SPLIT>
+int launch_inv_from(uint64_t *dst, const uint64_t *src, long src_item, int L, int batch, const fhe_ntt_tables *t,
+                    cudaStream_t st) {
+    if constexpr (!SPLIT) return 0;
+    else return launch_split_inv<LOGN, LOGC, LOGT, LOGE, MINB>(dst, L, (long)batch * L, t, st, src, src_item);
+}
+
 }  // namespace
 
 int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum, int batch,
@@ -1024,6 +1041,18 @@ int launch_ntt_fwd_ip(uint64_t *out, uint64_t *ext, const uint64_t *keys, int lo
         case 15: return launch_fwd_ip<15, FHE_SHAPE_15>(out, ext, keys, LK, dnum, batch, t, st);
         case 16: return launch_fwd_ip<16, FHE_SHAPE_16>(out, ext, keys, LK, dnum, batch, t, st);
         case 17: return launch_fwd_ip<17, FHE_SHAPE_17>(out, ext, keys, LK, dnum, batch, t, st);
+        default: return 0;
+    }
+}
+
+int launch_ntt_inv_from(uint64_t *dst, const uint64_t *src, long src_item, int log_n, int L, int batch,
+                        const fhe_ntt_tables *t, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (log_n) {
+        case 14: return launch_inv_from<14, FHE_INV_SHAPE_14>(dst, src, src_item, L, batch, t, st);
+        case 15: return launch_inv_from<15, FHE_INV_SHAPE_15>(dst, src, src_item, L, batch, t, st);
+        case 16: return launch_inv_from<16, FHE_INV_SHAPE_16>(dst, src, src_item, L, batch, t, st);
+        case 17: return launch_inv_from<17, FHE_INV_SHAPE_17>(dst, src, src_item, L, batch, t, st);
         default: return 0;
     }
 }
