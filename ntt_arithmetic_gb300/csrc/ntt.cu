@@ -40,10 +40,18 @@
 // a split transform, or the product or automorphism that reads the transform's
 // output -- then finds part of them in L2.
 //
+// Fused block kernels: the key switch's digit transform ends in the inner
+// product with the keys (k_ntt_fwd_blk_ip) and ModDown's transform of its
+// correction ends in the last product (x - d) P^-1 (k_ntt_fwd_blk_md); both
+// keep the reduced block in shared memory instead of storing it.
+//
 // Arithmetic: lazy Shoup butterflies (fhe_arith.cuh).  Values grow by < 4q
-// per stage with no comparisons (forward: < 69 q after 17 stages; inverse:
-// < 128 q, the twiddle-1 butterflies of its first pass doubling instead) and
-// are reduced once, before the store.
+// per stage with no comparisons and are reduced once, before the store.
+// Forward inputs below B stay below B + 68 q after 17 stages: B = q for the
+// public transform; the key switch's extended digits and ModDown's
+// correction arrive below 20 q (their lazy Barrett outputs), so every value
+// stays below 2^57.  Inverse: < 128 q, the twiddle-1 butterflies of its
+// first pass doubling instead.
 //
 // Shared-memory index swizzle: index p is stored at p ^ (((p >> LOGE) & 7) << 1),
 // which makes every pass's accesses bank-conflict-free (two wavefronts per
@@ -64,6 +72,8 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+// wait until at most the most recent committed group is still in flight
+__device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
 template <int LOGN_, int LOGC_, int LOGT_, int LOGE_>
 struct Shape {
@@ -577,22 +587,28 @@ k_ntt_fwd_blk_md(uint64_t *__restrict__ out, const uint64_t *__restrict__ d, con
     c.q = c.kc[K_Q];
     ulonglong2 *etw = reinterpret_cast<ulonglong2 *>(sm + SH::M);
     c.etw = etw;
+    uint64_t *xs = sm + SH::M + 2 * SH::FWD_TW;   // the block of x, for the last product
+    const uint64_t *src = in + ((b * (L + K) + l) << LOGN) + (long)c.r * SH::M;
     etw_issue_pass<SH, 0>(etw, c.tw, c.r, c.t);
+    cp_async_commit();
+    // x is only needed after the transform: its copy is a commit group of its
+    // own, so the first pass waits for the staged twiddles alone
+    for (int u = 2 * c.t; u < SH::M; u += 2 * SH::T) cp_async16(xs + u, src + u);
     cp_async_commit();
     uint64_t x[SH::E];
     global_load<SH, (SH::P - 1) * LOGE, SH::EREM>(x, d + row * SH::N + (long)c.r * SH::M, c.t);
-    cp_async_wait_all();
+    cp_async_wait_but_last();
     __syncthreads();   // the staged twiddles are visible to every thread
     fwd_passes<SH, 0, true>(x, sm, nullptr, c);
-    __syncthreads();   // the reduced block is in shared memory
+    cp_async_wait_all();
+    __syncthreads();   // the reduced block and x are in shared memory
     const ulonglong2 pi = __ldg(pinv + l);
-    const uint64_t *src = in + ((b * (L + K) + l) << LOGN) + (long)c.r * SH::M;
     uint64_t *dst = out + row * SH::N + (long)c.r * SH::M;
 #pragma unroll
     for (int k = 0; k < SH::E / 2; k++) {
         const int p = 2 * (c.t + SH::T * k);
         const ulonglong2 dv = *reinterpret_cast<const ulonglong2 *>(sm + swz<SH::LOGE>(p));
-        const ulonglong2 xv = __ldcs(reinterpret_cast<const ulonglong2 *>(src + p));
+        const ulonglong2 xv = *reinterpret_cast<const ulonglong2 *>(xs + p);
         __stcs(reinterpret_cast<ulonglong2 *>(dst + p),
                make_ulonglong2(reduce4(shoup_lazy(xv.x + c.q - dv.x, pi.x, pi.y, c.q), c.q),
                                reduce4(shoup_lazy(xv.y + c.q - dv.y, pi.x, pi.y, c.q), c.q)));
@@ -999,7 +1015,7 @@ int launch_fwd_md(uint64_t *out, uint64_t *d, const uint64_t *in, int L, int K, 
                                                                                                 tw, t->consts);
         if (cudaGetLastError() != cudaSuccess) return -1;
         auto kern = k_ntt_fwd_blk_md<LOGN, LOGC, LOGT, LOGE, MINB>;
-        const size_t smem = (size_t)SH::smem_words(false) * sizeof(uint64_t);
+        const size_t smem = (size_t)(SH::smem_words(false) + SH::M) * sizeof(uint64_t);
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
