@@ -34,6 +34,7 @@ __device__ __forceinline__ uint32_t aut_src(uint32_t i, int log_n, uint32_t k) {
 
 __global__ void __launch_bounds__(kThreads)
 k_aut_ntt(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n, int lb, uint32_t k) {
+    pdl_begin();
     extern __shared__ __align__(16) uint64_t blk[];
     const int per_row = log_n - lb;
     const long row = (long)blockIdx.x >> per_row;
@@ -56,6 +57,7 @@ k_aut_ntt(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n
 __global__ void __launch_bounds__(kThreads)
 k_aut_coeff(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, long pairs, int log_n, int L,
             uint32_t kinv, const uint64_t *__restrict__ consts) {
+    pdl_begin();
     const uint32_t n = 1u << log_n, mask2n = (2u << log_n) - 1u;
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 k_bconv(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, int log_n, int S, int T, int tchunk,
         const uint64_t *__restrict__ src, const ulonglong2 *__restrict__ dst, const ulonglong2 *__restrict__ garner,
         const ulonglong2 *__restrict__ weights) {
+    pdl_begin();
     // APPROX: `garner` holds the bracket constants [S], `weights` the CRT
     // weights [T][S]; exact: Garner constants [S][S] and radix weights [T][S].
     const long n = 1L << log_n;
@@ -132,10 +133,10 @@ void launch_t(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int ba
     chunks = (T + tchunk - 1) / tchunk;
     dim3 grid((unsigned)bx, (unsigned)chunks, (unsigned)batch);
     auto kern = approx ? k_bconv<MAXS, true> : k_bconv<MAXS, false>;
-    kern<<<grid, kThreads, 0, st>>>(out, in, log_n, S, T, tchunk, (const uint64_t *)(base + lay.off_src),
-                                    (const ulonglong2 *)(base + lay.off_dst),
-                                    (const ulonglong2 *)(base + (approx ? lay.off_qinv : lay.off_garner)),
-                                    (const ulonglong2 *)(base + (approx ? lay.off_qhat : lay.off_mr)));
+    launch_pdl(kern, grid, kThreads, 0, st, out, in, log_n, S, T, tchunk, (const uint64_t *)(base + lay.off_src),
+               (const ulonglong2 *)(base + lay.off_dst),
+               (const ulonglong2 *)(base + (approx ? lay.off_qinv : lay.off_garner)),
+               (const ulonglong2 *)(base + (approx ? lay.off_qhat : lay.off_mr)));
 }
 
 }  // namespace

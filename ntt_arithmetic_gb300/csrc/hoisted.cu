@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kThreads)
 k_ks_ip_aut(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, const uint64_t *__restrict__ keys,
             int log_n, int lb, int LK, int dnum_rt, int batch, int R, const GaloisSet g,
             const uint64_t *__restrict__ consts) {
+    pdl_begin();
     extern __shared__ __align__(16) uint64_t blk[];   // [dnum][2^lb]
     const int dnum = DN > 0 ? DN : dnum_rt;
     const int nb = log_n - lb;
@@ -136,8 +137,8 @@ int launch_ks_ip_aut(uint64_t *out, const uint64_t *ext, const uint64_t *keys, i
     const size_t smem = ((size_t)dnum << lb) * 8;
     auto kern = dnum == 1 ? k_ks_ip_aut<1> : dnum == 2 ? k_ks_ip_aut<2> : dnum == 3 ? k_ks_ip_aut<3>
               : dnum == 4 ? k_ks_ip_aut<4> : k_ks_ip_aut<0>;
-    kern<<<(unsigned)blocks, kThreads, smem, (cudaStream_t)stream>>>(out, ext, keys, log_n, lb, LK, dnum, batch, R, g,
-                                                                      t->consts);
+    launch_pdl(kern, (unsigned)blocks, kThreads, smem, (cudaStream_t)stream, out, ext, keys, log_n, lb, LK, dnum,
+               batch, R, g, t->consts);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

@@ -33,6 +33,7 @@ constexpr int kThreads = 256;
 // ws[b][k][i] = in[b][L + k][i]  (the P limbs of each batch item)
 __global__ void __launch_bounds__(kThreads)
 k_copy_limbs(uint64_t *__restrict__ ws, const uint64_t *__restrict__ in, long pairs, int log_n, int L, int K) {
+    pdl_begin();
     const long stride = (long)gridDim.x * blockDim.x;
     const long per_item = (long)K << log_n;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
@@ -55,6 +56,7 @@ k_moddown_conv(uint64_t *__restrict__ d, const uint64_t *__restrict__ src, long 
                int batch, int nearest, const ulonglong2 *__restrict__ garner, const ulonglong2 *__restrict__ mr,
                const uint64_t *__restrict__ hp, const uint64_t *__restrict__ hq, const ulonglong2 *__restrict__ pinv,
                const uint64_t *__restrict__ consts_q, const uint64_t *__restrict__ consts_p) {
+    pdl_begin();
     const long n = 1L << log_n;
     const long total = n * batch;
     const long stride = (long)gridDim.x * blockDim.x;
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(kThreads)
 k_moddown_finish(uint64_t *__restrict__ out, const uint64_t *__restrict__ in, const uint64_t *__restrict__ d,
                  long pairs, int log_n, int L, int K, const ulonglong2 *__restrict__ pinv,
                  const uint64_t *__restrict__ consts) {
+    pdl_begin();
     const long stride = (long)gridDim.x * blockDim.x;
     const long plane = (long)L << log_n;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
@@ -167,11 +170,11 @@ void launch_conv(uint64_t *d, const uint64_t *src, long src_item, int log_n, int
     const bool staged = L <= kMaxBasis;
     auto kern = fused ? (staged ? k_moddown_conv<MAXK, true, true> : k_moddown_conv<MAXK, true, false>)
                       : (staged ? k_moddown_conv<MAXK, false, true> : k_moddown_conv<MAXK, false, false>);
-    kern<<<grid, kThreads, 0, st>>>(d, src, src_item, log_n, L, K, batch, nearest ? 1 : 0,
-                                    (const ulonglong2 *)(md + lay.off_garner), (const ulonglong2 *)(md + lay.off_mr),
-                                    (const uint64_t *)(md + lay.off_hp), (const uint64_t *)(md + lay.off_hq),
-                                    (const ulonglong2 *)(md + lay.off_pinv), t_qp->consts,
-                                    t_qp->consts + (long)L * K_COUNT);
+    launch_pdl(kern, grid, kThreads, 0, st, d, src, src_item, log_n, L, K, batch, nearest ? 1 : 0,
+               (const ulonglong2 *)(md + lay.off_garner), (const ulonglong2 *)(md + lay.off_mr),
+               (const uint64_t *)(md + lay.off_hp), (const uint64_t *)(md + lay.off_hq),
+               (const ulonglong2 *)(md + lay.off_pinv), t_qp->consts,
+               t_qp->consts + (long)L * K_COUNT);
 }
 
 }  // namespace
@@ -193,7 +196,7 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
         if (r < 0) return -1;
         if (r == 0) {
             const long pairs = ((long)batch * K << log_n) / 2;
-            k_copy_limbs<<<stream_grid(pairs, kThreads, 8), kThreads, 0, st>>>(pl, in, pairs, log_n, L, K);
+            launch_pdl(k_copy_limbs, stream_grid(pairs, kThreads, 8), kThreads, 0, st, pl, in, pairs, log_n, L, K);
             if (cudaGetLastError() != cudaSuccess) return -1;
             launched++;
             r = launch_ntt(pl, log_n, K, (long)batch * K, &tp, true, stream);
@@ -220,8 +223,8 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
     if (r < 0) return -1;
     launched += r;
     const long pairs = ((long)batch * L << log_n) / 2;
-    k_moddown_finish<<<stream_grid(pairs, kThreads, 8), kThreads, 0, st>>>(
-        out, in, d, pairs, log_n, L, K, (const ulonglong2 *)(md + lay.off_pinv), t_qp->consts);
+    launch_pdl(k_moddown_finish, stream_grid(pairs, kThreads, 8), kThreads, 0, st, out, in, d, pairs, log_n, L, K,
+               (const ulonglong2 *)(md + lay.off_pinv), t_qp->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
     return launched + 1;
 }

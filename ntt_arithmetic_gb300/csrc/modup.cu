@@ -23,6 +23,7 @@
 
 #include "fhe_arith.cuh"
 #include "fhe_internal.h"
+#include "launch_util.h"
 
 namespace fhe {
 namespace {
@@ -34,6 +35,7 @@ __global__ void __launch_bounds__(kThreads)
 k_modup(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int dnum, int alpha,
         const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ garner, const ulonglong2 *__restrict__ mr,
         const uint64_t *__restrict__ consts) {
+    pdl_begin();
     // APPROX: `garner` holds the bracket constants [dnum][alpha] and `mr` the
     // CRT weights [dnum][LK][alpha] of the approximate conversion.
     const long n = 1L << log_n;

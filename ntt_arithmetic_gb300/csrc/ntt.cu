@@ -60,6 +60,7 @@
 
 #include "fhe_arith.cuh"
 #include "fhe_internal.h"
+#include "launch_util.h"
 #include "ntt_shapes.h"
 
 namespace fhe {
@@ -353,6 +354,7 @@ template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
           const uint64_t *__restrict__ consts) {
+    pdl_begin();
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     static_assert(SH::C == 1, "a row of more than one block takes the split kernels");
     extern __shared__ __align__(16) uint64_t sm[];
@@ -391,6 +393,7 @@ template <int LOGN, int LOGC, int LOGTPC>
 __global__ void __launch_bounds__(256, 4)
 k_ntt_fwd_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ulonglong2 *__restrict__ tw,
                const uint64_t *__restrict__ consts) {
+    pdl_begin();
     constexpr int C = 1 << LOGC, M = 1 << (LOGN - LOGC);
     constexpr int TPC = 1 << LOGTPC, LOGVPT = LOGC - LOGTPC, VPT = 1 << LOGVPT;
     constexpr int COLS = 256 / TPC, CPR = M / COLS;   // columns per CTA, CTAs per row
@@ -459,6 +462,7 @@ template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd_blk(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
               const uint64_t *__restrict__ consts) {
+    pdl_begin();
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
@@ -498,6 +502,7 @@ template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB, int DN>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd_blk_ip(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, const uint64_t *__restrict__ keys,
                  int LK, int batch, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts) {
+    pdl_begin();
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];   // [DN][M] digit blocks, then the staged twiddles
     const unsigned bid = gridDim.x - 1 - blockIdx.x;   // last rows first (still in L2)
@@ -573,6 +578,7 @@ __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_fwd_blk_md(uint64_t *__restrict__ out, const uint64_t *__restrict__ d, const uint64_t *__restrict__ in, int L,
                  int K, int batch, const ulonglong2 *__restrict__ tw, const uint64_t *__restrict__ consts,
                  const ulonglong2 *__restrict__ pinv) {
+    pdl_begin();
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     extern __shared__ __align__(16) uint64_t sm[];
     Ctx c;
@@ -722,6 +728,7 @@ template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_inv(uint64_t *__restrict__ res, int L, int batch, const ulonglong2 *__restrict__ tw,
           const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__ twist_tab) {
+    pdl_begin();
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
     static_assert(SH::C == 1, "a row of more than one block takes the split kernels");
     extern __shared__ __align__(16) uint64_t sm[];
@@ -762,6 +769,7 @@ template <int LOGN, int LOGC, int LOGT, int LOGE, int MINB>
 __global__ void __launch_bounds__(1 << LOGT, MINB)
 k_ntt_inv_blk(uint64_t *res, const uint64_t *src, long src_item, int L, int batch, const ulonglong2 *__restrict__ tw,
               const uint64_t *__restrict__ consts) {
+    pdl_begin();
     // reads row (b, l) at src + b src_item + l N (src = res, src_item = L N:
     // in place) and writes it to res + (b L + l) N
     using SH = Shape<LOGN, LOGC, LOGT, LOGE>;
@@ -805,6 +813,7 @@ template <int LOGN, int LOGC, int LOGTPC>
 __global__ void __launch_bounds__(256)
 k_ntt_inv_cols(uint64_t *__restrict__ res, int L, int batch, int chunk, const ulonglong2 *__restrict__ tw,
                const uint64_t *__restrict__ consts, const ulonglong2 *__restrict__ twist_tab) {
+    pdl_begin();
     constexpr int C = 1 << LOGC, M = 1 << (LOGN - LOGC);
     constexpr int TPC = 1 << LOGTPC, LOGVPT = LOGC - LOGTPC, VPT = 1 << LOGVPT;
     constexpr int COLS = 256 / TPC, CPR = M / COLS;   // columns per CTA, CTAs per row
@@ -886,14 +895,14 @@ int launch_shape(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, cudaS
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
-        kern<<<(unsigned)rows, SH::T, smem, st>>>(res, L, batch, reinterpret_cast<const ulonglong2 *>(t->inv),
+        launch_pdl(kern, (unsigned)rows, SH::T, smem, st, res, L, batch, reinterpret_cast<const ulonglong2 *>(t->inv),
                                                   t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
     } else {
         auto kern = k_ntt_fwd<LOGN, LOGC, LOGT, LOGE, MINB>;
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
-        kern<<<(unsigned)rows, SH::T, smem, st>>>(res, L, batch, reinterpret_cast<const ulonglong2 *>(t->fwd),
+        launch_pdl(kern, (unsigned)rows, SH::T, smem, st, res, L, batch, reinterpret_cast<const ulonglong2 *>(t->fwd),
                                                   t->consts);
     }
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
@@ -912,15 +921,15 @@ int launch_split_fwd(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, c
     // b + 1 while it transforms item b)
     const int nch = (batch + 3) / 4, chunk = (batch + nch - 1) / nch;
     const int nchunks = (batch + chunk - 1) / chunk;
-    k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)L * nchunks * CPR), 256, 0, st>>>(res, L, batch, chunk,
-                                                                                            tw, t->consts);
+    launch_pdl(k_ntt_fwd_cols<LOGN, LOGC, LOGTPC>, (unsigned)((long)L * nchunks * CPR), 256, 0, st, res, L, batch,
+               chunk, tw, t->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
     auto kern = k_ntt_fwd_blk<LOGN, LOGC, LOGT, LOGE, MINB>;
     const size_t smem = (size_t)SH::smem_words(false) * sizeof(uint64_t);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
-    kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, L, batch, tw, t->consts);
+    launch_pdl(kern, (unsigned)(rows * SH::C), SH::T, smem, st, res, L, batch, tw, t->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
     return 2;
 }
@@ -950,14 +959,14 @@ int launch_split_inv(uint64_t *res, int L, long rows, const fhe_ntt_tables *t, c
         src = res;
         src_item = (long)L << LOGN;
     }
-    kern<<<(unsigned)(rows * SH::C), SH::T, smem, st>>>(res, src, src_item, L, batch, tw, t->consts);
+    launch_pdl(kern, (unsigned)(rows * SH::C), SH::T, smem, st, res, src, src_item, L, batch, tw, t->consts);
     if (cudaGetLastError() != cudaSuccess) return -1;
     // batch items per column CTA: up to 4, balanced, so the staged twiddles
     // serve several items and the grid still spans several waves
     const int nch = (batch + 3) / 4, chunk = (batch + nch - 1) / nch;
     const int nchunks = (batch + chunk - 1) / chunk;
-    k_ntt_inv_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)L * nchunks * CPR), 256, 0, st>>>(
-        res, L, batch, chunk, tw, t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
+    launch_pdl(k_ntt_inv_cols<LOGN, LOGC, LOGTPC>, (unsigned)((long)L * nchunks * CPR), 256, 0, st, res, L, batch,
+               chunk, tw, t->consts, reinterpret_cast<const ulonglong2 *>(t->twist));
     if (cudaGetLastError() != cudaSuccess) return -1;
     return 2;
 }
@@ -983,15 +992,16 @@ int launch_fwd_ip_dn(uint64_t *out, uint64_t *ext, const uint64_t *keys, int LK,
         const int items = batch * DN;   // rows of one prime in ext: [batch][DN][LK][n]
         const int nch = (items + 3) / 4, chunk = (items + nch - 1) / nch;
         const int nchunks = (items + chunk - 1) / chunk;
-        k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)LK * nchunks * CPR), 256, 0, st>>>(ext, LK, items, chunk,
-                                                                                                tw, t->consts);
+        launch_pdl(k_ntt_fwd_cols<LOGN, LOGC, LOGTPC>, (unsigned)((long)LK * nchunks * CPR), 256, 0, st, ext, LK,
+                   items, chunk, tw, t->consts);
         if (cudaGetLastError() != cudaSuccess) return -1;
         auto kern = k_ntt_fwd_blk_ip<LOGN, LOGC, LOGT, LOGE, MINB, DN>;
         const size_t smem = (size_t)(DN * SH::M + 2 * SH::FWD_TW) * sizeof(uint64_t);
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
-        kern<<<(unsigned)((long)LK * SH::C * batch), SH::T, smem, st>>>(out, ext, keys, LK, batch, tw, t->consts);
+        launch_pdl(kern, (unsigned)((long)LK * SH::C * batch), SH::T, smem, st, out, ext, keys, LK, batch, tw,
+                   t->consts);
         if (cudaGetLastError() != cudaSuccess) return -1;
         return 2;
     }
@@ -1011,15 +1021,16 @@ int launch_fwd_md(uint64_t *out, uint64_t *d, const uint64_t *in, int L, int K, 
         const ulonglong2 *tw = reinterpret_cast<const ulonglong2 *>(t->fwd);
         const int nch = (batch + 3) / 4, chunk = (batch + nch - 1) / nch;
         const int nchunks = (batch + chunk - 1) / chunk;
-        k_ntt_fwd_cols<LOGN, LOGC, LOGTPC><<<(unsigned)((long)L * nchunks * CPR), 256, 0, st>>>(d, L, batch, chunk,
-                                                                                                tw, t->consts);
+        launch_pdl(k_ntt_fwd_cols<LOGN, LOGC, LOGTPC>, (unsigned)((long)L * nchunks * CPR), 256, 0, st, d, L, batch,
+                   chunk, tw, t->consts);
         if (cudaGetLastError() != cudaSuccess) return -1;
         auto kern = k_ntt_fwd_blk_md<LOGN, LOGC, LOGT, LOGE, MINB>;
         const size_t smem = (size_t)(SH::smem_words(false) + SH::M) * sizeof(uint64_t);
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return -1;
-        kern<<<(unsigned)((long)batch * L * SH::C), SH::T, smem, st>>>(out, d, in, L, K, batch, tw, t->consts, pinv);
+        launch_pdl(kern, (unsigned)((long)batch * L * SH::C), SH::T, smem, st, out, d, in, L, K, batch, tw, t->consts,
+                   pinv);
         if (cudaGetLastError() != cudaSuccess) return -1;
         return 2;
     }

@@ -19,6 +19,7 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
 k_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
       const uint64_t *__restrict__ consts) {
+    pdl_begin();
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
         const long e = 2 * i;
@@ -34,6 +35,7 @@ k_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, long pairs, int log_n
 __global__ void __launch_bounds__(kThreads)
 k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
          const uint64_t *__restrict__ consts) {
+    pdl_begin();
     const long plane = (long)L << log_n;
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
@@ -73,6 +75,7 @@ template <int DN>
 __global__ void __launch_bounds__(kThreads)
 k_ks_ip(uint64_t *out, const uint64_t *ext, const uint64_t *keys, long pairs, int log_n, int LK, int dnum_rt,
         int batch, const uint64_t *__restrict__ consts) {
+    pdl_begin();
     const int dnum = DN > 0 ? DN : dnum_rt;
     const long plane = (long)LK << log_n;      // one [LK][n] block
     const long stride = (long)gridDim.x * blockDim.x;
