@@ -54,6 +54,9 @@ extern "C" {
 #define FHE_ESPACE (-4)    /* workspace or host buffer too small */
 #define FHE_EDEVICE (-5)   /* host pointer where a device pointer is required, or mixed devices */
 
+/* Bits of the device status word (fhe_device_status). */
+#define FHE_STATUS_TC_TIMEOUT 1   /* a tensor-core kernel gave up waiting for its MMA: its outputs are invalid */
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int fhe_version(void);
 
@@ -165,6 +168,16 @@ int fhe_ntt_inv(uint64_t *res, int log_n, int L, int batch, const fhe_ntt_tables
  * 1 <= ctas <= 1048576, 1 <= iters <= 128 (the lazy bound of the residues),
  * else FHE_EINVAL.  One launch on `stream`, no host sync. */
 int fhe_butterfly_probe(uint64_t *out, int ctas, int iters, const fhe_ntt_tables *t, void *stream);
+
+/* Device status word.  Kernels that wait on the tensor cores (the ModUp of
+ * fhe_keyswitch_ip and the other key-switch calls, for digits of at most 8
+ * primes) bound every wait (200 ms); one that gives up sets a
+ * FHE_STATUS_* bit here, releases its tensor memory and returns, leaving the
+ * context usable.  Waits for all work on the current device
+ * (cudaDeviceSynchronize), then writes the word to *status and, if reset is
+ * nonzero, clears it.  FHE_EINVAL for a null status, FHE_ECUDA if the
+ * synchronization or the copy fails. */
+int fhe_device_status(int *status, int reset);
 
 /* ---- NTT-domain kernels ------------------------------------------------ */
 

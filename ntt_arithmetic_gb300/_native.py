@@ -93,6 +93,7 @@ SIGNATURES = {
                                         ctypes.POINTER(NttTables), _vp, _vp]),
     "fhe_keyswitch_noalloc_max_bytes": (_size, []),
     "fhe_butterfly_probe": (_int, [_vp, _int, _int, ctypes.POINTER(NttTables), _vp]),
+    "fhe_device_status": (_int, [ctypes.POINTER(_int), _int]),
 }
 
 _lib = None

@@ -65,6 +65,15 @@ def launch_count() -> int:
     return int(N.lib().fhe_launch_count())
 
 
+def device_status(reset: bool = True) -> int:
+    """The library's device status word (fhe_device_status): 0 unless a
+    tensor-core kernel gave up a bounded wait (FHE_STATUS_TC_TIMEOUT).
+    Synchronizes the device; clears the word when `reset`."""
+    v = ctypes.c_int(0)
+    N.call("fhe_device_status", ctypes.byref(v), 1 if reset else 0)
+    return int(v.value)
+
+
 def butterfly_probe(out: torch.Tensor, iters: int, tables: "NttTables", stream=None) -> int:
     """Launch the butterfly throughput probe (fhe_butterfly_probe) with one
     CTA of 256 threads per 256 words of `out`; returns the number of

@@ -18,8 +18,8 @@ OUT = os.path.join(HERE, "libfhe_ntt.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["ntt.cu", "pointwise.cu", "automorph.cu", "modup.cu", "abi.cu", "keyswitch_noalloc.cu", "moddown.cu", "bconv.cu",
-           "hoisted.cu", "probe.cu", "tables.cpp"]
-HEADERS = ["fhe_arith.cuh", "fhe_internal.h", "launch_util.h", "ntt_shapes.h"]
+           "hoisted.cu", "probe.cu", "modup_tc.cu", "tables.cpp"]
+HEADERS = ["fhe_arith.cuh", "fhe_internal.h", "launch_util.h", "ntt_shapes.h", "tc_util.cuh"]
 
 
 def nvcc() -> str:

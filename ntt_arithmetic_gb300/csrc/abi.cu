@@ -115,6 +115,11 @@ extern "C" const char *fhe_status_str(int s) {
 
 extern "C" uint64_t fhe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+extern "C" int fhe_device_status(int *status, int reset) {
+    if (!status) return FHE_EINVAL;
+    return device_status(status, reset != 0);
+}
+
 extern "C" int fhe_butterfly_probe(uint64_t *out, int ctas, int iters, const fhe_ntt_tables *t, void *stream) {
     if (!out || !aligned16(out) || ctas < 1 || ctas > (1 << 20) || iters < 1 || iters > 128) return FHE_EINVAL;
     if (!t || t->log_n < 11) return FHE_EINVAL;

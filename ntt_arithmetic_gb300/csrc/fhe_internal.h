@@ -22,6 +22,21 @@ struct ModupDigit {
     int32_t lo;      // first limb of the digit
     int32_t count;   // limbs in the digit (<= alpha)
 };
+// One target prime of a digit's tensor-core extension (modup_tc.cu).
+struct ModupTcTarget {
+    uint64_t p;      // the target prime
+    uint64_t w28;    // 2^28 mod p
+    uint64_t w28p;   // floor(w28 2^64 / p), its Shoup companion
+    uint64_t limb;   // index of p in the extended basis
+};
+// The tensor-core extension takes digits of up to kTcMaxAlpha primes: one
+// digit's mixed-radix digits are 8 alpha = 64 fp16 byte limbs (K), and the
+// accumulators of up to kTcTargetsPerGroup targets (8 columns each) fill the
+// 128 TMEM columns a CTA holds.
+constexpr int kTcMaxAlpha = 8;
+constexpr int kTcTargetsPerGroup = 16;
+constexpr int kTcRowBytes = 8 * kTcMaxAlpha * 2;   // one operand row: 64 fp16
+
 struct ModupLayout {
     int alpha;
     size_t off_digits;   // [dnum] ModupDigit
@@ -29,6 +44,11 @@ struct ModupLayout {
     size_t off_mr;       // [dnum][L+K][alpha] split factors: prod_{b<a} d_b mod qp_l (exact)
     size_t off_qinv;     // [dnum][alpha] pairs: (D_j / d_a)^-1 mod d_a                (approximate)
     size_t off_qhat;     // [dnum][L+K][alpha] split factors: (D_j / d_a) mod qp_l     (approximate)
+    // tensor-core extension (alpha <= kTcMaxAlpha; tc_tmax = 0 otherwise):
+    int tc_tmax;         // target slots per digit (L+K rounded up to even)
+    size_t off_tc_tgt;   // [dnum][tc_tmax] ModupTcTarget
+    size_t off_tc_bx;    // [dnum][8 tc_tmax rows][64] fp16 weight limbs, operand layout (exact)
+    size_t off_tc_ba;    // the same for the approximate conversion
     size_t bytes;
 };
 ModupLayout modup_layout(int L, int K, int dnum);
@@ -79,6 +99,13 @@ int launch_automorph(uint64_t *out, const uint64_t *in, int log_n, int L, long r
                      int domain, const fhe_ntt_tables *t, void *stream);
 int launch_modup(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
                  bool approx, const fhe_ntt_tables *t, const void *modup, void *stream);
+// The tensor-core ModUp (modup_tc.cu); returns 0 without launching when the
+// shape has no tensor-core form (alpha > kTcMaxAlpha, n < 128).
+int launch_modup_tc(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
+                    bool approx, const fhe_ntt_tables *t, const void *modup, void *stream);
+// Synchronize the device, then read (and optionally clear) the status word
+// of the tensor-core kernels.
+int device_status(int *status, bool reset);
 int launch_ks_ip_aut(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum,
                      int batch, int R, const GaloisSet &g, const fhe_ntt_tables *t, void *stream);
 int launch_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int batch, bool approx,

@@ -140,6 +140,8 @@ void launch_modup_t(uint64_t *ext, const uint64_t *in, long in_stride, int log_n
 int launch_modup(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
                  bool approx, const fhe_ntt_tables *t, const void *modup, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
+    const int tc = launch_modup_tc(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, stream);
+    if (tc != 0) return tc;   // the tensor-core extension ran (or failed to launch)
     const int alpha = modup_layout(L, K, dnum).alpha;
     if (alpha <= 1) launch_modup_t<1>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);
     else if (alpha <= 2) launch_modup_t<2>(ext, in, in_stride, log_n, L, K, dnum, batch, approx, t, modup, st);

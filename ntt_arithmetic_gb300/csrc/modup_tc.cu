@@ -1,0 +1,250 @@
+// modup_tc.cu -- ModUp's basis extension as a tensor-core contraction.
+//
+// For digit j (primes d_0..d_{c-1}) every coefficient's extension to a
+// target prime p is the dot product sum_a v_a W_{a,p} of its c mixed-radix
+// digits v_a (Garner, exact) or CRT brackets v_a = [x_a (D_j/d_a)^-1]_{d_a}
+// (approximate) with per-digit weights W -- the "mixed-radix decomposition
+// and basis extension" of FHElium's CUDA layer ("Eager, Compile, and native
+// execution", section "CUDA execution") and the "Garner extension" of the
+// kestrel-llm chain (overview, section 4.2).  Over a tile of 128
+// coefficients and all targets this is a dense 128 x (8 targets) x (8 c)
+// contraction, which this kernel runs on the tensor cores exactly:
+//
+//  * each v_a < 2^50 is split into bytes b_{a,e}; the A operand row of a
+//    coefficient holds the fp16 values 1024 + b_{a,e} (bit pattern
+//    0x6400 | b, one byte permute per two elements);
+//  * the B operand (built on the host, tables.cpp: tc_weight_image) holds the
+//    7-bit limbs of W_{a,p} 2^(8e) mod p plus offset columns, so that every
+//    f32 accumulator is 2^23 + (an integer below 2^21): products and sums of
+//    integers below 2^24 are exact in f32, and the accumulator's bit pattern
+//    minus 0x4B000000 is the integer;
+//  * the eight accumulators u_s of a target recombine as
+//    sum_s u_s 2^(7s) = (u_0 + .. + u_3 2^21) + 2^28 (u_4 + .. + u_7 2^21),
+//    reduced with one Shoup product by 2^28 mod p to a value below 5 p (the
+//    forward NTT that follows takes inputs of that size).
+//
+// The integer pipes keep Garner's recursion (c (c - 1) / 2 Shoup products per
+// coefficient) and one Shoup product per output; the c multiply-accumulates
+// per output of the integer kernel (modup.cu) move to the tensor cores.
+//
+// CTA: 128 threads, thread m owns coefficient m of the tile and row m of the
+// accumulator (TMEM lane m).  Persistent over the tiles of one digit: the
+// digit's B operand and target constants are staged in shared memory once.
+// Targets are processed in groups of up to 16 (N = 128 columns), one MMA
+// chain of K = 64 (4 instructions) per group into the CTA's 128 TMEM columns.
+#include <cuda_runtime.h>
+
+#include "fhe_arith.cuh"
+#include "fhe_internal.h"
+#include "launch_util.h"
+#include "tc_util.cuh"
+
+namespace fhe {
+
+// Status word of the tensor-core kernels (FHE_STATUS_* bits), read and
+// cleared by fhe_device_status.
+__device__ int g_fhe_status;
+
+namespace {
+
+constexpr int kTcThreads = 128;                      // M = 128: one row per thread
+constexpr int kTileBytesA = 128 * kTcRowBytes;       // A operand, 16 KB
+constexpr uint32_t kCoreK = 128;                     // bytes between cores adjacent along K
+constexpr uint32_t kCoreRows = kTcMaxAlpha * 128;    // bytes between cores adjacent along the rows
+constexpr uint64_t kTcWaitNs = 200000000ull;         // give up an MMA wait after 200 ms
+constexpr uint32_t kF32Offset = 0x4B000000u;         // f32 bit pattern of 2^23
+
+// Shared memory of one CTA for a digit with T targets (padded to even).
+__host__ __device__ constexpr size_t tc_smem_bytes(int T) {
+    return (size_t)kTileBytesA + (size_t)((T + 1) & ~1) * 8 * kTcRowBytes + (size_t)T * sizeof(ModupTcTarget);
+}
+
+template <bool APPROX>
+__global__ void __launch_bounds__(kTcThreads, 4)
+k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int batch,
+           int alpha, const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ gconst,
+           const ModupTcTarget *__restrict__ tgt, const uint4 *__restrict__ wimg, int tmax,
+           const uint64_t *__restrict__ consts) {
+    pdl_begin();
+    // APPROX: gconst holds the brackets' constants [dnum][alpha], else Garner's [dnum][alpha][alpha].
+    extern __shared__ __align__(1024) uint8_t sm[];   // [A operand][B operand][targets]
+    __shared__ uint64_t mbar;
+    __shared__ uint32_t tslot;
+    const int t = threadIdx.x, warp = t >> 5;
+    const int j = blockIdx.y, dnum = gridDim.y;
+    const int lo = dg[j].lo, cnt = dg[j].count, T = LK - cnt, Tp = (T + 1) & ~1;
+    uint8_t *sA = sm, *sB = sm + kTileBytesA;
+    ModupTcTarget *sT = reinterpret_cast<ModupTcTarget *>(sB + (size_t)Tp * 8 * kTcRowBytes);
+    {
+        const uint4 *src = wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16;
+        for (int e = t; e < Tp * 8 * kTcRowBytes / 16; e += kTcThreads)
+            reinterpret_cast<uint4 *>(sB)[e] = __ldg(src + e);
+        for (int e = t; e < T; e += kTcThreads) sT[e] = tgt[(size_t)j * tmax + e];
+    }
+    if (warp == 0) tmem_alloc(&tslot, 128);
+    if (t == 0) mbar_init(&mbar, 1);
+    fence_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tslot, lanes = (uint32_t)(32 * warp) << 16;
+    const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
+    uint8_t *arow = sA + (t >> 3) * kCoreRows + (t & 7) * 16;   // this thread's operand row
+    const ulonglong2 *gj = gconst + (long)j * alpha * (APPROX ? 1 : alpha);
+    const long tiles_per_item = (1L << log_n) >> 7;
+    const long tiles = (long)batch * tiles_per_item;
+    uint32_t phase = 0;
+    bool ok = true;
+    // the residues of the CTA's next tile are loaded while the current one is converted
+    uint64_t xn[kTcMaxAlpha];
+    auto load_tile = [&](long tile) {
+        const int bi = (int)(tile / tiles_per_item);
+        const uint64_t *src = in + (long)bi * in_stride + ((long)lo << log_n) +
+                              ((tile - (long)bi * tiles_per_item) << 7) + t;
+#pragma unroll
+        for (int a = 0; a < kTcMaxAlpha; a++) xn[a] = a < cnt ? __ldcs(src + ((long)a << log_n)) : 0;
+    };
+    if (blockIdx.x < tiles) load_tile(blockIdx.x);
+    for (long tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+        const int bi = (int)(tile / tiles_per_item);
+        const long i = ((tile - (long)bi * tiles_per_item) << 7) + t;
+        uint64_t x[kTcMaxAlpha], v[kTcMaxAlpha];
+#pragma unroll
+        for (int a = 0; a < kTcMaxAlpha; a++) x[a] = xn[a];
+        if (tile + gridDim.x < tiles) load_tile(tile + gridDim.x);
+        if constexpr (APPROX) {
+#pragma unroll
+            for (int a = 0; a < kTcMaxAlpha; a++) {
+                v[a] = 0;
+                if (a < cnt) {
+                    const uint64_t d = __ldg(consts + (long)(lo + a) * K_COUNT + K_Q);
+                    const ulonglong2 c = __ldg(gj + a);
+                    v[a] = reduce4(shoup_lazy(x[a], c.x, c.y, d), d);
+                }
+            }
+        } else {
+            v[0] = x[0];
+#pragma unroll
+            for (int a = 1; a < kTcMaxAlpha; a++) {
+                v[a] = 0;
+                if (a < cnt) {
+                    const uint64_t d = __ldg(consts + (long)(lo + a) * K_COUNT + K_Q);
+                    uint64_t u = x[a];
+#pragma unroll
+                    for (int b = 0; b < a; b++) {
+                        const ulonglong2 c = __ldg(gj + a * alpha + b);
+                        u = shoup_lazy(u + 4 * d - v[b], c.x, c.y, d);   // v_b < 2^50 < 4 d
+                    }
+                    v[a] = reduce4(u, d);
+                }
+            }
+        }
+        uint64_t *dst = ext + (((long)bi * dnum + j) * LK << log_n) + i;
+#pragma unroll
+        for (int a = 0; a < kTcMaxAlpha; a++)
+            if (a < cnt) __stcs(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
+        // A operand row: fp16 1024 + byte, eight per digit (byte 7 of v_a < 2^50 is 0)
+#pragma unroll
+        for (int a = 0; a < kTcMaxAlpha; a++) {
+            const uint32_t vl = (uint32_t)v[a], vh = (uint32_t)(v[a] >> 32);
+            uint4 row;
+            row.x = __byte_perm(vl, 0x64646464u, 0x4140);
+            row.y = __byte_perm(vl, 0x64646464u, 0x4342);
+            row.z = __byte_perm(vh, 0x64646464u, 0x4140);
+            row.w = __byte_perm(vh, 0x64646464u, 0x4342);
+            *reinterpret_cast<uint4 *>(arow + a * kCoreK) = row;
+        }
+        fence_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        for (int g0 = 0; g0 < T; g0 += kTcTargetsPerGroup) {
+            const int gcnt = min(kTcTargetsPerGroup, T - g0);
+            if (t == 0) {
+                const uint32_t idesc = tc_idesc_f16_f32(8 * ((gcnt + 1) & ~1));
+#pragma unroll
+                for (int ks = 0; ks < kTcMaxAlpha / 2; ks++)
+                    tc_mma_f16(tmem, tc_smem_desc(a_addr + ks * 2 * kCoreK, kCoreK, kCoreRows),
+                               tc_smem_desc(b_addr + g0 * 8 * kTcRowBytes + ks * 2 * kCoreK, kCoreK, kCoreRows),
+                               idesc, ks > 0);
+                tc_commit(&mbar);
+            }
+            const bool done = mbar_wait(&mbar, phase, kTcWaitNs);
+            phase ^= 1;
+            ok = __syncthreads_and(done);
+            if (!ok) break;
+            tc_fence_after_sync();
+            for (int tt = 0; tt < gcnt; tt += 4) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lanes + 8 * tt, r);   // targets tt .. tt + 3 (columns inside the group's N)
+#pragma unroll
+                for (int h = 0; h < 4; h++) {
+                    if (tt + h < gcnt) {
+                        const uint32_t *u = r + 8 * h;
+                        const uint64_t l4 = (uint64_t)(u[0] - kF32Offset) + ((uint64_t)(u[1] - kF32Offset) << 7) +
+                                            ((uint64_t)(u[2] - kF32Offset) << 14) +
+                                            ((uint64_t)(u[3] - kF32Offset) << 21);
+                        const uint64_t h4 = (uint64_t)(u[4] - kF32Offset) + ((uint64_t)(u[5] - kF32Offset) << 7) +
+                                            ((uint64_t)(u[6] - kF32Offset) << 14) +
+                                            ((uint64_t)(u[7] - kF32Offset) << 21);
+                        const ModupTcTarget &tg = sT[g0 + tt + h];
+                        __stcs(dst + ((long)tg.limb << log_n), l4 + shoup_lazy(h4, tg.w28, tg.w28p, tg.p));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncthreads();   // every lane's TMEM reads are done before the next MMA overwrites them
+            tc_fence_after_sync();
+        }
+    }
+    if (!ok) {
+        if (t == 0) atomicOr(&g_fhe_status, FHE_STATUS_TC_TIMEOUT);
+        mbar_wait(&mbar, phase ^ 1, kTcWaitNs);   // let the abandoned MMA finish before its columns are freed
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+}  // namespace
+
+int launch_modup_tc(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
+                    bool approx, const fhe_ntt_tables *t, const void *modup, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const ModupLayout lay = modup_layout(L, K, dnum);
+    if (lay.tc_tmax == 0 || log_n < 7) return 0;
+    const int LK = L + K;
+    const int cnt_min = L - (dnum - 1) * lay.alpha;   // the last digit is the smallest
+    const size_t need = tc_smem_bytes(LK - cnt_min);
+    // at least 46 KB per CTA: at most 4 CTAs per SM, whose 4 x 128 TMEM columns fit the SM's 512
+    const size_t smem = need > 47104 ? need : 47104;
+    auto kern = approx ? k_modup_tc<true> : k_modup_tc<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
+    const int per_sm = (int)(228 * 1024 / (smem + 1024)) < 4 ? (int)(228 * 1024 / (smem + 1024)) : 4;
+    const long tiles = (long)batch << (log_n - 7);
+    // every CTA resident at once (a CTA left for a second wave would run its tiles alone at the end)
+    long gx = (long)sm_count() * per_sm / dnum;
+    if (gx < 1) gx = 1;
+    if (gx > tiles) gx = tiles;
+    const char *base = (const char *)modup;
+    kern<<<dim3((unsigned)gx, (unsigned)dnum), kTcThreads, smem, st>>>(
+        ext, in, in_stride, log_n, LK, batch, lay.alpha, (const ModupDigit *)(base + lay.off_digits),
+        (const ulonglong2 *)(base + (approx ? lay.off_qinv : lay.off_garner)),
+        (const ModupTcTarget *)(base + lay.off_tc_tgt), (const uint4 *)(base + (approx ? lay.off_tc_ba : lay.off_tc_bx)),
+        lay.tc_tmax, t->consts);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+int device_status(int *status, bool reset) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return FHE_ECUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fhe_status, sizeof(int)) != cudaSuccess) return FHE_ECUDA;
+    if (reset && v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_fhe_status, &zero, sizeof(int)) != cudaSuccess) return FHE_ECUDA;
+    }
+    *status = v;
+    return FHE_OK;
+}
+
+}  // namespace fhe

@@ -110,7 +110,12 @@ ModupLayout modup_layout(int L, int K, int dnum) {
     s.off_mr = align256(s.off_garner + (size_t)dnum * s.alpha * s.alpha * 16);
     s.off_qinv = align256(s.off_mr + (size_t)dnum * LK * s.alpha * 16);
     s.off_qhat = align256(s.off_qinv + (size_t)dnum * s.alpha * 16);
-    s.bytes = align256(s.off_qhat + (size_t)dnum * LK * s.alpha * 16);
+    const size_t end = align256(s.off_qhat + (size_t)dnum * LK * s.alpha * 16);
+    s.tc_tmax = s.alpha <= kTcMaxAlpha ? (LK + 1) & ~1 : 0;
+    s.off_tc_tgt = end;
+    s.off_tc_bx = align256(s.off_tc_tgt + (size_t)dnum * s.tc_tmax * sizeof(ModupTcTarget));
+    s.off_tc_ba = align256(s.off_tc_bx + (size_t)dnum * s.tc_tmax * 8 * kTcRowBytes);
+    s.bytes = align256(s.off_tc_ba + (size_t)dnum * s.tc_tmax * 8 * kTcRowBytes);
     return s;
 }
 
@@ -278,6 +283,56 @@ extern "C" int fhe_modup_tables_bytes(int L, int K, int dnum, size_t *bytes) {
 //  Extension:             X mod p = v_0 + sum_{i>=1} v_i (d_0 ... d_{i-1} mod p)
 //                                                                    -> mr[l][i] = d_0..d_{i-1} mod p_l
 // Both with Shoup companions (pairs of words).
+// fp16 bits of an integer 0 <= v <= 2048 (all exactly representable).
+static uint16_t fp16_of_int(int v) {
+    if (v == 0) return 0;
+    const int e = 31 - __builtin_clz((unsigned)v);
+    const int m = e <= 10 ? v << (10 - e) : v >> (e - 10);
+    return (uint16_t)(((e + 15) << 10) | (m & 0x3FF));
+}
+
+// The tensor-core extension's weight operand for one digit of cnt primes and
+// T targets.  With the digit's mixed-radix (or CRT) digits v_a split into
+// bytes b_{a,e} (e = 0..6; v_a < 2^50), the extension of target p is
+//   sum_a v_a W_{a,p} = sum_{a,e} b_{a,e} (W_{a,p} 2^(8e) mod p)   (mod p),
+// and each constant c = W_{a,p} 2^(8e) mod p < 2^56 is split into eight
+// 7-bit limbs c_s.  Operand row 8 t + s (target t, limb s), column 8 a + e,
+// holds c_s; the kernel's other operand holds 1024 + b_{a,e} (the fp16 bit
+// pattern 0x6400 | b), so accumulator column 8 t + s receives
+//   1024 * (row sum) + sum_{a,e} b_{a,e} c_s.
+// Column 8 a + 7 (byte 7 of v_a, always 0) holds integers <= 2048 that make
+// every row sum 8192: each accumulator is then 2^23 + (a value < 2^21) and
+// its f32 bit pattern minus 0x4B000000 is that value.  Rows of the odd
+// target that pads T to even carry only the 8192.
+static void tc_weight_image(uint8_t *img, int cnt, int T, const uint64_t *W, const uint64_t *P) {
+    const int Tp = (T + 1) & ~1;
+    for (int t = 0; t < Tp; t++) {
+        for (int s = 0; s < 8; s++) {
+            int val[8 * kTcMaxAlpha] = {0};
+            int sum = 0;
+            for (int a = 0; t < T && a < cnt; a++) {
+                uint64_t c = W[(size_t)a * T + t];
+                for (int e = 0; e < 7; e++, c = mul_mod(c, 256, P[t])) {
+                    val[8 * a + e] = (int)((c >> (7 * s)) & 127);
+                    sum += val[8 * a + e];
+                }
+            }
+            int rem = 8192 - sum;   // sum <= 7 * 8 * 127 = 7112
+            for (int a = 0; a < kTcMaxAlpha; a++) {
+                const int v = rem < 2048 ? rem : 2048;
+                val[8 * a + 7] = v;
+                rem -= v;
+            }
+            const int n = 8 * t + s;
+            for (int k = 0; k < 8 * kTcMaxAlpha; k++) {
+                const uint16_t h = fp16_of_int(val[k]);
+                std::memcpy(img + ((size_t)(n >> 3) * kTcMaxAlpha + (k >> 3)) * 128 + (n & 7) * 16 + (k & 7) * 2, &h,
+                            2);
+            }
+        }
+    }
+}
+
 extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_t *qp, void *host_blob,
                                            size_t bytes) {
     if (!qp || !host_blob || !modup_shape_ok(L, K, dnum)) return FHE_EINVAL;
@@ -334,6 +389,34 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
                     if (b != a) hp = mul_mod(hp, qp[lo + b] % p, p);
                 split25_store(hp, qh + (l * alpha + a) * 2);
             }
+        }
+        if (lay.tc_tmax > 0) {
+            // the digit's targets (every prime outside it) and both weight operands
+            const int cnt = hi - lo, T = LK - cnt;
+            ModupTcTarget *tg = (ModupTcTarget *)(base + lay.off_tc_tgt) + (size_t)j * lay.tc_tmax;
+            std::vector<uint64_t> P(T), Wx((size_t)cnt * T), Wa((size_t)cnt * T);
+            for (int l = 0, t = 0; l < LK; l++) {
+                if (l >= lo && l < hi) continue;
+                const uint64_t p = qp[l];
+                tg[t].p = p;
+                tg[t].w28 = (1ull << 28) % p;
+                tg[t].w28p = shoup(tg[t].w28, p);
+                tg[t].limb = (uint64_t)l;
+                P[t] = p;
+                uint64_t prod = 1 % p;
+                for (int a = 0; a < cnt; a++) {
+                    Wx[(size_t)a * T + t] = prod;   // d_0 ... d_{a-1} mod p
+                    prod = mul_mod(prod, qp[lo + a] % p, p);
+                    uint64_t hp = 1 % p;
+                    for (int b = 0; b < cnt; b++)
+                        if (b != a) hp = mul_mod(hp, qp[lo + b] % p, p);
+                    Wa[(size_t)a * T + t] = hp;     // (D_j / d_a) mod p
+                }
+                t++;
+            }
+            const size_t img = (size_t)lay.tc_tmax * 8 * kTcRowBytes;
+            tc_weight_image((uint8_t *)(base + lay.off_tc_bx) + j * img, cnt, T, Wx.data(), P.data());
+            tc_weight_image((uint8_t *)(base + lay.off_tc_ba) + j * img, cnt, T, Wa.data(), P.data());
         }
     }
     return FHE_OK;

@@ -1,0 +1,156 @@
+"""Host-side check of the tensor-core ModUp's encoding (no GPU).
+
+The tensor-core extension (csrc/modup_tc.cu) computes each target residue of
+a digit's basis extension as an exact fp16 x fp16 -> f32 contraction: the A
+operand row of a coefficient holds 1024 + b for every byte b of its
+mixed-radix digits v_a (exact) or CRT brackets (approximate), the B operand --
+written by the library's host builder into the ModUp table blob -- holds the
+7-bit limbs of the weights W_{a,p} 2^(8e) mod p and offset columns, every
+accumulator must come out as 2^23 + (an integer below 2^21), and the eight
+accumulators of a target recombine as sum_s u_s 2^(7s).
+
+Here the contraction is replayed in exact integer arithmetic from the blob
+the library builds (fhe_modup_tables_build_host), with the digits v_a taken
+from Python integers (the mixed-radix digits of the CRT value), and the
+result is compared with the oracle's ModUp (modup_batch).  A wrong weight, a
+wrong limb order, a wrong offset column, an operand row in the wrong place of
+the layout or a wrong target list fails here without a GPU.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from ntt_arithmetic_gb300 import _native as N
+from ntt_arithmetic_gb300 import build as B
+
+ROWB = 128          # bytes of one operand row: 64 fp16
+MAXA = 8            # digits of up to 8 primes take the tensor-core path
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.lib()
+
+
+def a256(x: int) -> int:
+    return (x + 255) & ~255
+
+
+def layout(L: int, K: int, dnum: int) -> dict:
+    """The ModUp blob's layout (the sections the tensor-core kernel reads)."""
+    alpha = -(-L // dnum)
+    LK = L + K
+    off_garner = a256(dnum * 8)
+    off_mr = a256(off_garner + dnum * alpha * alpha * 16)
+    off_qinv = a256(off_mr + dnum * LK * alpha * 16)
+    off_qhat = a256(off_qinv + dnum * alpha * 16)
+    end = a256(off_qhat + dnum * LK * alpha * 16)
+    tmax = (LK + 1) & ~1 if alpha <= MAXA else 0
+    off_tgt = end
+    off_bx = a256(off_tgt + dnum * tmax * 32)
+    off_ba = a256(off_bx + dnum * tmax * 8 * ROWB)
+    return {"alpha": alpha, "tmax": tmax, "tgt": off_tgt, "bx": off_bx, "ba": off_ba,
+            "bytes": a256(off_ba + dnum * tmax * 8 * ROWB)}
+
+
+def fp16_int(bits: np.ndarray) -> np.ndarray:
+    """Integer values of fp16 bit patterns holding integers (exact)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64).astype(np.int64)
+
+
+def weight_operand(blob: np.ndarray, off: int, rows: int) -> np.ndarray:
+    """[rows][64] integers of an operand image: core (r/8, k/8) at ((r/8) 8 + k/8) 128, row r%8 at +16 (r%8)."""
+    img = blob[off:off + rows * ROWB].view(np.uint16)
+    out = np.zeros((rows, 64), dtype=np.int64)
+    for r in range(rows):
+        for kc in range(8):
+            base = (((r >> 3) * 8 + kc) * ROWB + (r & 7) * 16) // 2
+            out[r, 8 * kc:8 * kc + 8] = fp16_int(img[base:base + 8])
+    return out
+
+
+def build_blob(lib, L, K, dnum, qp):
+    nb = ctypes.c_size_t()
+    assert lib.fhe_modup_tables_bytes(L, K, dnum, ctypes.byref(nb)) == 0
+    blob = np.zeros(nb.value, dtype=np.uint8)
+    arr = (ctypes.c_uint64 * len(qp))(*[int(q) for q in qp])
+    assert lib.fhe_modup_tables_build_host(L, K, dnum, arr, blob.ctypes.data_as(ctypes.c_void_p), nb.value) == 0
+    return blob
+
+
+def replay(blob, lay, qp, L, K, dnum, x, approx):
+    """The tensor-core kernel's arithmetic on coefficients x [L][m] (ints) -> [dnum][L+K][m]."""
+    LK, alpha, tmax = L + K, lay["alpha"], lay["tmax"]
+    m = len(x[0])
+    out = np.zeros((dnum, LK, m), dtype=object)
+    tg = blob[lay["tgt"]:lay["tgt"] + dnum * tmax * 32].view(np.uint64).reshape(dnum, tmax, 4)
+    for j in range(dnum):
+        lo = j * alpha
+        cnt = min(alpha, L - lo)
+        d = [int(q) for q in qp[lo:lo + cnt]]
+        T = LK - cnt
+        Tp = (T + 1) & ~1
+        Bw = weight_operand(blob, lay["ba" if approx else "bx"] + j * tmax * 8 * ROWB, 8 * Tp)
+        assert (Bw.sum(axis=1) == 8192).all(), "every weight row sums to 8192 (the 2^23 offset)"
+        assert (Bw <= 2048).all() and (Bw >= 0).all()
+        Dj = math.prod(d)
+        A = np.full((m, 64), 1024, dtype=np.int64)
+        for c in range(m):
+            xs = [int(x[lo + a][c]) for a in range(cnt)]
+            if approx:
+                v = [xs[a] * pow(Dj // d[a], -1, d[a]) % d[a] for a in range(cnt)]
+            else:   # mixed-radix digits of the CRT value: what Garner's recursion returns
+                X = sum(xs[a] * (Dj // d[a]) * pow(Dj // d[a], -1, d[a]) for a in range(cnt)) % Dj
+                v = []
+                for a in range(cnt):
+                    v.append(X % d[a])
+                    X //= d[a]
+            for a in range(cnt):
+                assert v[a] < 1 << 50
+                for e in range(8):
+                    A[c, 8 * a + e] = 1024 + ((v[a] >> (8 * e)) & 255)
+            for a in range(cnt):
+                out[j, lo + a, c] = xs[a]
+        Dacc = A @ Bw.T                         # exact: every value < 2^24
+        assert (Dacc >= 1 << 23).all() and (Dacc < (1 << 23) + (1 << 21)).all()
+        U = Dacc - (1 << 23)
+        for t in range(T):
+            p, limb = int(tg[j, t, 0]), int(tg[j, t, 3])
+            assert p == int(qp[limb]) and not (lo <= limb < lo + cnt)
+            assert int(tg[j, t, 1]) == (1 << 28) % p
+            for c in range(m):
+                S = sum(int(U[c, 8 * t + s]) << (7 * s) for s in range(8))
+                out[j, limb, c] = S % p
+    return out
+
+
+@pytest.mark.parametrize("L,K,dnum,approx", [(24, 8, 3, False), (24, 8, 3, True), (7, 3, 3, False),
+                                              (5, 2, 1, False), (16, 4, 2, True)])
+def test_tensor_core_modup_encoding(lib, L, K, dnum, approx):
+    qp = [int(v) for v in oracle.primes(1 << 12, L + K)]
+    lay = layout(L, K, dnum)
+    blob = build_blob(lib, L, K, dnum, qp)
+    assert blob.size == lay["bytes"], "the layout replayed here matches the library's"
+    assert lay["tmax"] > 0
+    rng = np.random.default_rng(L * 100 + K * 10 + dnum)
+    m = 16
+    x = [[int(v) for v in rng.integers(0, qp[l], m, dtype=np.uint64)] for l in range(L)]
+    for l in range(L):              # edge coefficients: 0, q - 1 and a small value in every limb
+        x[l][0], x[l][1], x[l][2] = 0, qp[l] - 1, 1
+    got = replay(blob, lay, qp, L, K, dnum, x, approx)
+    a = np.array(x, dtype=np.uint64).reshape(1, L, m)
+    want = oracle.modup_batch(a, np.array(qp, dtype=np.uint64), L, K, dnum, approx=approx)[0]
+    assert np.array_equal(np.array(got, dtype=np.uint64), want)
+
+
+def test_no_tensor_core_section_for_wide_digits(lib):
+    """Digits of more than 8 primes keep the integer kernel: no tensor-core section."""
+    lay = layout(24, 8, 2)
+    assert lay["tmax"] == 0
+    nb = ctypes.c_size_t()
+    assert lib.fhe_modup_tables_bytes(24, 8, 2, ctypes.byref(nb)) == 0
+    assert nb.value == lay["bytes"]
