@@ -61,12 +61,13 @@ def keyswitch_alu_floor_s(pairs: int = PAIRS) -> float:
     bench shape if it did nothing else: every 32-bit product the arithmetic
     needs, at the pipe's measured per-SM rates (low 64, high 32, wide 25.2 per
     clock) on 152 SMs at the maximum clock -- the same derivation as
-    ALU_PEAK_BFLY.  Lazy Shoup product (butterfly, Garner step): 3 wide +
-    2 high + 4 low; multiply-accumulate of 25-bit halves: 3 wide; reduction
-    of a 105-bit sum: 5 wide + 2 high + 3 low.  Per (coefficient, digit):
-    alpha (alpha - 1) / 2 Garner products, then per target outside the digit
-    alpha - 1 multiply-accumulates and one reduction; per output residue of
-    the inner product: 2 dnum multiply-accumulates and 2 reductions."""
+    ALU_PEAK_BFLY.  Lazy Shoup product (butterfly, Garner step, the tensor-core
+    ModUp's recombination): 3 wide + 2 high + 4 low; multiply-accumulate of
+    25-bit halves: 3 wide; reduction of a 105-bit sum: 5 wide + 2 high + 3 low.
+    Per (coefficient, digit): alpha (alpha - 1) / 2 Garner products, then per
+    target outside the digit one Shoup product (the extension's dot product
+    itself runs on the tensor cores, KS_TENSOR_FLOP); per output residue of the
+    inner product: 2 dnum multiply-accumulates and 2 reductions."""
     lo, hi, wide = 1 / 64.0, 1 / 32.0, 1 / 25.2          # SM-cycles per 32-bit product
     shoup, mac, red = 3 * wide + 2 * hi + 4 * lo, 3 * wide, 5 * wide + 2 * hi + 3 * lo
     alpha = L // DNUM
@@ -74,9 +75,14 @@ def keyswitch_alu_floor_s(pairs: int = PAIRS) -> float:
     bfly = pairs * DNUM * (L + K) * (N // 2) * LOG_N
     units = pairs * DNUM * N
     ip = pairs * (L + K) * N
-    cycles = (bfly * shoup + units * (alpha * (alpha - 1) // 2 * shoup + targets * ((alpha - 1) * mac + red))
-              + ip * (2 * DNUM * mac + 2 * red))
+    cycles = bfly * shoup + units * (alpha * (alpha - 1) // 2 + targets) * shoup + ip * (2 * DNUM * mac + 2 * red)
     return cycles / (SMS * SM_MAX_MHZ * 1e6)
+
+
+# fp16 tensor-core work of the tensor-core ModUp per call: every tile of 128
+# coefficients of a digit is a 128 x (8 targets) x (8 alpha) product (targets in
+# groups of 16, N padded to a multiple of 16), 2 flops per multiply-add.
+KS_TENSOR_FLOP = 2 * PAIRS * DNUM * N * (8 * (L + K - L // DNUM)) * (8 * (L // DNUM))
 
 
 def peaks():
@@ -571,10 +577,12 @@ def ours(args):
                                "hbm_bytes_min": KS_MIN_BYTES_X4,
                                "traffic": kernel_traffic("keyswitch", KS_T), "traffic_unit": "bytes/call",
                                "traffic_source": TRAFFIC_SOURCE,
+                               "tensor_flop": KS_TENSOR_FLOP,
                                "work": "4 key switches of [24][n] over 24 + 8 primes, dnum = 3: ModUp (28 Garner products "
-                                       "+ 24 x (7 multiply-accumulates + 1 reduction) per coefficient and digit), "
-                                       "384 NTT rows, inner product (6 multiply-accumulates + 2 reductions per output "
-                                       "residue); HBM floor: inputs + keys (read once) + outputs"},
+                                       "+ 24 Shoup products per coefficient and digit on the integer pipes; the "
+                                       "extension's 128 x 192 x 64 fp16 products per tile of 128 coefficients on the "
+                                       "tensor cores), 384 NTT rows, inner product (6 multiply-accumulates + 2 "
+                                       "reductions per output residue); HBM floor: inputs + keys (read once) + outputs"},
         "clocks": clocks,
         "gpu_launches": launches,
         "two_streams": {"value": whole_job_rate(UNITS, ws, two_ms), "unit": UNIT, "ms_per_step": two_ms,

@@ -66,7 +66,8 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
            const ModupTcTarget *__restrict__ tgt, const uint4 *__restrict__ wimg, int tmax,
            const uint64_t *__restrict__ consts) {
     pdl_begin();
-    // APPROX: gconst holds the brackets' constants [dnum][alpha], else Garner's [dnum][alpha][alpha].
+    // APPROX: gconst holds the brackets' constants [dnum][alpha], else Garner's [dnum][alpha][alpha]
+    // (staged as an 8 x 8 block: row 0 for the brackets, entry (a, b) = d_b^-1 mod d_a for Garner).
     extern __shared__ __align__(1024) uint8_t sm[];   // [A operand][B operand][targets]
     __shared__ uint64_t mbar;
     __shared__ uint32_t tslot;
@@ -75,11 +76,21 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
     const int lo = dg[j].lo, cnt = dg[j].count, T = LK - cnt, Tp = (T + 1) & ~1;
     uint8_t *sA = sm, *sB = sm + kTileBytesA;
     ModupTcTarget *sT = reinterpret_cast<ModupTcTarget *>(sB + (size_t)Tp * 8 * kTcRowBytes);
+    // the digit's Garner (or bracket) constants and primes, read in the recursion's dependency chain
+    __shared__ ulonglong2 sG[kTcMaxAlpha * kTcMaxAlpha];
+    __shared__ uint64_t sD[kTcMaxAlpha];
     {
         const uint4 *src = wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16;
         for (int e = t; e < Tp * 8 * kTcRowBytes / 16; e += kTcThreads)
             reinterpret_cast<uint4 *>(sB)[e] = __ldg(src + e);
         for (int e = t; e < T; e += kTcThreads) sT[e] = tgt[(size_t)j * tmax + e];
+        const ulonglong2 *gj = gconst + (long)j * alpha * (APPROX ? 1 : alpha);
+        for (int e = t; e < kTcMaxAlpha * kTcMaxAlpha; e += kTcThreads) {
+            const int a = e / kTcMaxAlpha, b = e - a * kTcMaxAlpha;
+            sG[e] = (a < cnt && b < cnt && (APPROX ? a == 0 : b < a))
+                        ? __ldg(gj + (APPROX ? b : a * alpha + b)) : make_ulonglong2(0, 0);
+        }
+        if (t < kTcMaxAlpha) sD[t] = t < cnt ? __ldg(consts + (long)(lo + t) * K_COUNT + K_Q) : 0;
     }
     if (warp == 0) tmem_alloc(&tslot, 128);
     if (t == 0) mbar_init(&mbar, 1);
@@ -90,7 +101,6 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
     const uint32_t tmem = tslot, lanes = (uint32_t)(32 * warp) << 16;
     const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
     uint8_t *arow = sA + (t >> 3) * kCoreRows + (t & 7) * 16;   // this thread's operand row
-    const ulonglong2 *gj = gconst + (long)j * alpha * (APPROX ? 1 : alpha);
     const long tiles_per_item = (1L << log_n) >> 7;
     const long tiles = (long)batch * tiles_per_item;
     uint32_t phase = 0;
@@ -117,8 +127,8 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
             for (int a = 0; a < kTcMaxAlpha; a++) {
                 v[a] = 0;
                 if (a < cnt) {
-                    const uint64_t d = __ldg(consts + (long)(lo + a) * K_COUNT + K_Q);
-                    const ulonglong2 c = __ldg(gj + a);
+                    const uint64_t d = sD[a];
+                    const ulonglong2 c = sG[a];   // bracket constant a (row 0 of the staged block)
                     v[a] = reduce4(shoup_lazy(x[a], c.x, c.y, d), d);
                 }
             }
@@ -128,11 +138,11 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
             for (int a = 1; a < kTcMaxAlpha; a++) {
                 v[a] = 0;
                 if (a < cnt) {
-                    const uint64_t d = __ldg(consts + (long)(lo + a) * K_COUNT + K_Q);
+                    const uint64_t d = sD[a];
                     uint64_t u = x[a];
 #pragma unroll
                     for (int b = 0; b < a; b++) {
-                        const ulonglong2 c = __ldg(gj + a * alpha + b);
+                        const ulonglong2 c = sG[a * kTcMaxAlpha + b];
                         u = shoup_lazy(u + 4 * d - v[b], c.x, c.y, d);   // v_b < 2^50 < 4 d
                     }
                     v[a] = reduce4(u, d);
@@ -181,12 +191,14 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
                 for (int h = 0; h < 4; h++) {
                     if (tt + h < gcnt) {
                         const uint32_t *u = r + 8 * h;
-                        const uint64_t l4 = (uint64_t)(u[0] - kF32Offset) + ((uint64_t)(u[1] - kF32Offset) << 7) +
-                                            ((uint64_t)(u[2] - kF32Offset) << 14) +
-                                            ((uint64_t)(u[3] - kF32Offset) << 21);
-                        const uint64_t h4 = (uint64_t)(u[4] - kF32Offset) + ((uint64_t)(u[5] - kF32Offset) << 7) +
-                                            ((uint64_t)(u[6] - kF32Offset) << 14) +
-                                            ((uint64_t)(u[7] - kF32Offset) << 21);
+                        // u_s = 2^23 bit pattern + d_s, d_s < 2^21: pairs d_s + d_{s+1} 2^7 < 2^29 taken
+                        // mod 2^32 with the two offsets folded into one constant
+                        const uint32_t p01 = u[0] + (u[1] << 7) - kF32Offset * 129u;
+                        const uint32_t p23 = u[2] + (u[3] << 7) - kF32Offset * 129u;
+                        const uint32_t p45 = u[4] + (u[5] << 7) - kF32Offset * 129u;
+                        const uint32_t p67 = u[6] + (u[7] << 7) - kF32Offset * 129u;
+                        const uint64_t l4 = (uint64_t)p23 * (1u << 14) + p01;   // d_0 + .. + d_3 2^21
+                        const uint64_t h4 = (uint64_t)p67 * (1u << 14) + p45;   // d_4 + .. + d_7 2^21
                         const ModupTcTarget &tg = sT[g0 + tt + h];
                         __stcs(dst + ((long)tg.limb << log_n), l4 + shoup_lazy(h4, tg.w28, tg.w28p, tg.p));
                     }
