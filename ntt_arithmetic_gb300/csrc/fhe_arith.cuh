@@ -227,6 +227,17 @@ FHE_HD void ct_bfly_one(uint64_t &X, uint64_t &Y, uint64_t b) {
     Y = x - y + b;
 }
 
+// x mod p up to 2p for any 64-bit x, with mu = floor(2^64 / p) and p > 2^48
+// (so mu < 2^16): Q = floor(x mu / 2^64) is computed exactly from the 32-bit
+// halves (x_hi mu + floor(x_lo mu / 2^32)) >> 32, and x/p - 2 < Q <= x/p,
+// so x - Q p lies in [0, 2p).  Two wide, one high and one low product.
+FHE_HD uint64_t reduce64_small_mu(uint64_t x, uint64_t p, uint64_t mu) {
+    const uint32_t m = (uint32_t)mu;
+    const uint64_t t = (uint64_t)hi32(x) * m + umulhi32(lo32(x), m);
+    const uint32_t Q = (uint32_t)(t >> 32);
+    return x - ((uint64_t)Q * lo32(p) + ((uint64_t)(Q * hi32(p)) << 32));
+}
+
 // [0, 4q) -> [0, q)
 FHE_HD uint64_t reduce4(uint64_t x, uint64_t q) { return csub(csub(x, 2 * q), q); }
 

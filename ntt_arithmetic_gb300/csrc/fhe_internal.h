@@ -22,11 +22,19 @@ struct ModupDigit {
     int32_t lo;      // first limb of the digit
     int32_t count;   // limbs in the digit (<= alpha)
 };
+// Per prime d_a of a digit, the constants of the tensor-core extension's
+// exact correction (modup_tc.cu): phi = floor(2^128 / d_a) as (hi, lo) words
+// for the fixed-point sum of y_a / d_a, and for the redundant-modulus
+// fallback (D / d_a) mod 2^64 and d_0 ... d_{a-1} mod 2^64.  Entry
+// kTcMaxAlpha of each digit holds D^-1 mod 2^64 in `dhat64`.
+struct ModupTcFrac {
+    uint64_t phi_hi, phi_lo, dhat64, w64;
+};
 // One target prime of a digit's tensor-core extension (modup_tc.cu).
 struct ModupTcTarget {
     uint64_t p;      // the target prime
-    uint64_t w28;    // 2^28 mod p
-    uint64_t w28p;   // floor(w28 2^64 / p), its Shoup companion
+    uint64_t mu;     // floor(2^64 / p) (< 2^16)
+    uint64_t zero;   // padding (keeps the record 32 bytes)
     uint64_t limb;   // index of p in the extended basis
 };
 // The tensor-core extension takes digits of up to kTcMaxAlpha primes: one
@@ -36,6 +44,7 @@ struct ModupTcTarget {
 constexpr int kTcMaxAlpha = 8;
 constexpr int kTcTargetsPerGroup = 16;
 constexpr int kTcRowBytes = 8 * kTcMaxAlpha * 2;   // one operand row: 64 fp16
+constexpr int kTcCorrCol = 15;                     // operand column of the correction count
 
 struct ModupLayout {
     int alpha;
@@ -47,8 +56,8 @@ struct ModupLayout {
     // tensor-core extension (alpha <= kTcMaxAlpha; tc_tmax = 0 otherwise):
     int tc_tmax;         // target slots per digit (L+K rounded up to even)
     size_t off_tc_tgt;   // [dnum][tc_tmax] ModupTcTarget
-    size_t off_tc_bx;    // [dnum][8 tc_tmax rows][64] fp16 weight limbs, operand layout (exact)
-    size_t off_tc_ba;    // the same for the approximate conversion
+    size_t off_tc_frac;  // [dnum][kTcMaxAlpha + 1] ModupTcFrac
+    size_t off_tc_b;     // [dnum][8 tc_tmax rows][64] fp16 weight limbs, operand layout
     size_t bytes;
 };
 ModupLayout modup_layout(int L, int K, int dnum);

@@ -19,9 +19,12 @@
 //    integers below 2^24 are exact in f32, and the accumulator's bit pattern
 //    minus 0x4B000000 is the integer;
 //  * the eight accumulators u_s of a target recombine as
-//    sum_s u_s 2^(7s) = (u_0 + .. + u_3 2^21) + 2^28 (u_4 + .. + u_7 2^21),
-//    reduced with one Shoup product by 2^28 mod p to a value below 5 p (the
-//    forward NTT that follows takes inputs of that size).
+//    S = sum_s u_s 2^(7s) = (u_0 + .. + u_3 2^21) + 2^28 (u_4 + .. + u_7 2^21).
+//    S < 2^64: u_s <= 8 (6 * 255 + 3) 127 < 2^20.6 for s < 7 (a digit's byte 6
+//    is below 4), and limb 7 of a constant below 2^50 is 0 or 1, so
+//    u_7 < 2^13.6 and S < 2^42 (2^20.6 * 1.008 + 2^13.6 2^7) < 2^63.6.  One
+//    Barrett step with mu = floor(2^64 / p) < 2^16 leaves S mod p below 2 p
+//    (the forward NTT that follows takes inputs of that size).
 //
 // The integer pipes keep Garner's recursion (c (c - 1) / 2 Shoup products per
 // coefficient) and one Shoup product per output; the c multiply-accumulates
@@ -62,12 +65,12 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int T) {
 template <bool APPROX>
 __global__ void __launch_bounds__(kTcThreads, 4)
 k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int batch,
-           int alpha, const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ gconst,
+           int alpha, const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ qinv,
+           const ulonglong2 *__restrict__ garner, const ModupTcFrac *__restrict__ frac,
            const ModupTcTarget *__restrict__ tgt, const uint4 *__restrict__ wimg, int tmax,
            const uint64_t *__restrict__ consts) {
     pdl_begin();
-    // APPROX: gconst holds the brackets' constants [dnum][alpha], else Garner's [dnum][alpha][alpha]
-    // (staged as an 8 x 8 block: row 0 for the brackets, entry (a, b) = d_b^-1 mod d_a for Garner).
+    // qinv: the brackets' constants [dnum][alpha]; garner: [dnum][alpha][alpha] (the exact fallback)
     extern __shared__ __align__(1024) uint8_t sm[];   // [A operand][B operand][targets]
     __shared__ uint64_t mbar;
     __shared__ uint32_t tslot;
@@ -76,21 +79,25 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
     const int lo = dg[j].lo, cnt = dg[j].count, T = LK - cnt, Tp = (T + 1) & ~1;
     uint8_t *sA = sm, *sB = sm + kTileBytesA;
     ModupTcTarget *sT = reinterpret_cast<ModupTcTarget *>(sB + (size_t)Tp * 8 * kTcRowBytes);
-    // the digit's Garner (or bracket) constants and primes, read in the recursion's dependency chain
-    __shared__ ulonglong2 sG[kTcMaxAlpha * kTcMaxAlpha];
+    // the digit's constants, read inside the per-coefficient dependency chains
+    __shared__ ulonglong2 sQ[kTcMaxAlpha];                   // bracket constants (D/d_a)^-1 mod d_a
+    __shared__ ulonglong2 sG[kTcMaxAlpha * kTcMaxAlpha];     // Garner: (a, b) = d_b^-1 mod d_a, b < a
+    __shared__ ModupTcFrac sF[kTcMaxAlpha + 1];              // reciprocals, redundant-modulus constants
     __shared__ uint64_t sD[kTcMaxAlpha];
     {
         const uint4 *src = wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16;
         for (int e = t; e < Tp * 8 * kTcRowBytes / 16; e += kTcThreads)
             reinterpret_cast<uint4 *>(sB)[e] = __ldg(src + e);
         for (int e = t; e < T; e += kTcThreads) sT[e] = tgt[(size_t)j * tmax + e];
-        const ulonglong2 *gj = gconst + (long)j * alpha * (APPROX ? 1 : alpha);
         for (int e = t; e < kTcMaxAlpha * kTcMaxAlpha; e += kTcThreads) {
             const int a = e / kTcMaxAlpha, b = e - a * kTcMaxAlpha;
-            sG[e] = (a < cnt && b < cnt && (APPROX ? a == 0 : b < a))
-                        ? __ldg(gj + (APPROX ? b : a * alpha + b)) : make_ulonglong2(0, 0);
+            sG[e] = (a < cnt && b < a) ? __ldg(garner + ((long)j * alpha + a) * alpha + b) : make_ulonglong2(0, 0);
         }
-        if (t < kTcMaxAlpha) sD[t] = t < cnt ? __ldg(consts + (long)(lo + t) * K_COUNT + K_Q) : 0;
+        if (t < kTcMaxAlpha) {
+            sQ[t] = t < cnt ? __ldg(qinv + (long)j * alpha + t) : make_ulonglong2(0, 0);
+            sD[t] = t < cnt ? __ldg(consts + (long)(lo + t) * K_COUNT + K_Q) : 0;
+        }
+        if (t <= kTcMaxAlpha) sF[t] = frac[(long)j * (kTcMaxAlpha + 1) + t];
     }
     if (warp == 0) tmem_alloc(&tslot, 128);
     if (t == 0) mbar_init(&mbar, 1);
@@ -122,38 +129,67 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
 #pragma unroll
         for (int a = 0; a < kTcMaxAlpha; a++) x[a] = xn[a];
         if (tile + gridDim.x < tiles) load_tile(tile + gridDim.x);
-        if constexpr (APPROX) {
+        // CRT brackets v_a = [x_a (D/d_a)^-1]_{d_a}: sum_a v_a (D/d_a) = X + e D with
+        // e = floor(sum_a v_a / d_a) < cnt
+#pragma unroll
+        for (int a = 0; a < kTcMaxAlpha; a++) {
+            v[a] = 0;
+            if (a < cnt) {
+                const uint64_t d = sD[a];
+                const ulonglong2 c = sQ[a];
+                v[a] = reduce4(shoup_lazy(x[a], c.x, c.y, d), d);
+            }
+        }
+        uint32_t ec = 0;   // the correction count e (0 for the approximate conversion)
+        if constexpr (!APPROX) {
+            // e from the 64.64 fixed-point sum of v_a / d_a (each term below the true value by < 2)
+            uint64_t F = 0;
 #pragma unroll
             for (int a = 0; a < kTcMaxAlpha; a++) {
-                v[a] = 0;
                 if (a < cnt) {
-                    const uint64_t d = sD[a];
-                    const ulonglong2 c = sG[a];   // bracket constant a (row 0 of the staged block)
-                    v[a] = reduce4(shoup_lazy(x[a], c.x, c.y, d), d);
+                    const uint64_t term = v[a] * sF[a].phi_hi + umulhi64(v[a], sF[a].phi_lo);
+                    F += term;
+                    ec += F < term;
                 }
             }
-        } else {
-            v[0] = x[0];
+            // X / D within 2 cnt 2^-64 of 1 (or of 0, wrapped): the sum may round either way
+            const bool near = F > ~0ull - 2 * (uint64_t)cnt;
+            if (__any_sync(0xffffffffu, near) && near) {
+                // exact e by a redundant modulus: Garner gives X's mixed-radix digits w_a, and
+                // e = (sum v_a (D/d_a) - X) D^-1 mod 2^64
+                uint64_t w[kTcMaxAlpha];
+                w[0] = x[0];
 #pragma unroll
-            for (int a = 1; a < kTcMaxAlpha; a++) {
-                v[a] = 0;
-                if (a < cnt) {
-                    const uint64_t d = sD[a];
-                    uint64_t u = x[a];
+                for (int a = 1; a < kTcMaxAlpha; a++) {
+                    w[a] = 0;
+                    if (a < cnt) {
+                        const uint64_t d = sD[a];
+                        uint64_t u = x[a];
 #pragma unroll
-                    for (int b = 0; b < a; b++) {
-                        const ulonglong2 c = sG[a * kTcMaxAlpha + b];
-                        u = shoup_lazy(u + 4 * d - v[b], c.x, c.y, d);   // v_b < 2^50 < 4 d
+                        for (int b = 0; b < a; b++) {
+                            const ulonglong2 c = sG[a * kTcMaxAlpha + b];
+                            u = shoup_lazy(u + 4 * d - w[b], c.x, c.y, d);   // w_b < 2^50 < 4 d
+                        }
+                        w[a] = reduce4(u, d);
                     }
-                    v[a] = reduce4(u, d);
                 }
+                uint64_t Y = 0, X = 0;
+#pragma unroll
+                for (int a = 0; a < kTcMaxAlpha; a++) {
+                    if (a < cnt) {
+                        Y += v[a] * sF[a].dhat64;
+                        X += w[a] * sF[a].w64;
+                    }
+                }
+                ec = (uint32_t)((Y - X) * sF[kTcMaxAlpha].dhat64);
             }
         }
         uint64_t *dst = ext + (((long)bi * dnum + j) * LK << log_n) + i;
 #pragma unroll
         for (int a = 0; a < kTcMaxAlpha; a++)
             if (a < cnt) __stcs(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
-        // A operand row: fp16 1024 + byte, eight per digit (byte 7 of v_a < 2^50 is 0)
+        // A operand row: fp16 1024 + byte, eight per digit (byte 7 of v_a < 2^50 is 0);
+        // column 15 (byte 7 of v_1) carries 1024 + e
 #pragma unroll
         for (int a = 0; a < kTcMaxAlpha; a++) {
             const uint32_t vl = (uint32_t)v[a], vh = (uint32_t)(v[a] >> 32);
@@ -162,6 +198,7 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
             row.y = __byte_perm(vl, 0x64646464u, 0x4342);
             row.z = __byte_perm(vh, 0x64646464u, 0x4140);
             row.w = __byte_perm(vh, 0x64646464u, 0x4342);
+            if (8 * a + 7 == kTcCorrCol) row.w |= ec << 16;
             *reinterpret_cast<uint4 *>(arow + a * kCoreK) = row;
         }
         fence_async_smem();
@@ -200,7 +237,7 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
                         const uint64_t l4 = (uint64_t)p23 * (1u << 14) + p01;   // d_0 + .. + d_3 2^21
                         const uint64_t h4 = (uint64_t)p67 * (1u << 14) + p45;   // d_4 + .. + d_7 2^21
                         const ModupTcTarget &tg = sT[g0 + tt + h];
-                        __stcs(dst + ((long)tg.limb << log_n), l4 + shoup_lazy(h4, tg.w28, tg.w28p, tg.p));
+                        __stcs(dst + ((long)tg.limb << log_n), reduce64_small_mu(l4 + (h4 << 28), tg.p, tg.mu));
                     }
                 }
             }
@@ -241,9 +278,9 @@ int launch_modup_tc(uint64_t *ext, const uint64_t *in, long in_stride, int log_n
     const char *base = (const char *)modup;
     kern<<<dim3((unsigned)gx, (unsigned)dnum), kTcThreads, smem, st>>>(
         ext, in, in_stride, log_n, LK, batch, lay.alpha, (const ModupDigit *)(base + lay.off_digits),
-        (const ulonglong2 *)(base + (approx ? lay.off_qinv : lay.off_garner)),
-        (const ModupTcTarget *)(base + lay.off_tc_tgt), (const uint4 *)(base + (approx ? lay.off_tc_ba : lay.off_tc_bx)),
-        lay.tc_tmax, t->consts);
+        (const ulonglong2 *)(base + lay.off_qinv), (const ulonglong2 *)(base + lay.off_garner),
+        (const ModupTcFrac *)(base + lay.off_tc_frac), (const ModupTcTarget *)(base + lay.off_tc_tgt),
+        (const uint4 *)(base + lay.off_tc_b), lay.tc_tmax, t->consts);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

@@ -113,9 +113,9 @@ ModupLayout modup_layout(int L, int K, int dnum) {
     const size_t end = align256(s.off_qhat + (size_t)dnum * LK * s.alpha * 16);
     s.tc_tmax = s.alpha <= kTcMaxAlpha ? (LK + 1) & ~1 : 0;
     s.off_tc_tgt = end;
-    s.off_tc_bx = align256(s.off_tc_tgt + (size_t)dnum * s.tc_tmax * sizeof(ModupTcTarget));
-    s.off_tc_ba = align256(s.off_tc_bx + (size_t)dnum * s.tc_tmax * 8 * kTcRowBytes);
-    s.bytes = align256(s.off_tc_ba + (size_t)dnum * s.tc_tmax * 8 * kTcRowBytes);
+    s.off_tc_frac = align256(s.off_tc_tgt + (size_t)dnum * s.tc_tmax * sizeof(ModupTcTarget));
+    s.off_tc_b = align256(s.off_tc_frac + (s.tc_tmax ? (size_t)dnum * (kTcMaxAlpha + 1) * sizeof(ModupTcFrac) : 0));
+    s.bytes = align256(s.off_tc_b + (size_t)dnum * s.tc_tmax * 8 * kTcRowBytes);
     return s;
 }
 
@@ -292,19 +292,22 @@ static uint16_t fp16_of_int(int v) {
 }
 
 // The tensor-core extension's weight operand for one digit of cnt primes and
-// T targets.  With the digit's mixed-radix (or CRT) digits v_a split into
-// bytes b_{a,e} (e = 0..6; v_a < 2^50), the extension of target p is
-//   sum_a v_a W_{a,p} = sum_{a,e} b_{a,e} (W_{a,p} 2^(8e) mod p)   (mod p),
+// T targets.  With the digit's CRT brackets y_a split into bytes b_{a,e}
+// (e = 0..6; y_a < 2^50) and the correction count e_c, the extension of
+// target p is
+//   sum_a y_a W_{a,p} - e_c D = sum_{a,e} b_{a,e} (W_{a,p} 2^(8e) mod p)
+//                              + e_c ((-D) mod p)                  (mod p),
 // and each constant c = W_{a,p} 2^(8e) mod p < 2^56 is split into eight
 // 7-bit limbs c_s.  Operand row 8 t + s (target t, limb s), column 8 a + e,
 // holds c_s; the kernel's other operand holds 1024 + b_{a,e} (the fp16 bit
-// pattern 0x6400 | b), so accumulator column 8 t + s receives
-//   1024 * (row sum) + sum_{a,e} b_{a,e} c_s.
-// Column 8 a + 7 (byte 7 of v_a, always 0) holds integers <= 2048 that make
+// pattern 0x6400 | b) and 1024 + e_c in column 15, so accumulator column
+// 8 t + s receives 1024 * (row sum) + sum_{a,e} b_{a,e} c_s + e_c m_s, with
+// m_s the 7-bit limbs of (-D) mod p in column 15 (kTcCorrCol).  The other
+// columns 8 a + 7 (byte 7 of y_a, always 0) hold integers <= 2048 that make
 // every row sum 8192: each accumulator is then 2^23 + (a value < 2^21) and
 // its f32 bit pattern minus 0x4B000000 is that value.  Rows of the odd
 // target that pads T to even carry only the 8192.
-static void tc_weight_image(uint8_t *img, int cnt, int T, const uint64_t *W, const uint64_t *P) {
+static void tc_weight_image(uint8_t *img, int cnt, int T, const uint64_t *W, const uint64_t *P, const uint64_t *corr) {
     const int Tp = (T + 1) & ~1;
     for (int t = 0; t < Tp; t++) {
         for (int s = 0; s < 8; s++) {
@@ -317,8 +320,13 @@ static void tc_weight_image(uint8_t *img, int cnt, int T, const uint64_t *W, con
                     sum += val[8 * a + e];
                 }
             }
-            int rem = 8192 - sum;   // sum <= 7 * 8 * 127 = 7112
+            if (t < T) {
+                val[kTcCorrCol] = (int)((corr[t] >> (7 * s)) & 127);
+                sum += val[kTcCorrCol];
+            }
+            int rem = 8192 - sum;   // sum <= 7 * 8 * 127 + 127 = 7239
             for (int a = 0; a < kTcMaxAlpha; a++) {
+                if (8 * a + 7 == kTcCorrCol) continue;
                 const int v = rem < 2048 ? rem : 2048;
                 val[8 * a + 7] = v;
                 rem -= v;
@@ -394,29 +402,46 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
             // the digit's targets (every prime outside it) and both weight operands
             const int cnt = hi - lo, T = LK - cnt;
             ModupTcTarget *tg = (ModupTcTarget *)(base + lay.off_tc_tgt) + (size_t)j * lay.tc_tmax;
-            std::vector<uint64_t> P(T), Wx((size_t)cnt * T), Wa((size_t)cnt * T);
+            std::vector<uint64_t> P(T), Wa((size_t)cnt * T), corr(T);
             for (int l = 0, t = 0; l < LK; l++) {
                 if (l >= lo && l < hi) continue;
                 const uint64_t p = qp[l];
                 tg[t].p = p;
-                tg[t].w28 = (1ull << 28) % p;
-                tg[t].w28p = shoup(tg[t].w28, p);
+                tg[t].mu = (uint64_t)(((u128)1 << 64) / p);
                 tg[t].limb = (uint64_t)l;
                 P[t] = p;
-                uint64_t prod = 1 % p;
+                uint64_t Dp = 1 % p;
                 for (int a = 0; a < cnt; a++) {
-                    Wx[(size_t)a * T + t] = prod;   // d_0 ... d_{a-1} mod p
-                    prod = mul_mod(prod, qp[lo + a] % p, p);
+                    Dp = mul_mod(Dp, qp[lo + a] % p, p);
                     uint64_t hp = 1 % p;
                     for (int b = 0; b < cnt; b++)
                         if (b != a) hp = mul_mod(hp, qp[lo + b] % p, p);
                     Wa[(size_t)a * T + t] = hp;     // (D_j / d_a) mod p
                 }
+                corr[t] = (p - Dp) % p;             // (-D_j) mod p
                 t++;
             }
             const size_t img = (size_t)lay.tc_tmax * 8 * kTcRowBytes;
-            tc_weight_image((uint8_t *)(base + lay.off_tc_bx) + j * img, cnt, T, Wx.data(), P.data());
-            tc_weight_image((uint8_t *)(base + lay.off_tc_ba) + j * img, cnt, T, Wa.data(), P.data());
+            tc_weight_image((uint8_t *)(base + lay.off_tc_b) + j * img, cnt, T, Wa.data(), P.data(), corr.data());
+            // fixed-point reciprocals and the redundant-modulus constants
+            ModupTcFrac *fr = (ModupTcFrac *)(base + lay.off_tc_frac) + (size_t)j * (kTcMaxAlpha + 1);
+            uint64_t D64 = 1, W64 = 1;
+            for (int a = 0; a < cnt; a++) D64 *= qp[lo + a];
+            for (int a = 0; a < cnt; a++) {
+                const uint64_t da = qp[lo + a];
+                const u128 phi = ~(u128)0 / da;     // floor((2^128 - 1) / d_a) = floor(2^128 / d_a): d_a is odd
+                fr[a].phi_hi = (uint64_t)(phi >> 64);
+                fr[a].phi_lo = (uint64_t)phi;
+                uint64_t h = 1;
+                for (int b = 0; b < cnt; b++)
+                    if (b != a) h *= qp[lo + b];
+                fr[a].dhat64 = h;                   // (D_j / d_a) mod 2^64
+                fr[a].w64 = W64;                    // d_0 ... d_{a-1} mod 2^64
+                W64 *= da;
+            }
+            uint64_t inv = D64;                     // D_j^-1 mod 2^64 (D_j odd), Newton on the 2-adic inverse
+            for (int k = 0; k < 6; k++) inv *= 2 - D64 * inv;
+            fr[kTcMaxAlpha].dhat64 = inv;
         }
     }
     return FHE_OK;
@@ -583,6 +608,10 @@ int selftest_arith(uint64_t seed, int iters) {
             // the lazy form: congruent, below (4 + terms) q
             const uint64_t lz = mac25_reduce_lazy(acc, extra, q, mu12);
             if (lz % q != (uint64_t)((ref_sum + extra) % q) || lz >= (uint64_t)(4 + terms) * q) return 15;
+            // the 64-bit reduction with mu = floor(2^64 / q): congruent, below 2q, for any word
+            const uint64_t w = it % 7 == 0 ? ~0ull - (uint64_t)(it % 3) : next();
+            const uint64_t r64 = reduce64_small_mu(w, q, (uint64_t)(((u128)1 << 64) / q));
+            if (r64 >= 2 * q || r64 % q != w % q) return 16;
         }
     }
     return 0;

@@ -1,20 +1,24 @@
 """Host-side check of the tensor-core ModUp's encoding (no GPU).
 
 The tensor-core extension (csrc/modup_tc.cu) computes each target residue of
-a digit's basis extension as an exact fp16 x fp16 -> f32 contraction: the A
-operand row of a coefficient holds 1024 + b for every byte b of its
-mixed-radix digits v_a (exact) or CRT brackets (approximate), the B operand --
-written by the library's host builder into the ModUp table blob -- holds the
-7-bit limbs of the weights W_{a,p} 2^(8e) mod p and offset columns, every
-accumulator must come out as 2^23 + (an integer below 2^21), and the eight
-accumulators of a target recombine as sum_s u_s 2^(7s).
+a digit's basis extension as an exact fp16 x fp16 -> f32 contraction.  Per
+coefficient it forms the CRT brackets y_a = [x_a (D/d_a)^-1]_{d_a}, for the
+exact extension also the count e = floor(sum_a y_a / d_a) (from a 64.64
+fixed-point sum, or -- when that sum is within 2 cnt units of an integer --
+from Garner's digits and a redundant modulus 2^64); the A operand row holds
+1024 + b for every byte b of the y_a and 1024 + e in column 15, the B operand
+-- written by the library's host builder into the ModUp table blob -- the
+7-bit limbs of (D/d_a) 2^(8e) mod p, the limbs of (-D) mod p in column 15 and
+offset columns, so that every accumulator comes out as 2^23 + (an integer
+below 2^21); the eight accumulators of a target recombine as
+sum_s u_s 2^(7s) < 2^64, reduced with one Barrett step by
+mu = floor(2^64 / p).
 
-Here the contraction is replayed in exact integer arithmetic from the blob
-the library builds (fhe_modup_tables_build_host), with the digits v_a taken
-from Python integers (the mixed-radix digits of the CRT value), and the
-result is compared with the oracle's ModUp (modup_batch).  A wrong weight, a
-wrong limb order, a wrong offset column, an operand row in the wrong place of
-the layout or a wrong target list fails here without a GPU.
+Here all of it is replayed in exact integer arithmetic from the blob the
+library builds (fhe_modup_tables_build_host) and compared with the oracle's
+ModUp (modup_batch).  A wrong weight, limb order, offset or correction
+column, a wrong reciprocal or redundant-modulus constant, a wrong target list
+or a near-integer test that misses a case fails here without a GPU.
 """
 import ctypes
 import math
@@ -51,10 +55,10 @@ def layout(L: int, K: int, dnum: int) -> dict:
     end = a256(off_qhat + dnum * LK * alpha * 16)
     tmax = (LK + 1) & ~1 if alpha <= MAXA else 0
     off_tgt = end
-    off_bx = a256(off_tgt + dnum * tmax * 32)
-    off_ba = a256(off_bx + dnum * tmax * 8 * ROWB)
-    return {"alpha": alpha, "tmax": tmax, "tgt": off_tgt, "bx": off_bx, "ba": off_ba,
-            "bytes": a256(off_ba + dnum * tmax * 8 * ROWB)}
+    off_frac = a256(off_tgt + dnum * tmax * 32)
+    off_b = a256(off_frac + (dnum * (MAXA + 1) * 32 if tmax else 0))
+    return {"alpha": alpha, "tmax": tmax, "tgt": off_tgt, "frac": off_frac, "b": off_b,
+            "bytes": a256(off_b + dnum * tmax * 8 * ROWB)}
 
 
 def fp16_int(bits: np.ndarray) -> np.ndarray:
@@ -82,37 +86,65 @@ def build_blob(lib, L, K, dnum, qp):
     return blob
 
 
+def correction_count(xs, d, frac, approx):
+    """The kernel's e: 0 for the approximate conversion; else the fixed-point
+    estimate, or the redundant-modulus value when the estimate is near an integer."""
+    M64 = (1 << 64) - 1
+    Dj = math.prod(d)
+    y = [xs[a] * pow(Dj // d[a], -1, d[a]) % d[a] for a in range(len(d))]
+    if approx:
+        return y, 0, False
+    F, e = 0, 0
+    for a in range(len(d)):
+        phi = (int(frac[a, 0]) << 64) | int(frac[a, 1])
+        assert phi == (1 << 128) // d[a]
+        term = y[a] * int(frac[a, 0]) + ((y[a] * int(frac[a, 1])) >> 64)
+        F += term
+    e, F = F >> 64, F & M64
+    near = F > M64 - 2 * len(d)
+    if near:   # Garner's mixed-radix digits of X, then e = (sum y_a (D/d_a) - X) D^-1 mod 2^64
+        X = sum(xs[a] * (Dj // d[a]) * pow(Dj // d[a], -1, d[a]) for a in range(len(d))) % Dj
+        w = []
+        for a in range(len(d)):
+            w.append(X % d[a])
+            X //= d[a]
+        Y = sum(y[a] * int(frac[a, 2]) for a in range(len(d))) & M64
+        Xr = sum(w[a] * int(frac[a, 3]) for a in range(len(d))) & M64
+        e = ((Y - Xr) * int(frac[MAXA, 2])) & M64
+    true_e = sum(y[a] * (Dj // d[a]) for a in range(len(d))) // Dj
+    assert e == true_e, "the kernel's correction count is the exact one"
+    return y, e, near
+
+
 def replay(blob, lay, qp, L, K, dnum, x, approx):
     """The tensor-core kernel's arithmetic on coefficients x [L][m] (ints) -> [dnum][L+K][m]."""
     LK, alpha, tmax = L + K, lay["alpha"], lay["tmax"]
     m = len(x[0])
     out = np.zeros((dnum, LK, m), dtype=object)
     tg = blob[lay["tgt"]:lay["tgt"] + dnum * tmax * 32].view(np.uint64).reshape(dnum, tmax, 4)
+    fr = blob[lay["frac"]:lay["frac"] + dnum * (MAXA + 1) * 32].view(np.uint64).reshape(dnum, MAXA + 1, 4)
+    nears = 0
     for j in range(dnum):
         lo = j * alpha
         cnt = min(alpha, L - lo)
         d = [int(q) for q in qp[lo:lo + cnt]]
+        Dj = math.prod(d)
+        assert (int(fr[j, MAXA, 2]) * (Dj & ((1 << 64) - 1))) & ((1 << 64) - 1) == 1
         T = LK - cnt
         Tp = (T + 1) & ~1
-        Bw = weight_operand(blob, lay["ba" if approx else "bx"] + j * tmax * 8 * ROWB, 8 * Tp)
+        Bw = weight_operand(blob, lay["b"] + j * tmax * 8 * ROWB, 8 * Tp)
         assert (Bw.sum(axis=1) == 8192).all(), "every weight row sums to 8192 (the 2^23 offset)"
         assert (Bw <= 2048).all() and (Bw >= 0).all()
-        Dj = math.prod(d)
         A = np.full((m, 64), 1024, dtype=np.int64)
         for c in range(m):
             xs = [int(x[lo + a][c]) for a in range(cnt)]
-            if approx:
-                v = [xs[a] * pow(Dj // d[a], -1, d[a]) % d[a] for a in range(cnt)]
-            else:   # mixed-radix digits of the CRT value: what Garner's recursion returns
-                X = sum(xs[a] * (Dj // d[a]) * pow(Dj // d[a], -1, d[a]) for a in range(cnt)) % Dj
-                v = []
-                for a in range(cnt):
-                    v.append(X % d[a])
-                    X //= d[a]
+            y, e, near = correction_count(xs, d, fr[j], approx)
+            nears += near
             for a in range(cnt):
-                assert v[a] < 1 << 50
-                for e in range(8):
-                    A[c, 8 * a + e] = 1024 + ((v[a] >> (8 * e)) & 255)
+                assert y[a] < 1 << 50
+                for k in range(7):
+                    A[c, 8 * a + k] = 1024 + ((y[a] >> (8 * k)) & 255)
+            A[c, 15] = 1024 + e
             for a in range(cnt):
                 out[j, lo + a, c] = xs[a]
         Dacc = A @ Bw.T                         # exact: every value < 2^24
@@ -121,11 +153,15 @@ def replay(blob, lay, qp, L, K, dnum, x, approx):
         for t in range(T):
             p, limb = int(tg[j, t, 0]), int(tg[j, t, 3])
             assert p == int(qp[limb]) and not (lo <= limb < lo + cnt)
-            assert int(tg[j, t, 1]) == (1 << 28) % p
+            mu = int(tg[j, t, 1])
+            assert mu == (1 << 64) // p
             for c in range(m):
                 S = sum(int(U[c, 8 * t + s]) << (7 * s) for s in range(8))
-                out[j, limb, c] = S % p
-    return out
+                assert S < 1 << 64, "the recombined sum fits one word"
+                r = S - ((S * mu) >> 64) * p      # the kernel's Barrett step
+                assert 0 <= r < 2 * p
+                out[j, limb, c] = r % p
+    return out, nears
 
 
 @pytest.mark.parametrize("L,K,dnum,approx", [(24, 8, 3, False), (24, 8, 3, True), (7, 3, 3, False),
@@ -141,7 +177,9 @@ def test_tensor_core_modup_encoding(lib, L, K, dnum, approx):
     x = [[int(v) for v in rng.integers(0, qp[l], m, dtype=np.uint64)] for l in range(L)]
     for l in range(L):              # edge coefficients: 0, q - 1 and a small value in every limb
         x[l][0], x[l][1], x[l][2] = 0, qp[l] - 1, 1
-    got = replay(blob, lay, qp, L, K, dnum, x, approx)
+    got, nears = replay(blob, lay, qp, L, K, dnum, x, approx)
+    if not approx:
+        assert nears > 0, "the edge coefficients (1 and q - 1 in every limb) take the exact fallback"
     a = np.array(x, dtype=np.uint64).reshape(1, L, m)
     want = oracle.modup_batch(a, np.array(qp, dtype=np.uint64), L, K, dnum, approx=approx)[0]
     assert np.array_equal(np.array(got, dtype=np.uint64), want)
