@@ -1,38 +1,50 @@
 // modup_tc.cu -- ModUp's basis extension as a tensor-core contraction.
 //
-// For digit j (primes d_0..d_{c-1}) every coefficient's extension to a
-// target prime p is the dot product sum_a v_a W_{a,p} of its c mixed-radix
-// digits v_a (Garner, exact) or CRT brackets v_a = [x_a (D_j/d_a)^-1]_{d_a}
-// (approximate) with per-digit weights W -- the "mixed-radix decomposition
-// and basis extension" of FHElium's CUDA layer ("Eager, Compile, and native
-// execution", section "CUDA execution") and the "Garner extension" of the
-// kestrel-llm chain (overview, section 4.2).  Over a tile of 128
-// coefficients and all targets this is a dense 128 x (8 targets) x (8 c)
-// contraction, which this kernel runs on the tensor cores exactly:
+// For digit j (primes d_0..d_{c-1}, product D) every coefficient x with
+// residues x_a is extended to each target prime p outside the digit -- the
+// "mixed-radix decomposition and basis extension" of FHElium's CUDA layer
+// ("Eager, Compile, and native execution", section "CUDA execution") and the
+// "Garner extension" of the kestrel-llm chain (overview, section 4.2).  With
+// the CRT brackets y_a = [x_a (D/d_a)^-1]_{d_a},
+//   sum_a y_a (D/d_a) = X + e D,   e = floor(sum_a y_a / d_a) < c,
+// where X in [0, D) is the coefficient's CRT value.  The approximate
+// conversion stops at X + e D; the exact one subtracts e D.  Over a tile of
+// 128 coefficients and all targets this is a dense 128 x (8 targets) x (8 c)
+// contraction, run on the tensor cores exactly:
 //
-//  * each v_a < 2^50 is split into bytes b_{a,e}; the A operand row of a
+//  * each y_a < 2^50 is split into bytes b_{a,e}; the A operand row of a
 //    coefficient holds the fp16 values 1024 + b_{a,e} (bit pattern
-//    0x6400 | b, one byte permute per two elements);
+//    0x6400 | b, one byte permute per two elements) and 1024 + e in the
+//    spare column 15;
 //  * the B operand (built on the host, tables.cpp: tc_weight_image) holds the
-//    7-bit limbs of W_{a,p} 2^(8e) mod p plus offset columns, so that every
-//    f32 accumulator is 2^23 + (an integer below 2^21): products and sums of
-//    integers below 2^24 are exact in f32, and the accumulator's bit pattern
-//    minus 0x4B000000 is the integer;
+//    7-bit limbs of (D/d_a) 2^(8e) mod p, the limbs of (-D) mod p in column
+//    15 and offset columns, so that every f32 accumulator is 2^23 + (an
+//    integer below 2^21): products and sums of integers below 2^24 are exact
+//    in f32, and the accumulator's bit pattern minus 0x4B000000 is the integer;
 //  * the eight accumulators u_s of a target recombine as
 //    S = sum_s u_s 2^(7s) = (u_0 + .. + u_3 2^21) + 2^28 (u_4 + .. + u_7 2^21).
-//    S < 2^64: u_s <= 8 (6 * 255 + 3) 127 < 2^20.6 for s < 7 (a digit's byte 6
-//    is below 4), and limb 7 of a constant below 2^50 is 0 or 1, so
-//    u_7 < 2^13.6 and S < 2^42 (2^20.6 * 1.008 + 2^13.6 2^7) < 2^63.6.  One
-//    Barrett step with mu = floor(2^64 / p) < 2^16 leaves S mod p below 2 p
-//    (the forward NTT that follows takes inputs of that size).
+//    S < 2^64: u_s <= 8 (6 * 255 + 3) 127 + 7 * 127 < 2^20.6 for s < 7 (a
+//    bracket's byte 6 is below 4), and limb 7 of a constant below 2^50 is 0
+//    or 1, so u_7 < 2^13.6 and S < 2^42 (2^20.6 * 1.008 + 2^13.6 2^7) < 2^63.6.
+//    One Barrett step with mu = floor(2^64 / p) < 2^16 leaves S mod p below
+//    2 p (the forward NTT that follows takes inputs of that size).
 //
-// The integer pipes keep Garner's recursion (c (c - 1) / 2 Shoup products per
-// coefficient) and one Shoup product per output; the c multiply-accumulates
+// e comes from a 64.64 fixed-point sum of y_a / d_a with the reciprocals
+// floor(2^128 / d_a); every term is below the true value by less than 2, so
+// the integer part is e unless the fraction lies within 2 c units of 1 (X near
+// 0 or near D, i.e. small coefficients).  Those lanes compute e exactly:
+// Garner's recursion gives X's mixed-radix digits w_a, X mod 2^64 =
+// sum_a w_a (d_0 .. d_{a-1}) mod 2^64, and with the redundant modulus 2^64
+// e = (sum_a y_a (D/d_a) - X) D^-1 mod 2^64.
+//
+// The integer pipes keep c Shoup products and c fixed-point products per
+// coefficient and one Barrett step per output; the c multiply-accumulates
 // per output of the integer kernel (modup.cu) move to the tensor cores.
 //
 // CTA: 128 threads, thread m owns coefficient m of the tile and row m of the
 // accumulator (TMEM lane m).  Persistent over the tiles of one digit: the
-// digit's B operand and target constants are staged in shared memory once.
+// digit's B operand and constants are staged in shared memory once, and each
+// thread loads its next tile's residues while the current one is converted.
 // Targets are processed in groups of up to 16 (N = 128 columns), one MMA
 // chain of K = 64 (4 instructions) per group into the CTA's 128 TMEM columns.
 #include <cuda_runtime.h>
