@@ -58,24 +58,28 @@ KS_MIN_BYTES_X4 = 8 * N * (PAIRS * (L + 2 * (L + K)) + DNUM * 2 * (L + K))   # 2
 
 def keyswitch_alu_floor_s(pairs: int = PAIRS) -> float:
     """Seconds the integer multiply pipe needs for `pairs` key switches of the
-    bench shape if it did nothing else: every 32-bit product the arithmetic
-    needs, at the pipe's measured per-SM rates (low 64, high 32, wide 25.2 per
-    clock) on 152 SMs at the maximum clock -- the same derivation as
-    ALU_PEAK_BFLY.  Lazy Shoup product (butterfly, Garner step, the tensor-core
-    ModUp's recombination): 3 wide + 2 high + 4 low; multiply-accumulate of
+    bench shape if it did nothing else: every 32-bit product the kernels
+    execute on it, at the pipe's measured per-SM rates (low 64, high 32, wide
+    25.2 per clock) on 152 SMs at the maximum clock -- the same derivation as
+    ALU_PEAK_BFLY.  Lazy Shoup product (butterfly, CRT bracket): 3 wide +
+    2 high + 4 low; fixed-point term of the correction count (64 x 16-bit low
+    product + 64 x 64 high product): 4 wide + 1 high + 1 low; 64-bit Barrett
+    step with a 16-bit mu: 2 wide + 1 high + 1 low; multiply-accumulate of
     25-bit halves: 3 wide; reduction of a 105-bit sum: 5 wide + 2 high + 3 low.
-    Per (coefficient, digit): alpha (alpha - 1) / 2 Garner products, then per
-    target outside the digit one Shoup product (the extension's dot product
-    itself runs on the tensor cores, KS_TENSOR_FLOP); per output residue of the
-    inner product: 2 dnum multiply-accumulates and 2 reductions."""
+    Per (coefficient, digit) the tensor-core ModUp does alpha brackets, alpha
+    fixed-point terms and one Barrett step per target (its dot products run on
+    the tensor cores, KS_TENSOR_FLOP); per output residue of the inner product:
+    2 dnum multiply-accumulates and 2 reductions."""
     lo, hi, wide = 1 / 64.0, 1 / 32.0, 1 / 25.2          # SM-cycles per 32-bit product
     shoup, mac, red = 3 * wide + 2 * hi + 4 * lo, 3 * wide, 5 * wide + 2 * hi + 3 * lo
+    fixp, barrett = 4 * wide + hi + lo, 2 * wide + hi + lo
     alpha = L // DNUM
     targets = L + K - alpha
     bfly = pairs * DNUM * (L + K) * (N // 2) * LOG_N
     units = pairs * DNUM * N
     ip = pairs * (L + K) * N
-    cycles = bfly * shoup + units * (alpha * (alpha - 1) // 2 + targets) * shoup + ip * (2 * DNUM * mac + 2 * red)
+    cycles = (bfly * shoup + units * (alpha * (shoup + fixp) + targets * barrett)
+              + ip * (2 * DNUM * mac + 2 * red))
     return cycles / (SMS * SM_MAX_MHZ * 1e6)
 
 
@@ -493,11 +497,16 @@ def ours(args):
         poll = NvmlClockPoller(device).start()
         start.record(stream)
         for i in range(args.steps):
-            run_step(st, args.warmup + i, evs[i])
+            run_step(st, args.warmup + i)
         stop.record(stream)
         barrier()
+        launches = api.launch_count() - launches0
+        # the same steps again with an event between calls, for the per-call times the rooflines use
+        # (an event between two calls also ends the early placement of the second call's CTAs)
+        for i in range(args.steps):
+            run_step(st, args.warmup + args.steps + i, evs[i])
+        barrier()
         poll.stop()
-    launches = api.launch_count() - launches0
     ms = start.elapsed_time(stop) / args.steps
     per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)] for i in range(args.steps)]
     kern = [statistics.mean(p[j] for p in per) for j in range(6)]
@@ -550,7 +559,7 @@ def ours(args):
                      "traffic_unit": "bytes/launch", "traffic_source": TRAFFIC_SOURCE,
                      "algorithmic_bytes": NTT_BYTES_PER_FWD,
                      "kernel": "forward NTT call = k_ntt_fwd_cols<16,6,3> (first 6 stages, strided columns) + "
-                               "k_ntt_fwd_blk<16,6,6,4,8> (last 10 stages, one CTA per 1024-residue block); "
+                               "k_ntt_fwd_blk<16,6,6,4,10> (last 10 stages, one CTA per 1024-residue block); "
                                "n=2^16, 384 rows; traffic = both launches",
                      "peak_kind": "derived: measured integer-pipe rates x 152 SMs x 2070 MHz",
                      "measured_butterfly_ceiling": ceiling / 1e9, "frac_of_measured_ceiling": achieved_bfly / ceiling,
@@ -578,11 +587,12 @@ def ours(args):
                                "traffic": kernel_traffic("keyswitch", KS_T), "traffic_unit": "bytes/call",
                                "traffic_source": TRAFFIC_SOURCE,
                                "tensor_flop": KS_TENSOR_FLOP,
-                               "work": "4 key switches of [24][n] over 24 + 8 primes, dnum = 3: ModUp (28 Garner products "
-                                       "+ 24 Shoup products per coefficient and digit on the integer pipes; the "
-                                       "extension's 128 x 192 x 64 fp16 products per tile of 128 coefficients on the "
-                                       "tensor cores), 384 NTT rows, inner product (6 multiply-accumulates + 2 "
-                                       "reductions per output residue); HBM floor: inputs + keys (read once) + outputs"},
+                               "work": "4 key switches of [24][n] over 24 + 8 primes, dnum = 3: ModUp (8 CRT brackets, 8 "
+                                       "fixed-point terms and 24 Barrett steps per coefficient and digit on the integer "
+                                       "pipes; the extension's 128 x 192 x 64 fp16 products per tile of 128 "
+                                       "coefficients on the tensor cores), 384 NTT rows, inner product (6 "
+                                       "multiply-accumulates + 2 reductions per output residue); HBM floor: inputs + "
+                                       "keys (read once) + outputs"},
         "clocks": clocks,
         "gpu_launches": launches,
         "two_streams": {"value": whole_job_rate(UNITS, ws, two_ms), "unit": UNIT, "ms_per_step": two_ms,
