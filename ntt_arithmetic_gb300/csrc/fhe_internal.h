@@ -34,7 +34,7 @@ struct ModupTcFrac {
 struct ModupTcTarget {
     uint64_t p;      // the target prime
     uint64_t mu;     // floor(2^64 / p) (< 2^16)
-    uint64_t zero;   // padding (keeps the record 32 bytes)
+    uint64_t aux;    // added to each output by ModDown with nearest rounding: (p - h) mod p; 0 for ModUp
     uint64_t limb;   // index of p in the extended basis
 };
 // The tensor-core extension takes digits of up to kTcMaxAlpha primes: one
@@ -67,6 +67,12 @@ bool modup_shape_ok(int L, int K, int dnum);
 struct ModdownLayout {
     size_t off_garner;   // [K][K] pairs: p_b^-1 mod p_a (b < a)
     size_t off_mr;       // [L][K] split factors: prod_{b<a} p_b mod q_l
+    // tensor-core conversion (K <= kTcMaxAlpha; tc_tmax = 0 otherwise), as ModupLayout's for one digit:
+    int tc_tmax;         // target slots (L rounded up to even)
+    size_t off_tc_qinv;  // [K] pairs: (P / p_a)^-1 mod p_a
+    size_t off_tc_tgt;   // [tc_tmax] ModupTcTarget
+    size_t off_tc_frac;  // [kTcMaxAlpha + 1] ModupTcFrac
+    size_t off_tc_b;     // [8 tc_tmax rows][64] fp16 weight limbs
     size_t off_hp;       // [K] words: (P-1)/2 mod p_k
     size_t off_hq;       // [L] words: (P-1)/2 mod q_l
     size_t off_pinv;     // [L] pairs: P^-1 mod q_l
@@ -112,6 +118,10 @@ int launch_modup(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, i
 // shape has no tensor-core form (alpha > kTcMaxAlpha, n < 128).
 int launch_modup_tc(uint64_t *ext, const uint64_t *in, long in_stride, int log_n, int L, int K, int dnum, int batch,
                     bool approx, const fhe_ntt_tables *t, const void *modup, void *stream);
+// ModDown's NTT-domain conversion d = ((X + h) mod P) - h mod q_l on the tensor
+// cores (below 3 q_l); returns 0 without launching when K > kTcMaxAlpha or n < 128.
+int launch_moddown_tc(uint64_t *d, const uint64_t *src, long src_item, int log_n, int L, int K, int batch, bool nearest,
+                      const fhe_ntt_tables *t_qp, const void *md, void *stream);
 // Synchronize the device, then read (and optionally clear) the status word
 // of the tensor-core kernels.
 int device_status(int *status, bool reset);

@@ -206,11 +206,16 @@ int launch_moddown(uint64_t *out, const uint64_t *in, int log_n, int L, int K, i
         src = pl;
         src_item = (long)K << log_n;
     }
-    if (K <= 1) launch_conv<1>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
-    else if (K <= 2) launch_conv<2>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
-    else if (K <= 4) launch_conv<4>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
-    else if (K <= 8) launch_conv<8>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
-    else launch_conv<16>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+    // the NTT-domain conversion on the tensor cores where the shape allows (K <= 8, n >= 128)
+    const int tc = ntt_domain ? launch_moddown_tc(d, src, src_item, log_n, L, K, batch, nearest, t_qp, md, stream) : 0;
+    if (tc < 0) return -1;
+    if (tc == 0) {
+        if (K <= 1) launch_conv<1>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+        else if (K <= 2) launch_conv<2>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+        else if (K <= 4) launch_conv<4>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+        else if (K <= 8) launch_conv<8>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+        else launch_conv<16>(d, src, src_item, log_n, L, K, batch, nearest, !ntt_domain, lay, md, t_qp, st);
+    }
     if (cudaGetLastError() != cudaSuccess) return -1;
     launched++;
     if (!ntt_domain) return launched;

@@ -74,42 +74,47 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int T) {
     return (size_t)kTileBytesA + (size_t)((T + 1) & ~1) * 8 * kTcRowBytes + (size_t)T * sizeof(ModupTcTarget);
 }
 
-template <bool APPROX>
-__global__ void __launch_bounds__(kTcThreads, 4)
-k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int batch,
-           int alpha, const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ qinv,
-           const ulonglong2 *__restrict__ garner, const ModupTcFrac *__restrict__ frac,
-           const ModupTcTarget *__restrict__ tgt, const uint4 *__restrict__ wimg, int tmax,
-           const uint64_t *__restrict__ consts) {
-    pdl_begin();
-    // qinv: the brackets' constants [dnum][alpha]; garner: [dnum][alpha][alpha] (the exact fallback)
-    extern __shared__ __align__(1024) uint8_t sm[];   // [A operand][B operand][targets]
+// One source basis (a ModUp digit, or ModDown's P) of `cnt` primes extended to
+// its T targets, for every coefficient of `batch` items: the body shared by
+// k_modup_tc (MD = false: the digit's own limbs are copied to `out` as well)
+// and k_moddown_tc (MD = true: the inputs get h added, the outputs get the
+// target's `aux` added).  Source limb a of item bi is at
+// in + bi in_stride + (lo + a) n; output row `limb` of item bi and digit j at
+// out + ((bi dnum + j) out_rows + limb) n.
+template <bool APPROX, bool MD>
+__device__ __forceinline__ void ext_tc(uint8_t *sm, uint64_t *__restrict__ out, int out_rows,
+                                       const uint64_t *__restrict__ in, long in_stride, int log_n, int batch,
+                                       int lo, int cnt, int T, int j, int dnum, const ulonglong2 *__restrict__ qinv,
+                                       const ulonglong2 *__restrict__ garner, int gstride,
+                                       const ModupTcFrac *__restrict__ frac, const ModupTcTarget *__restrict__ tgt,
+                                       const uint4 *__restrict__ wimg, const uint64_t *__restrict__ src_consts,
+                                       const uint64_t *__restrict__ hsrc) {
+    // qinv: the brackets' constants [cnt]; garner: [cnt][gstride] (the exact fallback)
     __shared__ uint64_t mbar;
     __shared__ uint32_t tslot;
     const int t = threadIdx.x, warp = t >> 5;
-    const int j = blockIdx.y, dnum = gridDim.y;
-    const int lo = dg[j].lo, cnt = dg[j].count, T = LK - cnt, Tp = (T + 1) & ~1;
+    const int Tp = (T + 1) & ~1;
     uint8_t *sA = sm, *sB = sm + kTileBytesA;
     ModupTcTarget *sT = reinterpret_cast<ModupTcTarget *>(sB + (size_t)Tp * 8 * kTcRowBytes);
-    // the digit's constants, read inside the per-coefficient dependency chains
+    // the basis' constants, read inside the per-coefficient dependency chains
     __shared__ ulonglong2 sQ[kTcMaxAlpha];                   // bracket constants (D/d_a)^-1 mod d_a
     __shared__ ulonglong2 sG[kTcMaxAlpha * kTcMaxAlpha];     // Garner: (a, b) = d_b^-1 mod d_a, b < a
     __shared__ ModupTcFrac sF[kTcMaxAlpha + 1];              // reciprocals, redundant-modulus constants
-    __shared__ uint64_t sD[kTcMaxAlpha];
+    __shared__ uint64_t sD[kTcMaxAlpha], sH[kTcMaxAlpha];    // the source primes, h mod each (ModDown)
     {
-        const uint4 *src = wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16;
         for (int e = t; e < Tp * 8 * kTcRowBytes / 16; e += kTcThreads)
-            reinterpret_cast<uint4 *>(sB)[e] = __ldg(src + e);
-        for (int e = t; e < T; e += kTcThreads) sT[e] = tgt[(size_t)j * tmax + e];
+            reinterpret_cast<uint4 *>(sB)[e] = __ldg(wimg + e);
+        for (int e = t; e < T; e += kTcThreads) sT[e] = tgt[e];
         for (int e = t; e < kTcMaxAlpha * kTcMaxAlpha; e += kTcThreads) {
             const int a = e / kTcMaxAlpha, b = e - a * kTcMaxAlpha;
-            sG[e] = (a < cnt && b < a) ? __ldg(garner + ((long)j * alpha + a) * alpha + b) : make_ulonglong2(0, 0);
+            sG[e] = (a < cnt && b < a) ? __ldg(garner + a * gstride + b) : make_ulonglong2(0, 0);
         }
         if (t < kTcMaxAlpha) {
-            sQ[t] = t < cnt ? __ldg(qinv + (long)j * alpha + t) : make_ulonglong2(0, 0);
-            sD[t] = t < cnt ? __ldg(consts + (long)(lo + t) * K_COUNT + K_Q) : 0;
+            sQ[t] = t < cnt ? __ldg(qinv + t) : make_ulonglong2(0, 0);
+            sD[t] = t < cnt ? __ldg(src_consts + (long)(lo + t) * K_COUNT + K_Q) : 0;
+            sH[t] = (MD && hsrc && t < cnt) ? __ldg(hsrc + t) : 0;
         }
-        if (t <= kTcMaxAlpha) sF[t] = frac[(long)j * (kTcMaxAlpha + 1) + t];
+        if (t <= kTcMaxAlpha) sF[t] = frac[t];
     }
     if (warp == 0) tmem_alloc(&tslot, 128);
     if (t == 0) mbar_init(&mbar, 1);
@@ -141,6 +146,11 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
 #pragma unroll
         for (int a = 0; a < kTcMaxAlpha; a++) x[a] = xn[a];
         if (tile + gridDim.x < tiles) load_tile(tile + gridDim.x);
+        if constexpr (MD) {   // the residues of X + h
+#pragma unroll
+            for (int a = 0; a < kTcMaxAlpha; a++)
+                if (a < cnt) x[a] = csub(x[a] + sH[a], sD[a]);
+        }
         // CRT brackets v_a = [x_a (D/d_a)^-1]_{d_a}: sum_a v_a (D/d_a) = X + e D with
         // e = floor(sum_a v_a / d_a) < cnt
 #pragma unroll
@@ -196,10 +206,12 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
                 ec = (uint32_t)((Y - X) * sF[kTcMaxAlpha].dhat64);
             }
         }
-        uint64_t *dst = ext + (((long)bi * dnum + j) * LK << log_n) + i;
+        uint64_t *dst = out + (((long)bi * dnum + j) * out_rows << log_n) + i;
+        if constexpr (!MD) {
 #pragma unroll
-        for (int a = 0; a < kTcMaxAlpha; a++)
-            if (a < cnt) __stcs(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
+            for (int a = 0; a < kTcMaxAlpha; a++)
+                if (a < cnt) __stcs(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
+        }
         // A operand row: fp16 1024 + byte, eight per digit (byte 7 of v_a < 2^50 is 0);
         // column 15 (byte 7 of v_1) carries 1024 + e
 #pragma unroll
@@ -249,7 +261,9 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
                         const uint64_t l4 = (uint64_t)p23 * (1u << 14) + p01;   // d_0 + .. + d_3 2^21
                         const uint64_t h4 = (uint64_t)p67 * (1u << 14) + p45;   // d_4 + .. + d_7 2^21
                         const ModupTcTarget &tg = sT[g0 + tt + h];
-                        __stcs(dst + ((long)tg.limb << log_n), reduce64_small_mu(l4 + (h4 << 28), tg.p, tg.mu));
+                        const uint64_t r = reduce64_small_mu(l4 + (h4 << 28), tg.p, tg.mu);
+                        if constexpr (MD) __stcg(dst + ((long)tg.limb << log_n), hsrc ? r + tg.aux : r);
+                        else __stcs(dst + ((long)tg.limb << log_n), r);
                     }
                 }
             }
@@ -265,6 +279,36 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+template <bool APPROX>
+__global__ void __launch_bounds__(kTcThreads, 4)
+k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_stride, int log_n, int LK, int batch,
+           int alpha, const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ qinv,
+           const ulonglong2 *__restrict__ garner, const ModupTcFrac *__restrict__ frac,
+           const ModupTcTarget *__restrict__ tgt, const uint4 *__restrict__ wimg, int tmax,
+           const uint64_t *__restrict__ consts) {
+    pdl_begin();
+    extern __shared__ __align__(1024) uint8_t sm[];   // [A operand][B operand][targets]
+    const int j = blockIdx.y;
+    const int lo = dg[j].lo, cnt = dg[j].count;
+    ext_tc<APPROX, false>(sm, ext, LK, in, in_stride, log_n, batch, lo, cnt, LK - cnt, j, gridDim.y,
+                          qinv + (long)j * alpha, garner + (long)j * alpha * alpha, alpha,
+                          frac + (long)j * (kTcMaxAlpha + 1), tgt + (long)j * tmax,
+                          wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16, consts, nullptr);
+}
+
+// ModDown's conversion d_l = ((X + h) mod P) - h mod q_l (below 3 q_l, for the
+// forward NTT) from the P limbs in[b][k][n], K <= kTcMaxAlpha.
+__global__ void __launch_bounds__(kTcThreads, 4)
+k_moddown_tc(uint64_t *__restrict__ d, const uint64_t *__restrict__ in, long in_stride, int log_n, int L, int K,
+             int batch, const ulonglong2 *__restrict__ qinv, const ulonglong2 *__restrict__ garner,
+             const ModupTcFrac *__restrict__ frac, const ModupTcTarget *__restrict__ tgt,
+             const uint4 *__restrict__ wimg, const uint64_t *__restrict__ consts_p, const uint64_t *__restrict__ hp) {
+    pdl_begin();
+    extern __shared__ __align__(1024) uint8_t sm[];
+    ext_tc<false, true>(sm, d, L, in, in_stride, log_n, batch, 0, K, L, 0, 1, qinv, garner, K, frac, tgt, wimg,
+                        consts_p, hp);
 }
 
 }  // namespace
@@ -293,6 +337,28 @@ int launch_modup_tc(uint64_t *ext, const uint64_t *in, long in_stride, int log_n
         (const ulonglong2 *)(base + lay.off_qinv), (const ulonglong2 *)(base + lay.off_garner),
         (const ModupTcFrac *)(base + lay.off_tc_frac), (const ModupTcTarget *)(base + lay.off_tc_tgt),
         (const uint4 *)(base + lay.off_tc_b), lay.tc_tmax, t->consts);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_moddown_tc(uint64_t *d, const uint64_t *src, long src_item, int log_n, int L, int K, int batch, bool nearest,
+                      const fhe_ntt_tables *t_qp, const void *md, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const ModdownLayout lay = moddown_layout(L, K);
+    if (lay.tc_tmax == 0 || log_n < 7) return 0;
+    const size_t need = tc_smem_bytes(L);
+    const size_t smem = need > 47104 ? need : 47104;   // at most 4 CTAs per SM (TMEM)
+    if (cudaFuncSetAttribute(k_moddown_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    const int per_sm = (int)(228 * 1024 / (smem + 1024)) < 4 ? (int)(228 * 1024 / (smem + 1024)) : 4;
+    const long tiles = (long)batch << (log_n - 7);
+    long gx = (long)sm_count() * per_sm;
+    if (gx > tiles) gx = tiles;
+    const char *base = (const char *)md;
+    launch_pdl(k_moddown_tc, dim3((unsigned)gx), kTcThreads, smem, st, d, src, src_item, log_n, L, K, batch,
+               (const ulonglong2 *)(base + lay.off_tc_qinv), (const ulonglong2 *)(base + lay.off_garner),
+               (const ModupTcFrac *)(base + lay.off_tc_frac), (const ModupTcTarget *)(base + lay.off_tc_tgt),
+               (const uint4 *)(base + lay.off_tc_b), t_qp->consts + (long)L * K_COUNT,
+               nearest ? (const uint64_t *)(base + lay.off_hp) : (const uint64_t *)nullptr);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

@@ -138,7 +138,14 @@ ModdownLayout moddown_layout(int L, int K) {
     s.off_hp = align256(s.off_mr + (size_t)L * K * 16);
     s.off_hq = align256(s.off_hp + (size_t)K * 8);
     s.off_pinv = align256(s.off_hq + (size_t)L * 8);
-    s.bytes = align256(s.off_pinv + (size_t)L * 16);
+    const size_t end = align256(s.off_pinv + (size_t)L * 16);
+    const bool tc = K <= kTcMaxAlpha;
+    s.tc_tmax = tc ? (L + 1) & ~1 : 0;
+    s.off_tc_qinv = end;
+    s.off_tc_tgt = align256(s.off_tc_qinv + (tc ? (size_t)K * 16 : 0));
+    s.off_tc_frac = align256(s.off_tc_tgt + (size_t)s.tc_tmax * sizeof(ModupTcTarget));
+    s.off_tc_b = align256(s.off_tc_frac + (tc ? (size_t)(kTcMaxAlpha + 1) * sizeof(ModupTcFrac) : 0));
+    s.bytes = align256(s.off_tc_b + (size_t)s.tc_tmax * 8 * kTcRowBytes);
     return s;
 }
 
@@ -341,6 +348,49 @@ static void tc_weight_image(uint8_t *img, int cnt, int T, const uint64_t *W, con
     }
 }
 
+// The tensor-core extension's constants for the source basis d[0..cnt) (product
+// D) and the targets p[0..T) (basis indices limb[t], output offsets aux[t]):
+// the target records, the weight operand ((D/d_a) mod p and the correction
+// (-D) mod p), and per source prime the reciprocal floor(2^128 / d_a) with
+// the redundant-modulus constants (D/d_a) mod 2^64 and d_0 .. d_{a-1} mod 2^64
+// (entry kTcMaxAlpha: D^-1 mod 2^64).
+static void tc_build_basis(const uint64_t *d, int cnt, const uint64_t *p, const int *limb, const uint64_t *aux, int T,
+                           ModupTcTarget *tg, ModupTcFrac *fr, uint8_t *img) {
+    std::vector<uint64_t> W((size_t)cnt * T), corr(T);
+    for (int t = 0; t < T; t++) {
+        tg[t].p = p[t];
+        tg[t].mu = (uint64_t)(((u128)1 << 64) / p[t]);
+        tg[t].aux = aux ? aux[t] : 0;
+        tg[t].limb = (uint64_t)limb[t];
+        uint64_t Dp = 1 % p[t];
+        for (int a = 0; a < cnt; a++) {
+            Dp = mul_mod(Dp, d[a] % p[t], p[t]);
+            uint64_t hp = 1 % p[t];
+            for (int b = 0; b < cnt; b++)
+                if (b != a) hp = mul_mod(hp, d[b] % p[t], p[t]);
+            W[(size_t)a * T + t] = hp;            // (D / d_a) mod p
+        }
+        corr[t] = (p[t] - Dp) % p[t];             // (-D) mod p
+    }
+    tc_weight_image(img, cnt, T, W.data(), p, corr.data());
+    uint64_t D64 = 1, W64 = 1;
+    for (int a = 0; a < cnt; a++) D64 *= d[a];
+    for (int a = 0; a < cnt; a++) {
+        const u128 phi = ~(u128)0 / d[a];         // floor((2^128 - 1) / d_a) = floor(2^128 / d_a): d_a is odd
+        fr[a].phi_hi = (uint64_t)(phi >> 64);
+        fr[a].phi_lo = (uint64_t)phi;
+        uint64_t h = 1;
+        for (int b = 0; b < cnt; b++)
+            if (b != a) h *= d[b];
+        fr[a].dhat64 = h;                         // (D / d_a) mod 2^64
+        fr[a].w64 = W64;                          // d_0 ... d_{a-1} mod 2^64
+        W64 *= d[a];
+    }
+    uint64_t inv = D64;                           // D^-1 mod 2^64 (D odd): Newton on the 2-adic inverse
+    for (int k = 0; k < 6; k++) inv *= 2 - D64 * inv;
+    fr[kTcMaxAlpha].dhat64 = inv;
+}
+
 extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_t *qp, void *host_blob,
                                            size_t bytes) {
     if (!qp || !host_blob || !modup_shape_ok(L, K, dnum)) return FHE_EINVAL;
@@ -399,49 +449,19 @@ extern "C" int fhe_modup_tables_build_host(int L, int K, int dnum, const uint64_
             }
         }
         if (lay.tc_tmax > 0) {
-            // the digit's targets (every prime outside it) and both weight operands
+            // the digit's targets (every prime outside it)
             const int cnt = hi - lo, T = LK - cnt;
-            ModupTcTarget *tg = (ModupTcTarget *)(base + lay.off_tc_tgt) + (size_t)j * lay.tc_tmax;
-            std::vector<uint64_t> P(T), Wa((size_t)cnt * T), corr(T);
-            for (int l = 0, t = 0; l < LK; l++) {
-                if (l >= lo && l < hi) continue;
-                const uint64_t p = qp[l];
-                tg[t].p = p;
-                tg[t].mu = (uint64_t)(((u128)1 << 64) / p);
-                tg[t].limb = (uint64_t)l;
-                P[t] = p;
-                uint64_t Dp = 1 % p;
-                for (int a = 0; a < cnt; a++) {
-                    Dp = mul_mod(Dp, qp[lo + a] % p, p);
-                    uint64_t hp = 1 % p;
-                    for (int b = 0; b < cnt; b++)
-                        if (b != a) hp = mul_mod(hp, qp[lo + b] % p, p);
-                    Wa[(size_t)a * T + t] = hp;     // (D_j / d_a) mod p
+            std::vector<uint64_t> P;
+            std::vector<int> limb;
+            for (int l = 0; l < LK; l++)
+                if (l < lo || l >= hi) {
+                    P.push_back(qp[l]);
+                    limb.push_back(l);
                 }
-                corr[t] = (p - Dp) % p;             // (-D_j) mod p
-                t++;
-            }
-            const size_t img = (size_t)lay.tc_tmax * 8 * kTcRowBytes;
-            tc_weight_image((uint8_t *)(base + lay.off_tc_b) + j * img, cnt, T, Wa.data(), P.data(), corr.data());
-            // fixed-point reciprocals and the redundant-modulus constants
-            ModupTcFrac *fr = (ModupTcFrac *)(base + lay.off_tc_frac) + (size_t)j * (kTcMaxAlpha + 1);
-            uint64_t D64 = 1, W64 = 1;
-            for (int a = 0; a < cnt; a++) D64 *= qp[lo + a];
-            for (int a = 0; a < cnt; a++) {
-                const uint64_t da = qp[lo + a];
-                const u128 phi = ~(u128)0 / da;     // floor((2^128 - 1) / d_a) = floor(2^128 / d_a): d_a is odd
-                fr[a].phi_hi = (uint64_t)(phi >> 64);
-                fr[a].phi_lo = (uint64_t)phi;
-                uint64_t h = 1;
-                for (int b = 0; b < cnt; b++)
-                    if (b != a) h *= qp[lo + b];
-                fr[a].dhat64 = h;                   // (D_j / d_a) mod 2^64
-                fr[a].w64 = W64;                    // d_0 ... d_{a-1} mod 2^64
-                W64 *= da;
-            }
-            uint64_t inv = D64;                     // D_j^-1 mod 2^64 (D_j odd), Newton on the 2-adic inverse
-            for (int k = 0; k < 6; k++) inv *= 2 - D64 * inv;
-            fr[kTcMaxAlpha].dhat64 = inv;
+            tc_build_basis(qp + lo, cnt, P.data(), limb.data(), nullptr, T,
+                           (ModupTcTarget *)(base + lay.off_tc_tgt) + (size_t)j * lay.tc_tmax,
+                           (ModupTcFrac *)(base + lay.off_tc_frac) + (size_t)j * (kTcMaxAlpha + 1),
+                           (uint8_t *)(base + lay.off_tc_b) + (size_t)j * lay.tc_tmax * 8 * kTcRowBytes);
         }
     }
     return FHE_OK;
@@ -556,6 +576,25 @@ extern "C" int fhe_moddown_tables_build_host(int L, int K, const uint64_t *qp, v
         const uint64_t pi = inv_mod(prod, q);
         pinv[l * 2] = pi;
         pinv[l * 2 + 1] = shoup(pi, q);
+    }
+    if (lay.tc_tmax > 0) {
+        // the tensor-core conversion from P to every q_l; aux = (q_l - h) mod q_l for nearest rounding
+        std::vector<int> limb(L);
+        std::vector<uint64_t> aux(L);
+        for (int l = 0; l < L; l++) {
+            limb[l] = l;
+            aux[l] = (qp[l] - hq[l]) % qp[l];
+        }
+        tc_build_basis(P, K, qp, limb.data(), aux.data(), L, (ModupTcTarget *)(base + lay.off_tc_tgt),
+                       (ModupTcFrac *)(base + lay.off_tc_frac), (uint8_t *)(base + lay.off_tc_b));
+        uint64_t *qi = (uint64_t *)(base + lay.off_tc_qinv);
+        for (int a = 0; a < K; a++) {
+            uint64_t h = 1 % P[a];
+            for (int b = 0; b < K; b++)
+                if (b != a) h = mul_mod(h, P[b] % P[a], P[a]);
+            qi[a * 2] = inv_mod(h, P[a]);                 // (P / p_a)^-1 mod p_a
+            qi[a * 2 + 1] = shoup(qi[a * 2], P[a]);
+        }
     }
     return FHE_OK;
 }

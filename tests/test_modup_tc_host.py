@@ -192,3 +192,78 @@ def test_no_tensor_core_section_for_wide_digits(lib):
     nb = ctypes.c_size_t()
     assert lib.fhe_modup_tables_bytes(24, 8, 2, ctypes.byref(nb)) == 0
     assert nb.value == lay["bytes"]
+
+
+def moddown_layout(L: int, K: int) -> dict:
+    """The ModDown blob's layout (the tensor-core sections after the integer kernel's)."""
+    off_mr = a256(K * K * 16)
+    off_hp = a256(off_mr + L * K * 16)
+    off_hq = a256(off_hp + K * 8)
+    off_pinv = a256(off_hq + L * 8)
+    end = a256(off_pinv + L * 16)
+    tc = K <= MAXA
+    tmax = (L + 1) & ~1 if tc else 0
+    off_qinv = end
+    off_tgt = a256(off_qinv + (K * 16 if tc else 0))
+    off_frac = a256(off_tgt + tmax * 32)
+    off_b = a256(off_frac + ((MAXA + 1) * 32 if tc else 0))
+    return {"tmax": tmax, "hp": off_hp, "hq": off_hq, "pinv": off_pinv, "qinv": off_qinv, "tgt": off_tgt,
+            "frac": off_frac, "b": off_b, "bytes": a256(off_b + tmax * 8 * ROWB)}
+
+
+@pytest.mark.parametrize("L,K,nearest", [(24, 8, True), (24, 8, False), (5, 3, True), (7, 1, True)])
+def test_tensor_core_moddown_encoding(lib, L, K, nearest):
+    """ModDown's tensor-core conversion d_l = ((X + h) mod P) - h mod q_l from the ModDown blob, replayed and
+    finished as (x_l - d_l) P^-1 mod q_l, against the oracle's ModDown."""
+    qp = [int(v) for v in oracle.primes(1 << 12, L + K)]
+    lay = moddown_layout(L, K)
+    nb = ctypes.c_size_t()
+    assert lib.fhe_moddown_tables_bytes(L, K, ctypes.byref(nb)) == 0
+    assert nb.value == lay["bytes"], "the layout replayed here matches the library's"
+    blob = np.zeros(nb.value, dtype=np.uint8)
+    arr = (ctypes.c_uint64 * len(qp))(*qp)
+    assert lib.fhe_moddown_tables_build_host(L, K, arr, blob.ctypes.data_as(ctypes.c_void_p), nb.value) == 0
+    P = qp[L:]
+    Pprod = math.prod(P)
+    tmax = lay["tmax"]
+    tg = blob[lay["tgt"]:lay["tgt"] + tmax * 32].view(np.uint64).reshape(tmax, 4)
+    fr = blob[lay["frac"]:lay["frac"] + (MAXA + 1) * 32].view(np.uint64).reshape(MAXA + 1, 4)
+    qi = blob[lay["qinv"]:lay["qinv"] + K * 16].view(np.uint64).reshape(K, 2)
+    hp = blob[lay["hp"]:lay["hp"] + K * 8].view(np.uint64)
+    for a in range(K):
+        assert int(qi[a, 0]) == pow(Pprod // P[a], -1, P[a])
+    Bw = weight_operand(blob, lay["b"], 8 * tmax)
+    assert (Bw.sum(axis=1) == 8192).all() and (Bw >= 0).all() and (Bw <= 2048).all()
+    rng = np.random.default_rng(L * 10 + K)
+    m = 16
+    x = [[int(v) for v in rng.integers(0, qp[l], m, dtype=np.uint64)] for l in range(L + K)]
+    for l in range(L + K):          # edge coefficients: 0 and q - 1 in every limb
+        x[l][0], x[l][1] = 0, qp[l] - 1
+    A = np.full((m, 64), 1024, dtype=np.int64)
+    for c in range(m):
+        xs = [(x[L + a][c] + (int(hp[a]) if nearest else 0)) % P[a] for a in range(K)]
+        y, e, _ = correction_count(xs, P, fr, False)
+        for a in range(K):
+            for k in range(7):
+                A[c, 8 * a + k] = 1024 + ((y[a] >> (8 * k)) & 255)
+        A[c, 15] = 1024 + e
+    Dacc = A @ Bw.T
+    assert (Dacc >= 1 << 23).all() and (Dacc < (1 << 23) + (1 << 21)).all()
+    U = Dacc - (1 << 23)
+    out = np.zeros((L, m), dtype=np.uint64)
+    h = (Pprod - 1) // 2 if nearest else 0
+    for t in range(L):
+        q, mu, aux, limb = (int(v) for v in tg[t])
+        assert limb == t and q == qp[t] and mu == (1 << 64) // q
+        assert aux == (q - ((Pprod - 1) // 2) % q) % q, "aux holds (q - h) mod q; truncation does not add it"
+        pinv = pow(Pprod, -1, q)
+        for c in range(m):
+            S = sum(int(U[c, 8 * t + s]) << (7 * s) for s in range(8))
+            assert S < 1 << 64
+            r = S - ((S * mu) >> 64) * q
+            d = r + (aux if nearest else 0)
+            assert d < 3 * q, "d stays below 3 q for the forward NTT"
+            out[t, c] = (x[t][c] - d) * pinv % q
+    a_in = np.array(x, dtype=np.uint64).reshape(1, L + K, m)
+    want = oracle.moddown_batch(a_in, np.array(qp, dtype=np.uint64), L, K, nearest)[0]
+    assert np.array_equal(out, want)
