@@ -830,7 +830,7 @@ class ModdownRow(RowBench):
     workload = ("ModDown of the 4 key-switch outputs KS[4][2][32][n] of the headline step (NTT domain, nearest "
                 "rounding, P = 8 primes) -> [4][2][24][n]; n=2^16")
     units_per_step = 8
-    traffic_rows = 8 * L         # output rows of the captured launch
+    traffic_rows = 8 * L         # output rows of the captured call
 
     def setup(self, dev):
         import torch
@@ -850,14 +850,24 @@ class ModdownRow(RowBench):
         api.moddown(self.out, self.x, L, K, self.t, self.md, domain="ntt", nearest=True, workspace=self.ws)
 
     def probe(self):
-        from ntt_arithmetic_gb300 import api
-        per_coeff = K * (K - 1) // 2 + L * (K - 1) + L      # Garner + extension + final products
-        ops = 8 * N * per_coeff
-        fn = lambda: api.moddown(self.out, self.x, L, K, self.t, self.md, domain="coeff", nearest=True,
-                                 workspace=self.ws)
-        return fn, {"bound": "alu", "work": ops, "peak": ALU_PEAK_SHOUP / 1e9, "unit": "Gmodmul/s",
-                    "kernel": "k_moddown_conv<8,fused> (coefficient-domain ModDown, one pass, batch 8)",
-                    "work_note": f"{per_coeff} lazy Shoup products per coefficient x 8 x 2^16 coefficients",
+        # the row's own call, against the integer-pipe floor of its products, in units of one lazy Shoup
+        # product (the butterfly peak's unit): the inverse NTT of the 8 x 8 rows of P limbs and the forward
+        # NTT of the 8 x 24 rows of d (one Shoup product per butterfly), the tensor-core conversion's K CRT
+        # brackets, K fixed-point terms and L Barrett steps per coefficient, and one Shoup product per output
+        lo, hi, wide = 1 / 64.0, 1 / 32.0, 1 / 25.2
+        shoup = 3 * wide + 2 * hi + 4 * lo
+        fixp, barrett = 4 * wide + hi + lo, 2 * wide + hi + lo
+        bfly = 8 * (K + L) * (N // 2) * LOG_N
+        conv = 8 * N * (K * (shoup + fixp) + L * barrett) / shoup
+        final = 8 * L * N
+        ops = bfly + conv + final
+        fn = self.step
+        return fn, {"bound": "alu", "work": ops, "peak": ALU_PEAK_SHOUP / 1e9, "unit": "G Shoup-product equivalents/s",
+                    "kernel": "one NTT-domain ModDown call, batch 8: k_ntt_inv_blk + k_ntt_inv_cols (64 rows of P "
+                              "limbs), k_moddown_tc (conversion on the tensor cores), k_ntt_fwd_cols + "
+                              "k_ntt_fwd_blk_md (192 rows of d + the last product)",
+                    "work_note": (f"{bfly / 1e6:.1f} M butterflies + {conv / 1e6:.1f} M (conversion, as Shoup "
+                                  f"products) + {final / 1e6:.1f} M final products"),
                     "algorithmic_bytes": 8 * N * (L + K + L) * 8}
 
     def e2e_step(self):

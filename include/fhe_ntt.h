@@ -252,7 +252,13 @@ int fhe_keyswitch_workspace_bytes(int log_n, int L, int K, int dnum, int batch, 
  * dnum <= 4, the column stages of the digits' NTT and one kernel that runs
  * their block stages and the inner product together (the transformed digits
  * never return to memory; 3 launches in all); otherwise the digits' NTT and
- * a separate inner-product kernel. */
+ * a separate inner-product kernel.
+ * For digits of at most 8 primes and n >= 128, ModUp's extension runs on the
+ * tensor cores (fp16 products of byte and 7-bit limbs, f32 sums, every sum an
+ * integer below 2^24, so the result is exact and identical to the integer
+ * path's): a kernel that gave up a bounded wait on them sets
+ * FHE_STATUS_TC_TIMEOUT in the device status word (fhe_device_status) and its
+ * outputs are invalid. */
 int fhe_keyswitch_ip(uint64_t *out, const uint64_t *in, size_t in_stride, const uint64_t *keys,
                      int log_n, int L, int K, int dnum, int batch, const fhe_ntt_tables *t_qp,
                      const void *modup, uint64_t *workspace, size_t ws_bytes, void *stream);
@@ -350,7 +356,10 @@ int fhe_bconv(uint64_t *out, const uint64_t *in, int log_n, int S, int T, int ba
  *   out_l = floor((X + h) / P) mod q_l,  h = (P-1)/2 (FHE_ROUND_NEAREST) or 0
  *   (FHE_ROUND_TRUNCATE).
  * Computed as (x_l - (((X + h) mod P) - h)) P^-1 mod q_l with (X + h) mod P
- * obtained exactly from the P residues by Garner's mixed radix. */
+ * obtained exactly from the P residues (Garner's mixed radix; in the NTT
+ * domain with K <= 8 and n >= 128 the same value from the CRT brackets and
+ * an exact correction count, extended on the tensor cores as in
+ * fhe_keyswitch_ip, with the same device status word). */
 
 /* Size of the constant blob for (L, K). */
 int fhe_moddown_tables_bytes(int L, int K, size_t *bytes);
