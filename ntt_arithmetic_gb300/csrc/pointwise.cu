@@ -31,7 +31,8 @@ k_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, long pairs, int log_n
     }
 }
 
-// d0 = a0 b0, d1 = a0 b1 + a1 b0, d2 = a1 b1 per batch item.
+// d0 = a0 b0, d1 = a0 b1 + a1 b0, d2 = a1 b1 per batch item; d1 by Karatsuba,
+// ((a0 + a1)(b0 + b1) - d0 - d2) mod q: three modular products instead of four.
 __global__ void __launch_bounds__(kThreads)
 k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
          const uint64_t *__restrict__ consts) {
@@ -47,22 +48,18 @@ k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_
         const long out_off = e + 2 * bi * plane;  // [batch][3][L][n]
         const uint64_t *kc = consts + l * K_COUNT;
         const uint64_t q = __ldg(kc + K_Q), mu = __ldg(kc + K_MU12);
-        const uint32_t c58 = (uint32_t)__ldg(kc + K_C58);
         const ulonglong2 a0 = __ldcs(reinterpret_cast<const ulonglong2 *>(a + in_off));
         const ulonglong2 a1 = __ldcs(reinterpret_cast<const ulonglong2 *>(a + in_off + plane));
         const ulonglong2 b0 = __ldcs(reinterpret_cast<const ulonglong2 *>(b + in_off));
         const ulonglong2 b1 = __ldcs(reinterpret_cast<const ulonglong2 *>(b + in_off + plane));
-        uint64_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
-        mac128(h0, l0, a0.x, b1.x);
-        mac128(h0, l0, a1.x, b0.x);
-        mac128(h1, l1, a0.y, b1.y);
-        mac128(h1, l1, a1.y, b0.y);
-        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off),
-               make_ulonglong2(mulmod(a0.x, b0.x, q, mu), mulmod(a0.y, b0.y, q, mu)));
-        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + plane),
-               make_ulonglong2(barrett_reduce128(h0, l0, q, mu, c58), barrett_reduce128(h1, l1, q, mu, c58)));
-        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + 2 * plane),
-               make_ulonglong2(mulmod(a1.x, b1.x, q, mu), mulmod(a1.y, b1.y, q, mu)));
+        const uint64_t d0x = mulmod(a0.x, b0.x, q, mu), d0y = mulmod(a0.y, b0.y, q, mu);
+        const uint64_t d2x = mulmod(a1.x, b1.x, q, mu), d2y = mulmod(a1.y, b1.y, q, mu);
+        const uint64_t sx = mulmod(csub(a0.x + a1.x, q), csub(b0.x + b1.x, q), q, mu);   // sums reduced below q
+        const uint64_t sy = mulmod(csub(a0.y + a1.y, q), csub(b0.y + b1.y, q), q, mu);
+        const uint64_t d1x = csub(sx + 2 * q - d0x - d2x, q), d1y = csub(sy + 2 * q - d0y - d2y, q);
+        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off), make_ulonglong2(d0x, d0y));
+        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + plane), make_ulonglong2(csub(d1x, q), csub(d1y, q)));
+        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + 2 * plane), make_ulonglong2(d2x, d2y));
     }
 }
 
