@@ -210,7 +210,7 @@ __device__ __forceinline__ void ext_tc(uint8_t *sm, uint64_t *__restrict__ out, 
         if constexpr (!MD) {
 #pragma unroll
             for (int a = 0; a < kTcMaxAlpha; a++)
-                if (a < cnt) __stcs(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
+                if (a < cnt) __stcg(dst + ((long)(lo + a) << log_n), x[a]);   // limbs of the digit are copies
         }
         // A operand row: fp16 1024 + byte, eight per digit (byte 7 of v_a < 2^50 is 0);
         // column 15 (byte 7 of v_1) carries 1024 + e
@@ -262,8 +262,8 @@ __device__ __forceinline__ void ext_tc(uint8_t *sm, uint64_t *__restrict__ out, 
                         const uint64_t h4 = (uint64_t)p67 * (1u << 14) + p45;   // d_4 + .. + d_7 2^21
                         const ModupTcTarget &tg = sT[g0 + tt + h];
                         const uint64_t r = reduce64_small_mu(l4 + (h4 << 28), tg.p, tg.mu);
-                        if constexpr (MD) __stcg(dst + ((long)tg.limb << log_n), hsrc ? r + tg.aux : r);
-                        else __stcs(dst + ((long)tg.limb << log_n), r);
+                        // L2 policy: the column stages of the forward NTT read these next
+                        __stcg(dst + ((long)tg.limb << log_n), MD && hsrc ? r + tg.aux : r);
                     }
                 }
             }
