@@ -176,7 +176,10 @@ int fhe_butterfly_probe(uint64_t *out, int ctas, int iters, const fhe_ntt_tables
  * context usable.  Waits for all work on the current device
  * (cudaDeviceSynchronize), then writes the word to *status and, if reset is
  * nonzero, clears it.  FHE_EINVAL for a null status, FHE_ECUDA if the
- * synchronization or the copy fails. */
+ * synchronization or the copy fails.
+ * For tests of that path: with FHE_TC_TEST_TIMEOUT=1 in the environment at
+ * launch time, the tensor-core kernels wait 1 ms on a barrier nothing
+ * arrives on and give up as above (their outputs are then invalid). */
 int fhe_device_status(int *status, int reset);
 
 /* ---- NTT-domain kernels ------------------------------------------------ */

@@ -22,6 +22,7 @@ FHE_DOMAIN_COEFF = 0
 FHE_DOMAIN_NTT = 1
 FHE_ROUND_TRUNCATE = 0
 FHE_ROUND_NEAREST = 1
+FHE_STATUS_TC_TIMEOUT = 1
 FHE_MODUP_EXACT = 0
 FHE_MODUP_APPROX = 1
 FHE_BCONV_EXACT = 0

@@ -49,6 +49,8 @@
 // chain of K = 64 (4 instructions) per group into the CTA's 128 TMEM columns.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "fhe_arith.cuh"
 #include "fhe_internal.h"
 #include "launch_util.h"
@@ -67,6 +69,7 @@ constexpr int kTileBytesA = 128 * kTcRowBytes;       // A operand, 16 KB
 constexpr uint32_t kCoreK = 128;                     // bytes between cores adjacent along K
 constexpr uint32_t kCoreRows = kTcMaxAlpha * 128;    // bytes between cores adjacent along the rows
 constexpr uint64_t kTcWaitNs = 200000000ull;         // give up an MMA wait after 200 ms
+constexpr uint64_t kTcTestWaitNs = 1000000ull;       // the test hook's wait on a barrier nobody arrives on
 constexpr uint32_t kF32Offset = 0x4B000000u;         // f32 bit pattern of 2^23
 
 // Shared memory of one CTA for a digit with T targets (padded to even).
@@ -88,9 +91,11 @@ __device__ __forceinline__ void ext_tc(uint8_t *sm, uint64_t *__restrict__ out, 
                                        const ulonglong2 *__restrict__ garner, int gstride,
                                        const ModupTcFrac *__restrict__ frac, const ModupTcTarget *__restrict__ tgt,
                                        const uint4 *__restrict__ wimg, const uint64_t *__restrict__ src_consts,
-                                       const uint64_t *__restrict__ hsrc) {
-    // qinv: the brackets' constants [cnt]; garner: [cnt][gstride] (the exact fallback)
-    __shared__ uint64_t mbar;
+                                       const uint64_t *__restrict__ hsrc, bool test_timeout) {
+    // qinv: the brackets' constants [cnt]; garner: [cnt][gstride] (the exact fallback).
+    // test_timeout: every MMA wait is on `idle`, a barrier nothing arrives on, for 1 ms -- the path of a
+    // wait that gives up, taken without any fault (the committed MMA still completes on `mbar`).
+    __shared__ uint64_t mbar, idle;
     __shared__ uint32_t tslot;
     const int t = threadIdx.x, warp = t >> 5;
     const int Tp = (T + 1) & ~1;
@@ -117,7 +122,10 @@ __device__ __forceinline__ void ext_tc(uint8_t *sm, uint64_t *__restrict__ out, 
         if (t <= kTcMaxAlpha) sF[t] = frac[t];
     }
     if (warp == 0) tmem_alloc(&tslot, 128);
-    if (t == 0) mbar_init(&mbar, 1);
+    if (t == 0) {
+        mbar_init(&mbar, 1);
+        mbar_init(&idle, 1);
+    }
     fence_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -240,7 +248,7 @@ __device__ __forceinline__ void ext_tc(uint8_t *sm, uint64_t *__restrict__ out, 
                                idesc, ks > 0);
                 tc_commit(&mbar);
             }
-            const bool done = mbar_wait(&mbar, phase, kTcWaitNs);
+            const bool done = test_timeout ? mbar_wait(&idle, 0, kTcTestWaitNs) : mbar_wait(&mbar, phase, kTcWaitNs);
             phase ^= 1;
             ok = __syncthreads_and(done);
             if (!ok) break;
@@ -287,7 +295,7 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
            int alpha, const ModupDigit *__restrict__ dg, const ulonglong2 *__restrict__ qinv,
            const ulonglong2 *__restrict__ garner, const ModupTcFrac *__restrict__ frac,
            const ModupTcTarget *__restrict__ tgt, const uint4 *__restrict__ wimg, int tmax,
-           const uint64_t *__restrict__ consts) {
+           const uint64_t *__restrict__ consts, int test_timeout) {
     pdl_begin();
     extern __shared__ __align__(1024) uint8_t sm[];   // [A operand][B operand][targets]
     const int j = blockIdx.y;
@@ -295,7 +303,7 @@ k_modup_tc(uint64_t *__restrict__ ext, const uint64_t *__restrict__ in, long in_
     ext_tc<APPROX, false>(sm, ext, LK, in, in_stride, log_n, batch, lo, cnt, LK - cnt, j, gridDim.y,
                           qinv + (long)j * alpha, garner + (long)j * alpha * alpha, alpha,
                           frac + (long)j * (kTcMaxAlpha + 1), tgt + (long)j * tmax,
-                          wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16, consts, nullptr);
+                          wimg + (size_t)j * tmax * 8 * kTcRowBytes / 16, consts, nullptr, test_timeout != 0);
 }
 
 // ModDown's conversion d_l = ((X + h) mod P) - h mod q_l (below 3 q_l, for the
@@ -304,11 +312,19 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 k_moddown_tc(uint64_t *__restrict__ d, const uint64_t *__restrict__ in, long in_stride, int log_n, int L, int K,
              int batch, const ulonglong2 *__restrict__ qinv, const ulonglong2 *__restrict__ garner,
              const ModupTcFrac *__restrict__ frac, const ModupTcTarget *__restrict__ tgt,
-             const uint4 *__restrict__ wimg, const uint64_t *__restrict__ consts_p, const uint64_t *__restrict__ hp) {
+             const uint4 *__restrict__ wimg, const uint64_t *__restrict__ consts_p, const uint64_t *__restrict__ hp,
+             int test_timeout) {
     pdl_begin();
     extern __shared__ __align__(1024) uint8_t sm[];
     ext_tc<false, true>(sm, d, L, in, in_stride, log_n, batch, 0, K, L, 0, 1, qinv, garner, K, frac, tgt, wimg,
-                        consts_p, hp);
+                        consts_p, hp, test_timeout != 0);
+}
+
+// The test hook: FHE_TC_TEST_TIMEOUT=1 in the environment makes the tensor-core
+// kernels take their give-up path (see ext_tc).
+int tc_test_timeout() {
+    const char *v = getenv("FHE_TC_TEST_TIMEOUT");
+    return v && v[0] == '1' && v[1] == 0;
 }
 
 }  // namespace
@@ -336,7 +352,7 @@ int launch_modup_tc(uint64_t *ext, const uint64_t *in, long in_stride, int log_n
         ext, in, in_stride, log_n, LK, batch, lay.alpha, (const ModupDigit *)(base + lay.off_digits),
         (const ulonglong2 *)(base + lay.off_qinv), (const ulonglong2 *)(base + lay.off_garner),
         (const ModupTcFrac *)(base + lay.off_tc_frac), (const ModupTcTarget *)(base + lay.off_tc_tgt),
-        (const uint4 *)(base + lay.off_tc_b), lay.tc_tmax, t->consts);
+        (const uint4 *)(base + lay.off_tc_b), lay.tc_tmax, t->consts, tc_test_timeout());
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -358,7 +374,7 @@ int launch_moddown_tc(uint64_t *d, const uint64_t *src, long src_item, int log_n
                (const ulonglong2 *)(base + lay.off_tc_qinv), (const ulonglong2 *)(base + lay.off_garner),
                (const ModupTcFrac *)(base + lay.off_tc_frac), (const ModupTcTarget *)(base + lay.off_tc_tgt),
                (const uint4 *)(base + lay.off_tc_b), t_qp->consts + (long)L * K_COUNT,
-               nearest ? (const uint64_t *)(base + lay.off_hp) : (const uint64_t *)nullptr);
+               nearest ? (const uint64_t *)(base + lay.off_hp) : (const uint64_t *)nullptr, tc_test_timeout());
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

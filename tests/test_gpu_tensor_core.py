@@ -98,3 +98,33 @@ def test_moddown_ntt_small_coefficients(g, nearest, mix):
     g.api.moddown(out, g.dev(x), L, K, t, md, domain="ntt", nearest=nearest)
     assert np.array_equal(g.host(out), oracle.moddown_ntt_batch(x, qp, ps, L, K, nearest))
     assert g.api.device_status() == 0
+
+
+def test_tensor_core_wait_gives_up_without_fault(g, monkeypatch):
+    """The bounded-wait path, taken on purpose: with FHE_TC_TEST_TIMEOUT=1 the tensor-core kernels wait
+    for 1 ms on a barrier nothing arrives on, give up, set FHE_STATUS_TC_TIMEOUT, let their committed MMA
+    finish, free their tensor memory and return.  The status word reports it, and the same context then
+    computes the exact result again."""
+    import torch
+    log_n, L, K, dnum, batch = 12, 24, 8, 3, 1
+    n = 1 << log_n
+    qp = g.qp_basis(log_n, L, K)
+    t = g.tables(log_n, tuple(qp))
+    mt = g.api.ModupTables(L, K, dnum, qp)
+    md = g.api.ModdownTables(L, K, qp)
+    x = inputs.uniform_residues((batch, L, n), qp[:L], 91, buffer=0)
+    keys = inputs.uniform_residues((dnum, 2, L + K, n), qp, 91, buffer=1)
+    dx, dk = g.dev(x), g.dev(keys)
+    out = torch.empty((batch, 2, L + K, n), dtype=torch.uint64, device="cuda")
+    down = torch.empty((2 * batch, L, n), dtype=torch.uint64, device="cuda")
+    assert g.api.device_status() == 0
+    monkeypatch.setenv("FHE_TC_TEST_TIMEOUT", "1")
+    g.api.keyswitch_ip(out, dx, dk, L, K, dnum, t, mt)
+    assert g.api.device_status() == g.api.N.FHE_STATUS_TC_TIMEOUT     # read and cleared
+    g.api.moddown(down, out.view(2 * batch, L + K, n), L, K, t, md, domain="ntt")
+    assert g.api.device_status() == g.api.N.FHE_STATUS_TC_TIMEOUT
+    monkeypatch.delenv("FHE_TC_TEST_TIMEOUT")
+    g.api.keyswitch_ip(out, dx, dk, L, K, dnum, t, mt)
+    want = oracle.keyswitch_batch(x, keys, qp, oracle.psis(qp, n), L, K, dnum)
+    assert np.array_equal(g.host(out), want)
+    assert g.api.device_status() == 0
