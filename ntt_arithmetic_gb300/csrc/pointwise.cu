@@ -16,23 +16,29 @@ namespace {
 constexpr int kThreads = 256;
 
 // out = a * b mod q_l over [rows][n], rows = batch * L; processed in pairs.
+// The grid walks the pairs from the end (the kernel before it in a step
+// finished there, so the first reads find L2) and stores with the L2 policy
+// (the next kernel reads this output).
 __global__ void __launch_bounds__(kThreads)
 k_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
       const uint64_t *__restrict__ consts) {
     pdl_begin();
     const long stride = (long)gridDim.x * blockDim.x;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+    for (long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x; i0 < pairs; i0 += stride) {
+        const long i = pairs - 1 - i0;
         const long e = 2 * i;
         const int l = (int)((uint32_t)(e >> log_n) % (uint32_t)L);
         const uint64_t q = __ldg(consts + l * K_COUNT + K_Q), mu = __ldg(consts + l * K_COUNT + K_MU12);
         const ulonglong2 va = __ldcs(reinterpret_cast<const ulonglong2 *>(a + e));
         const ulonglong2 vb = __ldcs(reinterpret_cast<const ulonglong2 *>(b + e));
-        __stcs(reinterpret_cast<ulonglong2 *>(out + e), make_ulonglong2(mulmod(va.x, vb.x, q, mu), mulmod(va.y, vb.y, q, mu)));
+        __stcg(reinterpret_cast<ulonglong2 *>(out + e), make_ulonglong2(mulmod(va.x, vb.x, q, mu), mulmod(va.y, vb.y, q, mu)));
     }
 }
 
 // d0 = a0 b0, d1 = a0 b1 + a1 b0, d2 = a1 b1 per batch item; d1 by Karatsuba,
 // ((a0 + a1)(b0 + b1) - d0 - d2) mod q: three modular products instead of four.
+// Stored with the L2 policy: the inverse NTT's block kernel reads the rows
+// written last first.
 __global__ void __launch_bounds__(kThreads)
 k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_n, int L,
          const uint64_t *__restrict__ consts) {
@@ -57,9 +63,9 @@ k_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, long pairs, int log_
         const uint64_t sx = mulmod(csub(a0.x + a1.x, q), csub(b0.x + b1.x, q), q, mu);   // sums reduced below q
         const uint64_t sy = mulmod(csub(a0.y + a1.y, q), csub(b0.y + b1.y, q), q, mu);
         const uint64_t d1x = csub(sx + 2 * q - d0x - d2x, q), d1y = csub(sy + 2 * q - d0y - d2y, q);
-        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off), make_ulonglong2(d0x, d0y));
-        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + plane), make_ulonglong2(csub(d1x, q), csub(d1y, q)));
-        __stcs(reinterpret_cast<ulonglong2 *>(d + out_off + 2 * plane), make_ulonglong2(d2x, d2y));
+        __stcg(reinterpret_cast<ulonglong2 *>(d + out_off), make_ulonglong2(d0x, d0y));
+        __stcg(reinterpret_cast<ulonglong2 *>(d + out_off + plane), make_ulonglong2(csub(d1x, q), csub(d1y, q)));
+        __stcg(reinterpret_cast<ulonglong2 *>(d + out_off + 2 * plane), make_ulonglong2(d2x, d2y));
     }
 }
 
