@@ -128,3 +128,29 @@ def test_tensor_core_wait_gives_up_without_fault(g, monkeypatch):
     want = oracle.keyswitch_batch(x, keys, qp, oracle.psis(qp, n), L, K, dnum)
     assert np.array_equal(g.host(out), want)
     assert g.api.device_status() == 0
+
+
+@pytest.mark.parametrize("log_n", [7, 8, 9])
+def test_tensor_core_smallest_rings(g, log_n):
+    """The tensor-core kernels from their smallest ring (n = 128: one tile per item, a grid of a few CTAs):
+    key switch (exact and approximate) and NTT-domain ModDown against the oracle."""
+    import torch
+    L, K, dnum, batch = 5, 2, 2, 3
+    n = 1 << log_n
+    qp = g.qp_basis(log_n, L, K)
+    t = g.tables(log_n, tuple(qp))
+    mt = g.api.ModupTables(L, K, dnum, qp)
+    md = g.api.ModdownTables(L, K, qp)
+    ps = oracle.psis(qp, n)
+    x = small_signed((batch, L, n), qp[:L], 95 + log_n, bound=1 << 30, mix=True)
+    keys = inputs.uniform_residues((dnum, 2, L + K, n), qp, 96 + log_n, buffer=1)
+    out = torch.empty((batch, 2, L + K, n), dtype=torch.uint64, device="cuda")
+    for approx in (False, True):
+        g.api.keyswitch_ip(out, g.dev(x), g.dev(keys), L, K, dnum, t, mt, approx=approx)
+        assert np.array_equal(g.host(out), oracle.keyswitch_batch(x, keys, qp, ps, L, K, dnum, approx=approx))
+    xs = inputs.uniform_residues((batch, L + K, n), qp, 97 + log_n)
+    down = torch.empty((batch, L, n), dtype=torch.uint64, device="cuda")
+    for nearest in (True, False):
+        g.api.moddown(down, g.dev(xs), L, K, t, md, domain="ntt", nearest=nearest)
+        assert np.array_equal(g.host(down), oracle.moddown_ntt_batch(xs, qp, ps, L, K, nearest))
+    assert g.api.device_status() == 0
