@@ -27,7 +27,13 @@ namespace fhe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSmemBudget = 32 * 1024;   // staged digit blocks per CTA
+// Staged digit blocks per CTA and the largest output block: 2^11 positions
+// for dnum <= 3 (48 KB at dnum = 3, 4 CTAs per SM).  Measured at n = 2^16,
+// dnum = 3, 16 rotations: blocks of 2^11 with 256 threads 462 us, 2^9 with
+// 128 threads 464 us, 2^10 with 256 or 128 threads 503 / 507 us, 2^8 or 2^9
+// with one pair per thread 542 / 581 us, 512-thread CTAs 929 us.
+constexpr int kSmemBudget = 48 * 1024;
+constexpr int kMaxLogBlock = 11;
 
 __device__ __forceinline__ uint32_t brv_bits(uint32_t x, int bits) { return __brev(x) >> (32 - bits); }
 
@@ -131,7 +137,7 @@ k_ks_ip_aut(uint64_t *__restrict__ out, const uint64_t *__restrict__ ext, const 
 int launch_ks_ip_aut(uint64_t *out, const uint64_t *ext, const uint64_t *keys, int log_n, int LK, int dnum,
                      int batch, int R, const GaloisSet &g, const fhe_ntt_tables *t, void *stream) {
     // largest block with dnum staged rows within the shared-memory budget
-    int lb = log_n < 10 ? log_n : 10;
+    int lb = log_n < kMaxLogBlock ? log_n : kMaxLogBlock;
     while (lb > 1 && ((size_t)dnum << lb) * 8 > (size_t)kSmemBudget) lb--;
     const long blocks = (long)LK * R << (log_n - lb);
     const size_t smem = ((size_t)dnum << lb) * 8;
