@@ -146,10 +146,30 @@ int launch_mul(uint64_t *out, const uint64_t *a, const uint64_t *b, int log_n, i
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
+// The tensor product's grid: two whole rounds of its resident CTAs per SM.
+// At 48 registers 5 CTAs of 256 threads are resident; a grid of 8 per SM left
+// a partial second round (the 2100-prime chain's tensor product 9 us slower
+// per step, measured against 5 and 10 per SM).
+static int tensor_ctas_per_sm() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+    if (cache[dev] == 0) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_tensor, kThreads, 0) != cudaSuccess || nb <= 0) {
+            cudaGetLastError();
+            nb = 4;
+        }
+        cache[dev] = 2 * nb;
+    }
+    return cache[dev];
+}
+
 int launch_tensor(uint64_t *d, const uint64_t *a, const uint64_t *b, int log_n, int L, int batch,
                   const fhe_ntt_tables *t, void *stream) {
     const long pairs = ((long)batch * L << log_n) / 2;
-    k_tensor<<<stream_grid(pairs, kThreads, 8), kThreads, 0, (cudaStream_t)stream>>>(d, a, b, pairs, log_n, L, t->consts);
+    k_tensor<<<stream_grid(pairs, kThreads, tensor_ctas_per_sm()), kThreads, 0, (cudaStream_t)stream>>>(
+        d, a, b, pairs, log_n, L, t->consts);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
